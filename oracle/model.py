@@ -1,0 +1,178 @@
+"""Decoder step of the oracle, composed from oracle.c's primitives.
+
+TEST INFRASTRUCTURE ONLY.  The step follows the Llama-style transformer that
+gpt-fast's model definition serves (gpt-fast README, "Supported models" and
+"Generate text"; Mixtral in "Efficiently implementing the Mixtral 8x7B model
+with gpt-fast"): embed -> per layer (RMSNorm, q/k/v, RoPE, KV append,
+attention, o, residual, RMSNorm, SwiGLU FFN or top-2 MoE, residual) ->
+RMSNorm -> lm_head -> fp32 logits -> greedy argmax.
+
+READING of the rounding points (the pages give none): the residual stream is
+kept at full precision (fp64 here, fp32 on the GPU); every linear output, q,
+k, v (and so the KV cache), the attention output, the SwiGLU product and the
+MoE combination are rounded to bf16; logits are not rounded.  Speculative
+verification (gpt-fast README, "Speculative sampling") accepts the longest
+prefix of draft tokens that equals the target's own greedy choices.
+"""
+import numpy as np
+
+from . import (BF16, INT4, INT8, argmax, attention, bf16_to_double, linear, quant_w4g,
+               quant_w8, rmsnorm, rope, round_bf16, swiglu)
+
+
+class _Mat:
+    """One weight matrix as the method stores it: bf16, int8 + s, int4 + s + z."""
+
+    def __init__(self, dt, W):
+        self.dt = dt
+        self.N, self.K = W.shape
+        if dt == BF16:
+            self.w, self.s, self.z = W, None, None
+        elif dt == INT8:
+            self.w, self.s = quant_w8(W)
+            self.z = None
+        else:
+            self.w, self.s, self.z = quant_w4g(W, 32)
+
+    def __call__(self, X):
+        return linear(self.dt, self.w, self.s, self.z, X)
+
+
+class OracleModel:
+    """fp64 decoder.  `weights` is a synth.models.WeightCache-like object
+    (`.glob`, `.layer(l)`).  Quantised layers are kept when `keep` is set."""
+
+    def __init__(self, cfg, dtype, weights, tmax, keep=True):
+        self.cfg, self.weights, self.keep = cfg, weights, keep
+        self.dt = {"bf16": BF16, "int8": INT8, "int4": INT4}[dtype] if isinstance(dtype, str) else dtype
+        self.tmax = tmax
+        c = cfg
+        self.K = [np.zeros((c["n_kv_heads"], tmax, c["head_dim"])) for _ in range(c["n_layers"])]
+        self.V = [np.zeros((c["n_kv_heads"], tmax, c["head_dim"])) for _ in range(c["n_layers"])]
+        self._layers = {}
+        g = weights.glob
+        self.embed = g["embed"]
+        self.g_final = g["g_final"]
+        self.lm_head = _Mat(self.dt, g["lm_head"])
+
+    def _layer(self, l):
+        if l in self._layers:
+            return self._layers[l]
+        w = self.weights.layer(l)
+        L = {"wq": _Mat(self.dt, w["wq"]), "wk": _Mat(self.dt, w["wk"]),
+             "wv": _Mat(self.dt, w["wv"]), "wo": _Mat(self.dt, w["wo"]),
+             "g_attn": w["g_attn"], "g_ffn": w["g_ffn"]}
+        if "experts" in w:
+            # The router stays bf16: the pages quantise linear weights, and a
+            # gate of 8 outputs carries no measurable bytes (READING).
+            L["router"] = _Mat(BF16, w["router"])
+            L["experts"] = [{k: _Mat(self.dt, e[k]) for k in ("wg", "wu", "wd")}
+                            for e in w["experts"]]
+        else:
+            for k in ("wg", "wu", "wd"):
+                L[k] = _Mat(self.dt, w[k])
+        if self.keep:
+            self._layers[l] = L
+        return L
+
+    # -- one layer over T consecutive tokens at positions pos0..pos0+T-1 ------
+    def _attn_block(self, l, L, X, pos0):
+        c = self.cfg
+        T = X.shape[0]
+        hd, Hq, Hkv = c["head_dim"], c["n_heads"], c["n_kv_heads"]
+        Nrm = np.stack([rmsnorm(X[t], L["g_attn"], c["eps"]) for t in range(T)])
+        Q = round_bf16(L["wq"](Nrm))
+        Kn = round_bf16(L["wk"](Nrm))
+        Vn = round_bf16(L["wv"](Nrm))
+        A = np.empty((T, Hq * hd))
+        for t in range(T):
+            p = pos0 + t
+            q = rope(Q[t], Hq, hd, p, c["theta"]).reshape(Hq, hd)
+            k = rope(Kn[t], Hkv, hd, p, c["theta"]).reshape(Hkv, hd)
+            self.K[l][:, p, :] = k
+            self.V[l][:, p, :] = Vn[t].reshape(Hkv, hd)
+            A[t] = attention(q, self.K[l][:, :p + 1, :], self.V[l][:, :p + 1, :]).reshape(-1)
+        A = round_bf16(A)
+        return X + round_bf16(L["wo"](A))
+
+    def _ffn_dense(self, L, M):
+        G = round_bf16(L["wg"](M))
+        U = round_bf16(L["wu"](M))
+        H = np.stack([swiglu(G[t], U[t]) for t in range(M.shape[0])])
+        return round_bf16(L["wd"](H))
+
+    def route(self, L, m):
+        """Top-2 of the router logits (lower index first on ties) and the
+        softmax over the two chosen logits."""
+        r = L["router"](m)
+        e1 = argmax(r)
+        r2 = r.copy()
+        r2[e1] = -np.inf
+        e2 = argmax(r2)
+        a, b = r[e1], r[e2]
+        mx = max(a, b)
+        wa, wb = np.exp(a - mx), np.exp(b - mx)
+        return (e1, e2), (wa / (wa + wb), wb / (wa + wb)), r
+
+    def _ffn_moe(self, L, M):
+        out = np.empty_like(M)
+        for t in range(M.shape[0]):
+            (e1, e2), (w1, w2), _ = self.route(L, M[t])
+            acc = 0.0
+            for e, w in ((e1, w1), (e2, w2)):
+                E = L["experts"][e]
+                g = round_bf16(E["wg"](M[t]))
+                u = round_bf16(E["wu"](M[t]))
+                y = round_bf16(E["wd"](swiglu(g, u)))
+                acc = acc + w * y
+            out[t] = round_bf16(acc)
+        return out
+
+    def layer_forward(self, l, X, pos0):
+        c = self.cfg
+        L = self._layer(l)
+        H = self._attn_block(l, L, X, pos0)
+        M = np.stack([rmsnorm(H[t], L["g_ffn"], c["eps"]) for t in range(H.shape[0])])
+        F = self._ffn_moe(L, M) if "experts" in L else self._ffn_dense(L, M)
+        return H + F
+
+    def forward(self, tokens, pos0):
+        """Teacher-forced forward of tokens at positions pos0.. (layer-major,
+        which equals token-by-token decoding).  Returns fp64 logits [T, V]."""
+        tokens = np.asarray(tokens, dtype=np.int64).reshape(-1)
+        X = bf16_to_double(self.embed[tokens])
+        for l in range(self.cfg["n_layers"]):
+            X = self.layer_forward(l, X, pos0)
+        Nrm = np.stack([rmsnorm(X[t], self.g_final, self.cfg["eps"]) for t in range(X.shape[0])])
+        return self.lm_head(Nrm)
+
+    def greedy(self, prompt, n_new):
+        """Prompt fed one token per step, then n_new greedy tokens.  Returns
+        (generated tokens, logits of every step)."""
+        logits_all, out = [], []
+        pos = 0
+        tok = None
+        for t in list(prompt):
+            lg = self.forward([t], pos)[0]
+            logits_all.append(lg)
+            pos += 1
+        tok = argmax(logits_all[-1])
+        for _ in range(n_new):
+            out.append(tok)
+            lg = self.forward([tok], pos)[0]
+            logits_all.append(lg)
+            pos += 1
+            tok = argmax(lg)
+        return out, np.stack(logits_all)
+
+    def verify(self, last_token, drafts, pos):
+        """Feed [last_token, d1..dk] at positions pos..pos+k; a_i = argmax of
+        row i; accept n = the largest n with a_{i-1} == d_i for all i <= n;
+        the next token is a_n.  Returns (n, next token, logits [k+1, V])."""
+        seq = [int(last_token)] + [int(d) for d in drafts]
+        logits = self.forward(seq, pos)
+        a = [argmax(row) for row in logits]
+        n = 0
+        while n < len(drafts) and a[n] == int(drafts[n]):
+            n += 1
+        return n, a[n], logits
