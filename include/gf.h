@@ -1,0 +1,210 @@
+/*
+ * gf.h — C-ABI of libgf, a GB300 (sm_103a) engine for the batch-size-1
+ * decode step of Llama-style transformers with bf16, int8 weight-only and
+ * int4 group-32 weight-only linear layers (the workload of the gpt-fast
+ * README, sections "Benchmarks" and "Quantization").
+ *
+ * Conventions for every call below:
+ *  - Return value: 0 (GF_OK) or a gf_status code; gf_last_error() returns a
+ *    message for the calling thread.  Arguments are checked on the host before
+ *    anything is launched; a failed check launches nothing.
+ *  - Tensor pointers are DEVICE pointers owned by the caller, 16-byte aligned
+ *    (GF_EALIGN otherwise).  The library keeps no reference to them after the
+ *    call returns, except for gf_model / gf_kv handles, which the library owns
+ *    and which are freed with gf_model_destroy / gf_kv_destroy.
+ *  - bf16 is the upper half of an IEEE binary32 (round-to-nearest-even on
+ *    conversion), passed as 16-bit words.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous on that stream unless stated; errors raised inside a kernel
+ *    (a bounded wait that gave up) are reported by gf_device_error().
+ *  - K must be a multiple of 8 (bf16), 16 (int8) or 32 (int4 G=32), and at
+ *    most GF_KMAX; otherwise GF_EINVAL.
+ */
+#ifndef GF_H_
+#define GF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GF_OK = 0,
+  GF_EINVAL = 1,        /* bad size, dtype or null pointer */
+  GF_EALIGN = 2,        /* pointer not 16-byte aligned */
+  GF_ECUDA = 3,         /* a CUDA runtime call failed */
+  GF_ENOMEM = 4,        /* device allocation failed (model / kv creation only) */
+  GF_EUNSUPPORTED = 5,  /* shape outside what the kernels handle */
+  GF_EDEVICE = 6        /* a kernel gave up a bounded wait (see gf_device_error) */
+} gf_status;
+
+typedef enum { GF_W_BF16 = 0, GF_W_INT8 = 1, GF_W_INT4G32 = 2 } gf_wdtype;
+typedef enum { GF_Y_BF16 = 0, GF_Y_F32 = 1 } gf_ydtype;
+
+#define GF_KMAX 14336
+#define GF_TILE_ROWS 32
+
+typedef void* gf_stream; /* cudaStream_t */
+
+const char* gf_last_error(void);
+int gf_version(void);
+
+/* Size in bytes of a packed weight buffer for an N x K matrix of `wdtype`
+ * (the device tile layout below), or -1 for a bad argument. */
+long long gf_packed_bytes(int wdtype, int N, int K);
+
+/*
+ * Packed tile layout (the "offline weight repack into a 128-bit-vectorised,
+ * coalesced tile layout").  A chunk is 16 bytes of one row: 8 bf16, 16 int8
+ * or 32 int4 weights, C = K / (weights per chunk) chunks per row.  Rows are
+ * grouped in tiles of GF_TILE_ROWS (the last tile may hold fewer, Rt), tiles
+ * are stored one after another, and inside a tile K-blocks of up to 32 chunks
+ * (Lb chunks; only the last block of a row may be narrower) one after
+ * another.  A block holds its Rt x Lb chunks row-major (chunk (r, l) at byte
+ * 16 (r Lb + l)); for int4 it is followed by Rt x Lb 32-bit words s | z << 16
+ * (the bf16 scale and zero of chunk (r, l)'s group) padded with zeros to a
+ * multiple of 16 bytes.  Inside an int8 / int4 chunk, 32-bit word j is the
+ * natural little-endian word (int8 code 4j+i in bits 8i..8i+7; int4 code
+ * 8j+i in bits 4i..4i+3) rotated left by 15 bits.  bf16 chunks are natural.
+ */
+
+/* int8 weight-only quantisation (gpt-fast README, "Int8 weight-only
+ * quantization"): per output row n, s_n = bf16(max_k |W[n,k]| / 127) (fp32
+ * divide) and q = clamp(rint(W / s_n), -127, 127) (fp32 divide, ties to
+ * even); an all-zero row gets s = 0, q = 0.
+ * W: bf16 [N][K] row-major.  packed: gf_packed_bytes(GF_W_INT8, N, K) bytes
+ * in the tile layout.  s: bf16 [N]. */
+int gf_quantize_w8(const void* W, int N, int K, void* packed, void* s, gf_stream stream);
+
+/* int4 weight-only grouped quantisation, group G = 32 along K (gpt-fast
+ * README, "Int4 weight-only quantization", --groupsize 32): per row and group
+ * z = min (bf16, exact), s = bf16((max - min) / 15) (fp32 subtract and
+ * divide), q = clamp(rint((W - min) / s), 0, 15) (fp32); s == 0 gives q = 0.
+ * The dequantised weight is q s + z.  packed receives codes, s and z in the
+ * tile layout.  G must be 32. */
+int gf_quantize_w4g(const void* W, int N, int K, int G, void* packed, gf_stream stream);
+
+/* bf16 weights into the tile layout (no arithmetic). */
+int gf_repack_bf16(const void* W, int N, int K, void* packed, gf_stream stream);
+
+/* Inverses of the above, for bit-exact checks: packed -> logical.
+ * gf_unpack_w8: q int8 [N][K].  gf_unpack_w4g: q uint8 [N][K] (one code per
+ * byte), s, z bf16 [N][K/32].  gf_unpack_bf16: W bf16 [N][K]. */
+int gf_unpack_w8(const void* packed, int N, int K, void* q, gf_stream stream);
+int gf_unpack_w4g(const void* packed, int N, int K, int G, void* q, void* s, void* z,
+                  gf_stream stream);
+int gf_unpack_bf16(const void* packed, int N, int K, void* W, gf_stream stream);
+
+/* Matrix-vector products y = x W^T of the pages' linear layers at batch
+ * size 1: y[n] = sum_k x[k] What[n,k], fp32 accumulation, What = W (bf16),
+ * q s_n (int8) or q s + z (int4 G=32).  x: bf16 [K].  y: [N] bf16 (rounded to
+ * nearest even) or fp32, by ydtype.  Weights stream through shared memory by
+ * bulk asynchronous copies; codes are dequantised in registers. */
+int gf_gemv_bf16(const void* x, const void* Wpacked, int N, int K, void* y, int ydtype,
+                 gf_stream stream);
+int gf_gemv_w8(const void* x, const void* qpacked, const void* s, int N, int K, void* y,
+               int ydtype, gf_stream stream);
+int gf_gemv_w4g(const void* x, const void* qpacked, int N, int K, int G, void* y, int ydtype,
+                gf_stream stream);
+
+/* Single-query attention of the decode step (the KV-cache attention the
+ * gpt-fast model runs at every generated token): for each of Hq heads,
+ * o_h = sum_t p_t v_t over positions t = 0..pos (inclusive), p = softmax of
+ * q_h . k_t / sqrt(hd), kv head = h / (Hq / Hkv).  q: bf16 [Hq][hd];
+ * kcache, vcache: bf16 [Hkv][Tmax][hd]; out: bf16 [Hq][hd].  The position
+ * range is split across CTAs and merged with a log-sum-exp combine; the
+ * caller provides `ws` of at least gf_attn_workspace_bytes() bytes (scratch,
+ * contents undefined after the call).  hd must be 64 or 128, Hq % Hkv == 0,
+ * Hq / Hkv <= 8, 0 <= pos < Tmax. */
+size_t gf_attn_workspace_bytes(int Hq, int Hkv, int hd);
+int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq, int Hkv, int hd,
+                   int Tmax, int pos, void* out, void* ws, size_t ws_bytes, gf_stream stream);
+
+/* ------------------------------------------------------ decode step ---- */
+typedef struct {
+  int d;           /* model width */
+  int n_layers;
+  int n_heads;     /* query heads */
+  int n_kv_heads;  /* key/value heads (grouped-query when < n_heads) */
+  int head_dim;    /* 64 or 128 */
+  int ffn;         /* SwiGLU hidden width (per expert for MoE) */
+  int vocab;
+  int n_experts;   /* 0 = dense FFN; else a top-2 mixture of experts */
+  float eps;       /* RMSNorm epsilon */
+  double theta;    /* RoPE base */
+} gf_model_config;
+
+/* Weights as bf16 device arrays owned by the caller (read during
+ * gf_model_create only).  Per-layer entries are arrays of n_layers pointers
+ * (MoE expert entries: n_layers * n_experts, layer-major).
+ *  wqkv  [(Hq + 2 Hkv) hd][d]: rows of Wq, then Wk, then Wv
+ *  wo    [d][Hq hd]
+ *  wgu   [2 ffn][d]: row 2j = gate row j, row 2j+1 = up row j
+ *  wd    [d][ffn]
+ *  router [n_experts][d] (MoE only; kept bf16) */
+typedef struct {
+  const void* embed;    /* [vocab][d], kept bf16 */
+  const void* g_final;  /* [d] */
+  const void* lm_head;  /* [vocab][d] */
+  const void* const* wqkv;
+  const void* const* wo;
+  const void* const* wgu;
+  const void* const* wd;
+  const void* const* g_attn;
+  const void* const* g_ffn;
+  const void* const* router;
+} gf_weights;
+
+typedef struct gf_model gf_model;
+typedef struct gf_kv gf_kv;
+
+/* Quantises (or repacks) every linear weight, lm_head included, into
+ * library-owned device buffers.  Synchronous.  GF_ENOMEM if they do not fit. */
+int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w, gf_model** out);
+int gf_model_destroy(gf_model* m);
+/* Bytes the model streams per token: linear weights + scales + norm gains +
+ * one embedding row (the KV bytes depend on the position and are added by
+ * the caller: 2 n_layers Hkv hd 2 (pos+1)). */
+long long gf_model_weight_bytes(const gf_model* m);
+
+/* KV cache (bf16 [layer][Hkv][Tmax][hd] for K and for V), RoPE table,
+ * scratch and the decode program, for contexts of up to Tmax positions. */
+int gf_kv_create(gf_model* m, int Tmax, gf_kv** out);
+int gf_kv_destroy(gf_kv* kv);
+/* Device pointers of the K and V caches (for tests that pre-fill them). */
+int gf_kv_cache_ptrs(gf_kv* kv, void** kcache, void** vcache);
+
+/* One decode step at position *d_pos (device int32): embeds *d_token, runs
+ * every layer (RMSNorm, q/k/v, RoPE, KV append, attention, o, residual,
+ * RMSNorm, SwiGLU or top-2 MoE, residual), the final RMSNorm and lm_head,
+ * writes fp32 logits [vocab] to d_logits and their argmax (lowest index on
+ * ties) to *d_argmax, then advances *d_pos by one.  One kernel launch on
+ * every SM; nothing is copied to the host. */
+int gf_decode_step(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t* d_pos,
+                   float* d_logits, int32_t* d_argmax, gf_stream stream);
+
+/* Speculative verification (gpt-fast README, "Speculative sampling"):
+ * d_tokens holds k+1 ids [last accepted token, draft_1 .. draft_k], fed at
+ * positions *d_pos .. *d_pos + k in one pass.  With a_i the argmax of row i,
+ * n = the largest n <= k with a_{i-1} == draft_i for all i <= n is written to
+ * *d_n_accepted, a_n to *d_next_token, and *d_pos advances by n + 1.  KV rows
+ * of all k+1 positions are written (rows past the accepted ones are
+ * overwritten by later steps).  d_logits, if not NULL, receives the fp32
+ * logits [k+1][vocab].  1 <= k+1 <= 8. */
+int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t* d_pos,
+                int32_t* d_n_accepted, int32_t* d_next_token, float* d_logits, gf_stream stream);
+
+/* Reads and clears the device error word of the engine (0 = none; otherwise
+ * a code naming the wait that gave up).  Synchronises the device. */
+int gf_device_error(void);
+
+/* Device-to-device copy at full bandwidth (16-byte vector loads and stores),
+ * used as the measured HBM ceiling.  bytes % 16 == 0. */
+int gf_copy_ceiling(const void* src, void* dst, size_t bytes, gf_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

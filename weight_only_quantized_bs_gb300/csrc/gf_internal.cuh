@@ -1,0 +1,155 @@
+// gf_internal.cuh — shared definitions of the sm_103a engine: tile layout
+// arithmetic, PTX wrappers (mbarrier, bulk asynchronous copy, acquire/release
+// loads), the phase program executed by the persistent kernel, and host-side
+// error helpers.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gf.h"
+
+namespace gf {
+
+// ------------------------------------------------------------- layout ----
+constexpr int TR = GF_TILE_ROWS;  // rows per tile
+constexpr int KBLK = 32;          // chunks per K-block (one per lane)
+constexpr int KMAX = GF_KMAX;
+enum { DT_BF16 = 0, DT_INT8 = 1, DT_INT4 = 2 };
+
+__host__ __device__ inline int per_chunk(int dt) { return dt == DT_BF16 ? 8 : dt == DT_INT8 ? 16 : 32; }
+
+__host__ __device__ inline long long block_bytes(int dt, int Rt, int Lb) {
+  long long b = (long long)Rt * Lb * 16;
+  if (dt == DT_INT4) b += ((long long)Rt * Lb * 4 + 15) / 16 * 16;
+  return b;
+}
+// Bytes of a full tile (TR rows, all K-blocks).  With TR a multiple of 4 the
+// int4 scale words need no padding, so this is TR times the row bytes.
+__host__ __device__ inline long long full_tile_bytes(int dt, int C) {
+  return (long long)TR * C * (dt == DT_INT4 ? 20 : 16);
+}
+__host__ __device__ inline long long packed_bytes(int dt, int N, int K) {
+  int C = K / per_chunk(dt);
+  int ntiles = (N + TR - 1) / TR;
+  long long total = (long long)(N / TR) * full_tile_bytes(dt, C);
+  if (N % TR) {
+    int Rt = N % TR;
+    for (int c0 = 0; c0 < C; c0 += KBLK) total += block_bytes(dt, Rt, C - c0 < KBLK ? C - c0 : KBLK);
+  }
+  (void)ntiles;
+  return total;
+}
+// Byte offset of K-block b of the tile holding row-tile t (rows Rt), and of
+// chunk (r, l) inside it.
+__host__ __device__ inline long long block_offset(int dt, int C, int t, int Rt, int b) {
+  return (long long)t * full_tile_bytes(dt, C) + (long long)b * block_bytes(dt, Rt, KBLK);
+}
+
+// ------------------------------------------------------- engine sizes ----
+constexpr int NCW = 8;                       // consumer warps per CTA
+constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp
+constexpr int RPW = TR / NCW;                // rows per consumer warp (4)
+constexpr int SLOT_BYTES = 20480;            // one int4 K-block of a full tile
+constexpr int NSLOT = 7;
+constexpr int OFF_RING = 0;
+constexpr int OFF_X = OFF_RING + NSLOT * SLOT_BYTES;     // fp32 x, swizzled
+constexpr int OFF_XSUM = OFF_X + KMAX * 4;               // float4 per chunk
+constexpr int OFF_BAR = OFF_XSUM + (KMAX / 16) * 16;     // mbarriers
+constexpr int OFF_MISC = OFF_BAR + 128;
+constexpr int SMEM_BYTES = OFF_MISC + 512;
+constexpr int ATT_POS_PER_SLOT = 32;
+constexpr int MAX_GQ = 8;                    // q heads per kv head
+constexpr int MAX_M = 8;                     // rows of a verify pass
+
+// --------------------------------------------------------------- phases --
+enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1, PH_MOE_ROUTE = 2 };
+enum XSrc { X_NONE = 0, X_BF16 = 1, X_NORM = 2, X_EMBED_NORM = 3 };
+enum Epi {
+  EPI_STORE_BF16 = 0,
+  EPI_STORE_F32 = 1,
+  EPI_QKV = 2,       // RoPE q and k, q -> q buffer, k/v -> cache row at pos
+  EPI_RESID = 3,     // resid[n] += bf16(y)
+  EPI_SWIGLU = 4,    // h[n/2] = bf16(silu(bf16 gate) * bf16 up)
+  EPI_LOGITS = 5,    // logits[n] = y (fp32), running argmax
+  EPI_MOE_GU = 6,    // SwiGLU into the expert slot's h
+  EPI_MOE_DOWN = 7   // resid[n] += bf16(w1 bf16(y1) + w2 bf16(y2))
+};
+enum ErrCode {
+  ERR_NONE = 0,
+  ERR_WAIT_FULL = 1,
+  ERR_WAIT_EMPTY = 2,
+  ERR_WAIT_GRID = 3,
+  ERR_WAIT_CTA = 4,
+  ERR_DRAIN = 5,
+  ERR_BAD_PROGRAM = 6,
+  ERR_BAD_POS = 7,    // *d_pos outside [0, Tmax)
+  ERR_BAD_TOKEN = 8   // token id outside [0, vocab)
+};
+
+struct Phase {
+  int kind;
+  int wait_bar;    // grid barrier to wait on before the phase (-1: none)
+  int signal_bar;  // grid barrier to arrive on after the phase (-1: none)
+  int rot;         // unit rotation across CTAs
+  // GEMV
+  int dtype, N, K;
+  int epi;
+  const uint8_t* W;        // packed weights
+  const uint16_t* s8;      // int8 row scales
+  long long expert_stride; // MoE: bytes between experts' packed matrices
+  int xsrc;
+  const void* xptr;        // bf16 vector, or fp32 residual for X_NORM
+  const uint16_t* gain;    // RMSNorm gain
+  float eps;
+  void* out;               // epilogue target
+  int layer;
+  int q_rows, kv_rows;     // EPI_QKV split
+  // attention (also used by EPI_QKV)
+  const uint16_t* qbuf;
+  uint16_t* kc;            // cache base for this layer [Hkv][Tmax][hd]
+  uint16_t* vc;
+  uint16_t* attn_out;
+  int Hq, Hkv, hd, Tmax;
+  float* part;             // [Hq][nch_max][hd + 2] partials
+  unsigned* tick;          // [Hkv] combine tickets
+  int stream_cur;          // 1: the row at pos is in memory before launch (standalone)
+};
+
+struct Params {
+  const Phase* prog;   // device program (nullptr: use `single`)
+  int nphases;
+  Phase single;
+  const int* d_pos;    // current position (nullptr: use pos_const)
+  int pos_const;
+  int nctas;           // CTAs taking part (grid size)
+  int unit_target;     // attention split target (normally the SM count)
+  unsigned* bars;      // grid barrier counters (zeroed before launch)
+  int* err;
+  const float2* rope;  // [Tmax][hd/2] cos, sin
+  float* resid;        // fp32 residual [d]
+  const uint16_t* embed;
+  const int* token;
+  float* logits;
+  int* argmax;
+  float* amax_val;     // [nctas]
+  int* amax_idx;       // [nctas]
+  unsigned* amax_tick;
+  int* pos_inc;        // advanced by one at the end (nullptr: no)
+  int vocab;
+  int tmax;            // positions must lie in [0, tmax) (0: not checked)
+};
+
+// ------------------------------------------------------------ host side --
+void set_error(const char* fmt, ...);
+int cuda_fail(cudaError_t e, const char* what);
+#define GF_CUDA(call)                                        \
+  do {                                                       \
+    cudaError_t e_ = (call);                                 \
+    if (e_ != cudaSuccess) return gf::cuda_fail(e_, #call);  \
+  } while (0)
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+int device_sms();
+int launch_engine(const Params& p, int grid, bool cooperative, cudaStream_t s);
+int* device_err_ptr();
+
+}  // namespace gf

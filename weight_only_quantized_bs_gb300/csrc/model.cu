@@ -1,0 +1,379 @@
+// model.cu — host side of the decode step: library-owned quantised weights
+// (gf_model), the KV cache with its RoPE table and scratch (gf_kv), and the
+// phase program that the persistent engine runs once per token.
+#include <math.h>
+#include <string.h>
+
+#include <vector>
+
+#include "gf_internal.cuh"
+
+struct gf_model {
+  gf_model_config cfg;
+  int wdtype;
+  struct Mat {
+    uint8_t* W = nullptr;
+    uint16_t* s8 = nullptr;
+    int N = 0, K = 0;
+  };
+  std::vector<Mat> qkv, o, gu, dn;  // per layer
+  std::vector<uint16_t*> g_attn, g_ffn;
+  Mat lm;
+  uint16_t* embed = nullptr;
+  uint16_t* g_final = nullptr;
+  std::vector<void*> allocs;
+  long long weight_bytes = 0;
+};
+
+struct gf_kv {
+  gf_model* m = nullptr;
+  int Tmax = 0;
+  uint16_t *kc = nullptr, *vc = nullptr;
+  float2* rope = nullptr;
+  uint16_t *qbuf = nullptr, *attn = nullptr, *h = nullptr;
+  float* resid = nullptr;
+  float* part = nullptr;
+  float* amax_val = nullptr;
+  int* amax_idx = nullptr;
+  unsigned* counters = nullptr;  // bars, then attention tickets, then the argmax ticket
+  size_t counter_bytes = 0;
+  unsigned *bars = nullptr, *ticks = nullptr, *amax_tick = nullptr;
+  gf::Phase* prog = nullptr;
+  int nphases = 0;
+  int sms = 0;
+  std::vector<void*> allocs;
+};
+
+namespace gf {
+
+static int dev_alloc(std::vector<void*>& list, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(p, (bytes + 255) / 256 * 256);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_error("device allocation of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+    return GF_ENOMEM;
+  }
+  list.push_back(*p);
+  return GF_OK;
+}
+
+static void free_all(std::vector<void*>& list) {
+  for (void* p : list) cudaFree(p);
+  list.clear();
+}
+
+static int make_mat(gf_model* m, const void* src, int N, int K, gf_model::Mat& out) {
+  out.N = N;
+  out.K = K;
+  const int dt = m->wdtype;
+  const long long bytes = packed_bytes(dt, N, K);
+  int rc = dev_alloc(m->allocs, (void**)&out.W, (size_t)bytes);
+  if (rc) return rc;
+  m->weight_bytes += bytes;
+  if (dt == DT_INT8) {
+    if ((rc = dev_alloc(m->allocs, (void**)&out.s8, (size_t)N * 2))) return rc;
+    m->weight_bytes += (long long)N * 2;
+    return gf_quantize_w8(src, N, K, out.W, out.s8, nullptr);
+  }
+  if (dt == DT_INT4) return gf_quantize_w4g(src, N, K, 32, out.W, nullptr);
+  return gf_repack_bf16(src, N, K, out.W, nullptr);
+}
+
+static int copy_vec(gf_model* m, const void* src, size_t elems, uint16_t** out) {
+  int rc = dev_alloc(m->allocs, (void**)out, elems * 2);
+  if (rc) return rc;
+  GF_CUDA(cudaMemcpy(*out, src, elems * 2, cudaMemcpyDeviceToDevice));
+  return GF_OK;
+}
+
+static int check_cfg(const gf_model_config* c) {
+  if (!c || c->d <= 0 || c->n_layers <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->ffn <= 0 || c->vocab <= 0 ||
+      c->n_heads % c->n_kv_heads || c->n_heads / c->n_kv_heads > MAX_GQ || (c->head_dim != 64 && c->head_dim != 128) ||
+      c->d % 32 || c->ffn % 32 || c->d > KMAX || c->ffn > KMAX || c->n_heads * c->head_dim > KMAX ||
+      !(c->eps > 0) || !(c->theta > 0)) {
+    set_error("gf_model_create: unsupported configuration");
+    return GF_EINVAL;
+  }
+  if (c->n_experts) {
+    set_error("gf_model_create: mixture-of-experts models are not supported by this build");
+    return GF_EUNSUPPORTED;
+  }
+  return GF_OK;
+}
+
+}  // namespace gf
+
+using namespace gf;
+
+extern "C" {
+
+int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w, gf_model** out) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!w || !out || wdtype < 0 || wdtype > 2 || !w->embed || !w->g_final || !w->lm_head || !w->wqkv || !w->wo ||
+      !w->wgu || !w->wd || !w->g_attn || !w->g_ffn) {
+    set_error("gf_model_create: null weights or bad dtype");
+    return GF_EINVAL;
+  }
+  gf_model* m = new gf_model();
+  m->cfg = *cfg;
+  m->wdtype = wdtype;
+  const gf_model_config& c = *cfg;
+  const int hd = c.head_dim, qkvN = (c.n_heads + 2 * c.n_kv_heads) * hd;
+  m->qkv.resize(c.n_layers);
+  m->o.resize(c.n_layers);
+  m->gu.resize(c.n_layers);
+  m->dn.resize(c.n_layers);
+  m->g_attn.resize(c.n_layers);
+  m->g_ffn.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers && !rc; ++l) {
+    if (!w->wqkv[l] || !w->wo[l] || !w->wgu[l] || !w->wd[l] || !w->g_attn[l] || !w->g_ffn[l]) {
+      set_error("gf_model_create: null weight pointer in layer %d", l);
+      rc = GF_EINVAL;
+      break;
+    }
+    if ((rc = make_mat(m, w->wqkv[l], qkvN, c.d, m->qkv[l]))) break;
+    if ((rc = make_mat(m, w->wo[l], c.d, c.n_heads * hd, m->o[l]))) break;
+    if ((rc = make_mat(m, w->wgu[l], 2 * c.ffn, c.d, m->gu[l]))) break;
+    if ((rc = make_mat(m, w->wd[l], c.d, c.ffn, m->dn[l]))) break;
+    if ((rc = copy_vec(m, w->g_attn[l], c.d, &m->g_attn[l]))) break;
+    if ((rc = copy_vec(m, w->g_ffn[l], c.d, &m->g_ffn[l]))) break;
+    m->weight_bytes += 2LL * c.d * 2;
+  }
+  if (!rc) rc = make_mat(m, w->lm_head, c.vocab, c.d, m->lm);
+  if (!rc) rc = copy_vec(m, w->embed, (size_t)c.vocab * c.d, &m->embed);
+  if (!rc) rc = copy_vec(m, w->g_final, c.d, &m->g_final);
+  if (!rc) {
+    m->weight_bytes += (long long)c.d * 2 /* g_final */ + (long long)c.d * 2 /* one embedding row */;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) rc = cuda_fail(e, "gf_model_create");
+  }
+  if (rc) {
+    free_all(m->allocs);
+    delete m;
+    return rc;
+  }
+  *out = m;
+  return GF_OK;
+}
+
+int gf_model_destroy(gf_model* m) {
+  if (!m) return GF_EINVAL;
+  free_all(m->allocs);
+  delete m;
+  return GF_OK;
+}
+
+long long gf_model_weight_bytes(const gf_model* m) { return m ? m->weight_bytes : -1; }
+
+int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
+  if (!m || !out || Tmax <= 0) {
+    set_error("gf_kv_create: bad arguments");
+    return GF_EINVAL;
+  }
+  const gf_model_config& c = m->cfg;
+  const int hd = c.head_dim, L = c.n_layers, Hq = c.n_heads, Hkv = c.n_kv_heads;
+  gf_kv* kv = new gf_kv();
+  kv->m = m;
+  kv->Tmax = Tmax;
+  kv->sms = device_sms();
+  const int G = kv->sms;
+  int rc = GF_OK;
+  const size_t cache_elems = (size_t)L * Hkv * Tmax * hd;
+  const int nch_max = (G + Hkv - 1) / Hkv;
+  const int nph = 5 * L + 1;
+  const int nbars = nph;
+  const size_t nticks = (size_t)L * Hkv;
+  kv->counter_bytes = (nbars + nticks + 1) * sizeof(unsigned);
+  do {
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->kc, cache_elems * 2))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->vc, cache_elems * 2))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->rope, (size_t)Tmax * (hd / 2) * sizeof(float2)))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->qbuf, (size_t)Hq * hd * 2))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->attn, (size_t)Hq * hd * 2))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->h, (size_t)c.ffn * 2))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->resid, (size_t)c.d * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->part, (size_t)Hq * nch_max * (hd + 2) * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_val, (size_t)G * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_idx, (size_t)G * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->counters, kv->counter_bytes))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->prog, (size_t)nph * sizeof(Phase)))) break;
+  } while (0);
+  if (rc) {
+    free_all(kv->allocs);
+    delete kv;
+    return rc;
+  }
+  kv->bars = kv->counters;
+  kv->ticks = kv->counters + nbars;
+  kv->amax_tick = kv->ticks + nticks;
+  cudaError_t e = cudaMemset(kv->kc, 0, cache_elems * 2);
+  if (e == cudaSuccess) e = cudaMemset(kv->vc, 0, cache_elems * 2);
+  if (e == cudaSuccess) e = cudaMemset(kv->counters, 0, kv->counter_bytes);
+
+  // RoPE table: angle pos * theta^(-2i/hd), evaluated in double on the host
+  std::vector<float2> rope((size_t)Tmax * (hd / 2));
+  for (int p = 0; p < Tmax; ++p)
+    for (int i = 0; i < hd / 2; ++i) {
+      const double a = (double)p * pow(c.theta, -2.0 * i / hd);
+      rope[(size_t)p * (hd / 2) + i] = make_float2((float)cos(a), (float)sin(a));
+    }
+  if (e == cudaSuccess) e = cudaMemcpy(kv->rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice);
+
+  // the program: 5 phases per layer + lm_head, each waiting on its predecessor
+  std::vector<Phase> ph(nph);
+  memset(ph.data(), 0, ph.size() * sizeof(Phase));
+  long long cum_units = 0;
+  auto gemv = [&](Phase& p, const gf_model::Mat& mat) {
+    p.kind = PH_GEMV;
+    p.dtype = m->wdtype;
+    p.N = mat.N;
+    p.K = mat.K;
+    p.W = mat.W;
+    p.s8 = mat.s8;
+    p.rot = (int)(cum_units % G);
+    cum_units += (mat.N + TR - 1) / TR;
+  };
+  for (int l = 0; l < L; ++l) {
+    Phase* P = &ph[5 * l];
+    uint16_t* kcl = kv->kc + (size_t)l * Hkv * Tmax * hd;
+    uint16_t* vcl = kv->vc + (size_t)l * Hkv * Tmax * hd;
+    // q/k/v with RoPE and the KV append
+    gemv(P[0], m->qkv[l]);
+    P[0].xsrc = l == 0 ? X_EMBED_NORM : X_NORM;
+    P[0].xptr = kv->resid;
+    P[0].gain = m->g_attn[l];
+    P[0].eps = c.eps;
+    P[0].epi = EPI_QKV;
+    P[0].q_rows = Hq * hd;
+    P[0].kv_rows = Hkv * hd;
+    P[0].qbuf = kv->qbuf;
+    P[0].kc = kcl;
+    P[0].vc = vcl;
+    P[0].hd = hd;
+    P[0].Tmax = Tmax;
+    // attention over positions 0..pos
+    P[1].kind = PH_ATTN;
+    P[1].qbuf = kv->qbuf;
+    P[1].kc = kcl;
+    P[1].vc = vcl;
+    P[1].attn_out = kv->attn;
+    P[1].Hq = Hq;
+    P[1].Hkv = Hkv;
+    P[1].hd = hd;
+    P[1].Tmax = Tmax;
+    P[1].part = kv->part;
+    P[1].tick = kv->ticks + (size_t)l * Hkv;
+    P[1].stream_cur = 0;
+    P[1].rot = (int)(cum_units % G);
+    // o projection + residual
+    gemv(P[2], m->o[l]);
+    P[2].xsrc = X_BF16;
+    P[2].xptr = kv->attn;
+    P[2].epi = EPI_RESID;
+    P[2].out = kv->resid;
+    // gate/up + SwiGLU
+    gemv(P[3], m->gu[l]);
+    P[3].xsrc = X_NORM;
+    P[3].xptr = kv->resid;
+    P[3].gain = m->g_ffn[l];
+    P[3].eps = c.eps;
+    P[3].epi = EPI_SWIGLU;
+    P[3].out = kv->h;
+    // down + residual
+    gemv(P[4], m->dn[l]);
+    P[4].xsrc = X_BF16;
+    P[4].xptr = kv->h;
+    P[4].epi = EPI_RESID;
+    P[4].out = kv->resid;
+  }
+  Phase& lm = ph[nph - 1];
+  gemv(lm, m->lm);
+  lm.xsrc = X_NORM;
+  lm.xptr = kv->resid;
+  lm.gain = m->g_final;
+  lm.eps = c.eps;
+  lm.epi = EPI_LOGITS;
+  for (int i = 0; i < nph; ++i) {
+    ph[i].wait_bar = i == 0 ? -1 : i - 1;
+    ph[i].signal_bar = i == nph - 1 ? -1 : i;
+  }
+  kv->nphases = nph;
+  if (e == cudaSuccess) e = cudaMemcpy(kv->prog, ph.data(), ph.size() * sizeof(Phase), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    rc = cuda_fail(e, "gf_kv_create");
+    free_all(kv->allocs);
+    delete kv;
+    return rc;
+  }
+  *out = kv;
+  return GF_OK;
+}
+
+int gf_kv_destroy(gf_kv* kv) {
+  if (!kv) return GF_EINVAL;
+  free_all(kv->allocs);
+  delete kv;
+  return GF_OK;
+}
+
+int gf_kv_cache_ptrs(gf_kv* kv, void** kcache, void** vcache) {
+  if (!kv || !kcache || !vcache) {
+    set_error("gf_kv_cache_ptrs: null argument");
+    return GF_EINVAL;
+  }
+  *kcache = kv->kc;
+  *vcache = kv->vc;
+  return GF_OK;
+}
+
+int gf_decode_step(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t* d_pos, float* d_logits,
+                   int32_t* d_argmax, gf_stream stream) {
+  if (!m || !kv || kv->m != m || !d_token || !d_pos || !d_logits || !d_argmax) {
+    set_error("gf_decode_step: bad arguments");
+    return GF_EINVAL;
+  }
+  if (!aligned16(d_logits)) {
+    set_error("gf_decode_step: logits must be 16-byte aligned");
+    return GF_EALIGN;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  GF_CUDA(cudaMemsetAsync(kv->counters, 0, kv->counter_bytes, s));
+  Params p;
+  memset(&p, 0, sizeof p);
+  p.prog = kv->prog;
+  p.nphases = kv->nphases;
+  p.d_pos = d_pos;
+  p.nctas = kv->sms;
+  p.unit_target = kv->sms;
+  p.bars = kv->bars;
+  p.err = device_err_ptr();
+  p.rope = kv->rope;
+  p.resid = kv->resid;
+  p.embed = m->embed;
+  p.token = d_token;
+  p.logits = d_logits;
+  p.argmax = d_argmax;
+  p.amax_val = kv->amax_val;
+  p.amax_idx = kv->amax_idx;
+  p.amax_tick = kv->amax_tick;
+  p.pos_inc = d_pos;
+  p.vocab = m->cfg.vocab;
+  p.tmax = kv->Tmax;
+  if (!p.err) {
+    set_error("gf_decode_step: cannot resolve the device error word");
+    return GF_ECUDA;
+  }
+  return launch_engine(p, kv->sms, true, s);
+}
+
+int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t* d_pos, int32_t* d_n_accepted,
+                int32_t* d_next_token, float* d_logits, gf_stream stream) {
+  (void)m; (void)kv; (void)d_tokens; (void)k; (void)d_pos; (void)d_n_accepted; (void)d_next_token;
+  (void)d_logits; (void)stream;
+  set_error("gf_verify_k: not available in this build");
+  return GF_EUNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,256 @@
+// quant.cu — offline weight preparation: int8 and int4-G32 weight-only
+// quantisation written straight into the packed tile layout, bf16 repack, and
+// the inverse unpack kernels used for bit-exact layout checks.
+//
+// Quantisation follows the gpt-fast README, section "Quantization" (int8
+// weight-only; int4 weight-only with --groupsize 32), read as: int8 symmetric
+// per output row, s = bf16(max|w| / 127); int4 per row and 32-wide K group,
+// z = min, s = bf16((max - min) / 15), codes 0..15.  Every quotient is an
+// IEEE fp32 division and every rounding to an integer is rint (ties to even),
+// so the codes are bit-identical to any IEEE implementation of the same steps.
+#include "gf_internal.cuh"
+
+namespace gf {
+
+__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+__device__ __forceinline__ uint32_t rotl15(uint32_t v) { return __funnelshift_l(v, v, 15); }
+__device__ __forceinline__ uint32_t rotr15(uint32_t v) { return __funnelshift_r(v, v, 15); }
+
+struct ChunkAddr {
+  long long code, sz;
+};
+__device__ __forceinline__ ChunkAddr chunk_addr(int dt, int N, int C, int n, int c) {
+  int t = n / TR, r = n % TR;
+  int Rt = min(TR, N - t * TR);
+  int b = c / KBLK, l = c % KBLK;
+  int Lb = min(KBLK, C - b * KBLK);
+  long long base = block_offset(dt, C, t, Rt, b);
+  ChunkAddr a;
+  a.code = base + (long long)(r * Lb + l) * 16;
+  a.sz = base + (long long)Rt * Lb * 16 + (long long)(r * Lb + l) * 4;
+  return a;
+}
+
+__device__ __forceinline__ int warp_id_global() { return (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); }
+__device__ __forceinline__ int warps_total() { return (int)((gridDim.x * blockDim.x) >> 5); }
+
+// int8: one warp per output row.
+__global__ void __launch_bounds__(256) k_quant_w8(const uint16_t* __restrict__ W, int N, int K,
+                                                  uint8_t* __restrict__ P, uint16_t* __restrict__ S) {
+  const int lane = threadIdx.x & 31, C = K / 16;
+  for (int n = warp_id_global(); n < N; n += warps_total()) {
+    const uint16_t* row = W + (size_t)n * K;
+    float mx = 0.0f;
+    for (int k = lane; k < K; k += 32) mx = fmaxf(mx, fabsf(bf2f(row[k])));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const uint16_t sb = f2bf(mx / 127.0f);
+    const float sv = bf2f(sb);
+    if (lane == 0) S[n] = sb;
+    for (int c = lane; c < C; c += 32) {
+      const uint4 raw0 = *reinterpret_cast<const uint4*>(row + c * 16);
+      const uint4 raw1 = *reinterpret_cast<const uint4*>(row + c * 16 + 8);
+      const uint32_t h[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
+      uint32_t words[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t nat = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int k = 4 * j + i;
+          const uint16_t wb = (uint16_t)(h[k >> 1] >> ((k & 1) * 16));
+          int code = 0;
+          if (sv != 0.0f) {
+            code = (int)rintf(bf2f(wb) / sv);
+            code = max(-127, min(127, code));
+          }
+          nat |= (uint32_t)(uint8_t)(int8_t)code << (8 * i);
+        }
+        words[j] = rotl15(nat);
+      }
+      ChunkAddr a = chunk_addr(DT_INT8, N, C, n, c);
+      *reinterpret_cast<uint4*>(P + a.code) = make_uint4(words[0], words[1], words[2], words[3]);
+    }
+  }
+}
+
+// int4 G=32: one warp per output row, one lane per group.
+__global__ void __launch_bounds__(256) k_quant_w4g(const uint16_t* __restrict__ W, int N, int K,
+                                                   uint8_t* __restrict__ P) {
+  const int lane = threadIdx.x & 31, C = K / 32;
+  for (int n = warp_id_global(); n < N; n += warps_total()) {
+    const uint16_t* row = W + (size_t)n * K;
+    for (int c = lane; c < C; c += 32) {
+      float w[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(row + c * 32 + q * 8);
+        const uint32_t h[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          w[q * 8 + 2 * i] = __uint_as_float(h[i] << 16);
+          w[q * 8 + 2 * i + 1] = __uint_as_float(h[i] & 0xFFFF0000u);
+        }
+      }
+      // running min / max in index order, strict comparisons (so a signed
+      // zero is kept exactly as the first one met)
+      float mn = w[0], mx = w[0];
+#pragma unroll
+      for (int i = 1; i < 32; ++i) {
+        if (w[i] < mn) mn = w[i];
+        if (w[i] > mx) mx = w[i];
+      }
+      const float range = mx - mn;
+      const uint16_t sb = f2bf(range / 15.0f);
+      const float sv = bf2f(sb);
+      const uint16_t zb = f2bf(mn);
+      uint32_t words[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t nat = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          int code = 0;
+          if (sv != 0.0f) {
+            code = (int)rintf((w[8 * j + i] - mn) / sv);
+            code = max(0, min(15, code));
+          }
+          nat |= (uint32_t)code << (4 * i);
+        }
+        words[j] = rotl15(nat);
+      }
+      ChunkAddr a = chunk_addr(DT_INT4, N, C, n, c);
+      *reinterpret_cast<uint4*>(P + a.code) = make_uint4(words[0], words[1], words[2], words[3]);
+      *reinterpret_cast<uint32_t*>(P + a.sz) = (uint32_t)sb | ((uint32_t)zb << 16);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_repack_bf16(const uint16_t* __restrict__ W, int N, int K,
+                                                     uint8_t* __restrict__ P) {
+  const int lane = threadIdx.x & 31, C = K / 8;
+  for (int n = warp_id_global(); n < N; n += warps_total()) {
+    for (int c = lane; c < C; c += 32) {
+      ChunkAddr a = chunk_addr(DT_BF16, N, C, n, c);
+      *reinterpret_cast<uint4*>(P + a.code) = *reinterpret_cast<const uint4*>(W + (size_t)n * K + c * 8);
+    }
+  }
+}
+
+// packed -> logical (for layout checks)
+__global__ void __launch_bounds__(256) k_unpack(int dt, const uint8_t* __restrict__ P, int N, int K,
+                                                void* __restrict__ Q, uint16_t* __restrict__ S,
+                                                uint16_t* __restrict__ Z) {
+  const int lane = threadIdx.x & 31, E = per_chunk(dt), C = K / E;
+  for (int n = warp_id_global(); n < N; n += warps_total()) {
+    for (int c = lane; c < C; c += 32) {
+      ChunkAddr a = chunk_addr(dt, N, C, n, c);
+      const uint4 v = *reinterpret_cast<const uint4*>(P + a.code);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      if (dt == DT_BF16) {
+        *reinterpret_cast<uint4*>((uint16_t*)Q + (size_t)n * K + c * 8) = v;
+      } else if (dt == DT_INT8) {
+        uint32_t o[4];
+        for (int j = 0; j < 4; ++j) o[j] = rotr15(wv[j]);
+        *reinterpret_cast<uint4*>((uint8_t*)Q + (size_t)n * K + c * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+      } else {
+        uint8_t* q = (uint8_t*)Q + (size_t)n * K + c * 32;
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t nat = rotr15(wv[j]);
+          for (int i = 0; i < 8; ++i) q[8 * j + i] = (uint8_t)((nat >> (4 * i)) & 15u);
+        }
+        const uint32_t sz = *reinterpret_cast<const uint32_t*>(P + a.sz);
+        S[(size_t)n * C + c] = (uint16_t)sz;
+        Z[(size_t)n * C + c] = (uint16_t)(sz >> 16);
+      }
+    }
+  }
+}
+
+static int check_w(const char* fn, int dt, const void* W, int N, int K) {
+  if (!W || N <= 0 || K <= 0 || K % per_chunk(dt) || K > KMAX * 64) {
+    set_error("%s: bad arguments (N=%d, K=%d; K must be a multiple of %d)", fn, N, K, per_chunk(dt));
+    return GF_EINVAL;
+  }
+  if (!aligned16(W)) {
+    set_error("%s: pointers must be 16-byte aligned", fn);
+    return GF_EALIGN;
+  }
+  return GF_OK;
+}
+
+static int grid_for_rows(int N) {
+  int sms = device_sms();
+  int blocks = (N + 7) / 8;
+  return blocks < sms * 16 ? blocks : sms * 16;
+}
+
+}  // namespace gf
+
+using namespace gf;
+
+extern "C" {
+
+int gf_quantize_w8(const void* W, int N, int K, void* packed, void* s, gf_stream stream) {
+  int rc = check_w("gf_quantize_w8", DT_INT8, W, N, K);
+  if (rc) return rc;
+  if (!packed || !s) { set_error("gf_quantize_w8: null output"); return GF_EINVAL; }
+  if (!aligned16(packed) || !aligned16(s)) { set_error("gf_quantize_w8: outputs must be 16-byte aligned"); return GF_EALIGN; }
+  k_quant_w8<<<grid_for_rows(N), 256, 0, (cudaStream_t)stream>>>((const uint16_t*)W, N, K, (uint8_t*)packed,
+                                                                   (uint16_t*)s);
+  GF_CUDA(cudaGetLastError());
+  return GF_OK;
+}
+
+int gf_quantize_w4g(const void* W, int N, int K, int G, void* packed, gf_stream stream) {
+  if (G != 32) { set_error("gf_quantize_w4g: only group size 32 is supported (got %d)", G); return GF_EUNSUPPORTED; }
+  int rc = check_w("gf_quantize_w4g", DT_INT4, W, N, K);
+  if (rc) return rc;
+  if (!packed) { set_error("gf_quantize_w4g: null output"); return GF_EINVAL; }
+  if (!aligned16(packed)) { set_error("gf_quantize_w4g: output must be 16-byte aligned"); return GF_EALIGN; }
+  // scale-word padding of a ragged tile must read as zero
+  if (N % TR) GF_CUDA(cudaMemsetAsync(packed, 0, (size_t)packed_bytes(DT_INT4, N, K), (cudaStream_t)stream));
+  k_quant_w4g<<<grid_for_rows(N), 256, 0, (cudaStream_t)stream>>>((const uint16_t*)W, N, K, (uint8_t*)packed);
+  GF_CUDA(cudaGetLastError());
+  return GF_OK;
+}
+
+int gf_repack_bf16(const void* W, int N, int K, void* packed, gf_stream stream) {
+  int rc = check_w("gf_repack_bf16", DT_BF16, W, N, K);
+  if (rc) return rc;
+  if (!packed) { set_error("gf_repack_bf16: null output"); return GF_EINVAL; }
+  if (!aligned16(packed)) { set_error("gf_repack_bf16: output must be 16-byte aligned"); return GF_EALIGN; }
+  k_repack_bf16<<<grid_for_rows(N), 256, 0, (cudaStream_t)stream>>>((const uint16_t*)W, N, K, (uint8_t*)packed);
+  GF_CUDA(cudaGetLastError());
+  return GF_OK;
+}
+
+static int unpack_common(const char* fn, int dt, const void* packed, int N, int K, void* q, void* s, void* z,
+                         gf_stream stream) {
+  int rc = check_w(fn, dt, packed, N, K);
+  if (rc) return rc;
+  if (!q || (dt == DT_INT4 && (!s || !z))) { set_error("%s: null output", fn); return GF_EINVAL; }
+  if (!aligned16(q)) { set_error("%s: outputs must be 16-byte aligned", fn); return GF_EALIGN; }
+  k_unpack<<<grid_for_rows(N), 256, 0, (cudaStream_t)stream>>>(dt, (const uint8_t*)packed, N, K, q, (uint16_t*)s,
+                                                                 (uint16_t*)z);
+  GF_CUDA(cudaGetLastError());
+  return GF_OK;
+}
+
+int gf_unpack_w8(const void* packed, int N, int K, void* q, gf_stream stream) {
+  return unpack_common("gf_unpack_w8", DT_INT8, packed, N, K, q, nullptr, nullptr, stream);
+}
+int gf_unpack_w4g(const void* packed, int N, int K, int G, void* q, void* s, void* z, gf_stream stream) {
+  if (G != 32) { set_error("gf_unpack_w4g: only group size 32 is supported"); return GF_EUNSUPPORTED; }
+  return unpack_common("gf_unpack_w4g", DT_INT4, packed, N, K, q, s, z, stream);
+}
+int gf_unpack_bf16(const void* packed, int N, int K, void* W, gf_stream stream) {
+  return unpack_common("gf_unpack_bf16", DT_BF16, packed, N, K, W, nullptr, nullptr, stream);
+}
+
+}  // extern "C"
