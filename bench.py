@@ -1,0 +1,367 @@
+"""Benchmark: batch-size-1 greedy decode of a random-init Llama-2-7B-shaped
+model (32 layers, d 4096, 32 heads x 128, SwiGLU 11008, vocab 32000, RMSNorm
+eps 1e-5, RoPE theta 1e4; 5-token random prompt, then greedy tokens; KV cache
+bf16 up to 2048), with int4-G32 weight-only weights as the headline and bf16 /
+int8 measured in the same run (the gpt-fast README's "Benchmarks" table:
+tokens/s at batch size 1, and the bandwidth those tokens imply).
+
+One step = one decode token = one launch of the persistent engine, which runs
+every layer.  `value` is tokens/s with the model resident in HBM (the timed
+loop feeds each step's argmax back as the next token on the device); `e2e`
+times the same loop through the C-ABI with the token copied in from pinned
+host memory and the argmax read back every step.  The model (4.1-13.5 GB) is
+far larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--dtype int4|int8|bf16]
+                  [--impl ours|reference] [--workload llama2-7b|llama3.1-8b]
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PUBLISHED_TOKS = {  # gpt-fast README "Benchmarks", 1x A100-80GB at 330 W (context)
+    ("llama2-7b", "bf16"): 104.9, ("llama2-7b", "int8"): 155.58, ("llama2-7b", "int4"): 196.80,
+    ("llama3.1-8b", "bf16"): 93.89, ("llama3.1-8b", "int8"): 137.64,
+}
+METRIC = "bs=1 decode tokens/s and achieved HBM GB/s vs GB300 peak (bf16/int8/int4-G32)"
+N_PROMPT = 5
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--dtype", default="int4", choices=["int4", "int8", "bf16"])
+    ap.add_argument("--workload", default="llama2-7b", choices=["llama2-7b", "llama3.1-8b"])
+    ap.add_argument("--only-headline", action="store_true", help="skip the other two weight dtypes")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0, help="use only the first L layers (profiling runs)")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ------------------------------------------------------------- clocks -----
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------ CPU baseline -----
+def oracle_token_seconds(cfg, dtype, seed, n_layers_sample):
+    """The oracle as it stands, on one host core: one decode token at position
+    5 through `n_layers_sample` of the model's layers plus the full lm_head;
+    per-token seconds scaled to all layers.  Quantisation is not timed."""
+    import numpy as np
+    import oracle
+    from synth import models
+    wc = models.WeightCache(cfg, seed=seed, keep=False)
+    om = oracle.OracleModel(cfg, dtype, wc, tmax=8, keep=True)
+    for l in range(n_layers_sample):
+        om._layer(l)   # quantise outside the timed region
+    om.lm_head        # already built
+    x = oracle.bf16_to_double(wc.glob["embed"][[1]])
+    t0 = time.perf_counter()
+    for l in range(n_layers_sample):
+        x = om.layer_forward(l, x, 0)
+    t_layers = time.perf_counter() - t0
+    nrm = np.stack([oracle.rmsnorm(x[0], wc.glob["g_final"], cfg["eps"])])
+    t1 = time.perf_counter()
+    om.lm_head(nrm)
+    t_head = time.perf_counter() - t1
+    per_token = t_layers / n_layers_sample * cfg["n_layers"] + t_head
+    return per_token, t_layers + t_head
+
+
+# ------------------------------------------------------------ our arm -----
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    from synth import models
+    import weight_only_quantized_bs_gb300 as gf
+    from weight_only_quantized_bs_gb300.weights import device_globals, fuse_layer
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    gf.lib()
+    cfg = models.config(args.workload)
+    if args.layers:
+        cfg["n_layers"] = args.layers
+    tmax = 2048
+    dtypes = [args.dtype] if args.only_headline else [d for d in ("int4", "int8", "bf16")
+                                                       if args.workload == "llama2-7b" or d != "int4"]
+    if args.dtype not in dtypes:
+        dtypes.insert(0, args.dtype)
+
+    # synthetic weights: drawn once on the host, fused, resident in HBM as bf16
+    t0 = time.time()
+    wc = models.WeightCache(cfg, seed=args.seed, keep=False)
+    glob = device_globals(wc.glob, dev)
+    layers = [fuse_layer(wc.layer(l), dev) for l in range(cfg["n_layers"])]
+    torch.cuda.synchronize()
+    gen_s = time.time() - t0
+    prompt = models.prompt(cfg, args.seed, N_PROMPT)
+
+    # copy ceiling of this GPU in this process: 1 GiB -> 1 GiB, 16-byte vectors
+    nb = 1 << 30
+    a = torch.empty(nb, dtype=torch.uint8, device=dev)
+    b = torch.empty(nb, dtype=torch.uint8, device=dev)
+    a.fill_(1)
+    for _ in range(3):
+        gf.copy_ceiling(a, b, nb)
+    e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    best = 0.0
+    for _ in range(10):
+        e0.record()
+        gf.copy_ceiling(a, b, nb)
+        e1.record()
+        e1.synchronize()
+        best = max(best, 2 * nb / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    copy_gbs = best
+    del a, b
+
+    hbm_peak, peak_kind = measured_peaks()
+    sampler = ClockSampler(local)
+    results = {}
+    stream = torch.cuda.current_stream()
+    for dt in dtypes:
+        m = gf.Model(cfg, dt, glob, layers)
+        kv = gf.KV(m, tmax)
+        wbytes = m.weight_bytes()
+        tok = torch.zeros(1, dtype=torch.int32, device=dev)
+        pos = torch.zeros(1, dtype=torch.int32, device=dev)
+        logits = torch.empty(cfg["vocab"], dtype=torch.float32, device=dev)
+        # warm-up: the prompt, one token per step, then greedy steps
+        n_warm = max(args.warmup, N_PROMPT)
+        for i in range(n_warm):
+            if i < N_PROMPT:
+                tok.fill_(int(prompt[i]))
+            gf.decode_step(m, kv, tok, pos, logits, tok)   # argmax -> next token
+        torch.cuda.synchronize()
+        p0 = int(pos.item())
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if dt == args.dtype:
+            sampler.start()
+            time.sleep(0.3)
+        ev0, ev1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            gf.decode_step(m, kv, tok, pos, logits, tok)
+        ev1.record(stream)
+        ev1.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        # repeat the timed loop for the clock record (not used for the number)
+        if dt == args.dtype:
+            for _ in range(max(1, int(1500 / max(ms, 1)))):
+                for _ in range(args.steps):
+                    gf.decode_step(m, kv, tok, pos, logits, tok)
+                torch.cuda.synchronize()
+                pos.fill_(p0)
+            clocks = sampler.stop()
+        err = gf.device_error()
+        # algorithmic bytes: weights + KV rows 0..pos read + one row written, per token
+        L, Hkv, hd = cfg["n_layers"], cfg["n_kv_heads"], cfg["head_dim"]
+        row = 2 * L * Hkv * hd * 2
+        kv_bytes = sum(row * (p + 1) + row for p in range(p0, p0 + args.steps))
+        alg_bytes = wbytes * args.steps + kv_bytes
+        toks = args.steps / (ms * 1e-3)
+        gbs = alg_bytes / (ms * 1e-3) / 1e9
+
+        # end to end through the C-ABI: token in from pinned host memory,
+        # argmax out to pinned host memory, every step
+        pos.fill_(p0)
+        h_tok = torch.zeros(1, dtype=torch.int32).pin_memory()
+        h_out = torch.zeros(1, dtype=torch.int32).pin_memory()
+        h_tok[0] = int(prompt[-1])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            tok.copy_(h_tok, non_blocking=True)
+            gf.decode_step(m, kv, tok, pos, logits, tok)
+            h_out.copy_(tok, non_blocking=True)
+            stream.synchronize()
+            h_tok[0] = h_out[0]
+        e2e_s = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        results[dt] = {"tok_s": toks * world, "ms_per_token": ms / args.steps, "gbs": gbs,
+                       "frac_of_peak": gbs / hbm_peak, "frac_of_copy": gbs / copy_gbs,
+                       "bytes_per_token": alg_bytes / args.steps, "weight_bytes": wbytes,
+                       "e2e_tok_s": args.steps / e2e_s * world, "device_error": err}
+        kv.close()
+        m.close()
+        torch.cuda.synchronize()
+    del layers, glob
+
+    head = results[args.dtype]
+    out = {
+        "metric": METRIC,
+        "value": round(head["tok_s"], 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, N_PROMPT),
+        "ms_per_step": round(head["ms_per_token"], 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": (round(head["tok_s"] / world / PUBLISHED_TOKS[(args.workload, args.dtype)], 3)
+                        if (args.workload, args.dtype) in PUBLISHED_TOKS else None),
+        "dtype": "f32",
+        "data": "synthetic (seeded random-init weights, uniform random prompt)",
+        "config": {"workload": "%s-shaped greedy decode, %s weights" % (args.workload, args.dtype),
+                   "model": args.workload, "n_layers": cfg["n_layers"], "weights": args.dtype + ("-g32" if args.dtype == "int4" else ""),
+                   "global_batch": 1, "prompt": N_PROMPT, "tmax": tmax,
+                   "positions": [N_PROMPT if args.warmup <= N_PROMPT else args.warmup,
+                                 max(args.warmup, N_PROMPT) + args.steps],
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush: the model's %d MB stream per step is far above L2" %
+                         int(head["weight_bytes"] / 1e6)},
+        "achieved_gbs": round(head["gbs"], 1),
+        "roofline": {"bound": "hbm", "achieved": round(head["gbs"], 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(head["gbs"] / hbm_peak, 4), "traffic": None,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind,
+                     "kernel": "k_engine (one launch per token)"},
+        "copy_ceiling_gbs": round(copy_gbs, 1),
+        "per_dtype": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                      for k, v in results.items()},
+        "e2e": {"value": round(head["e2e_tok_s"], 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "setup_s": round(gen_s, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        per_tok, spent = oracle_token_seconds(cfg, args.dtype, args.seed, n_layers_sample=2)
+        out["cpu_baseline"] = {"value": round(1.0 / per_tok, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                               "sample": "one token through 2 of %d layers + full lm_head, scaled to %d layers "
+                                         "(%.1f s of CPU)" % (cfg["n_layers"], cfg["n_layers"], spent)}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------ reference arm -----
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle  # noqa: F401  (the oracle is this tier's reference implementation)
+    from synth import models
+    cfg = models.config(args.workload)
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm state
+    per = []
+    spent_all = 0.0
+    for _ in range(args.steps):
+        t, spent = oracle_token_seconds(cfg, args.dtype, args.seed, n_layers_sample=1)
+        per.append(t)
+        spent_all += spent
+    per_tok = statistics.median(per)
+    v = 1.0 / per_tok
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_tok * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded random-init weights)",
+        "config": {"workload": "%s-shaped greedy decode, %s weights" % (args.workload, args.dtype),
+                   "model": args.workload, "global_batch": 1},
+        "cpu_baseline": {"value": round(v, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step: one token through 1 of %d layers + full lm_head, scaled"
+                                   % cfg["n_layers"]},
+        "e2e": {"value": round(v, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

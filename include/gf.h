@@ -176,6 +176,11 @@ int gf_kv_destroy(gf_kv* kv);
 /* Device pointers of the K and V caches (for tests that pre-fill them). */
 int gf_kv_cache_ptrs(gf_kv* kv, void** kcache, void** vcache);
 
+/* Device pointers of the step's activations after the last layer that ran:
+ * q bf16 [Hq hd] (after RoPE), attention output bf16 [Hq hd], SwiGLU output
+ * bf16 [ffn], residual fp32 [d] (for tests of intermediate values). */
+int gf_kv_activation_ptrs(gf_kv* kv, void** q, void** attn, void** h, void** resid);
+
 /* One decode step at position *d_pos (device int32): embeds *d_token, runs
  * every layer (RMSNorm, q/k/v, RoPE, KV append, attention, o, residual,
  * RMSNorm, SwiGLU or top-2 MoE, residual), the final RMSNorm and lm_head,
@@ -184,6 +189,17 @@ int gf_kv_cache_ptrs(gf_kv* kv, void** kcache, void** vcache);
  * every SM; nothing is copied to the host. */
 int gf_decode_step(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t* d_pos,
                    float* d_logits, int32_t* d_argmax, gf_stream stream);
+
+/* Decode step with a phase trace: as gf_decode_step, and for every phase of
+ * the step's program and every CTA, eight 64-bit words are written to d_trace
+ * ([phase][cta][8]): %globaltimer ns at phase entry, after the grid barrier,
+ * after input staging, after the phase's work, at phase close, and when the
+ * CTA's producer finished issuing the phase's copies; then the number of
+ * consumer slot waits that found the slot still in flight and of producer
+ * waits that found no free slot.  gf_trace_bytes() gives the buffer size. */
+size_t gf_trace_bytes(const gf_kv* kv);
+int gf_decode_step_traced(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t* d_pos, float* d_logits,
+                          int32_t* d_argmax, unsigned long long* d_trace, gf_stream stream);
 
 /* Speculative verification (gpt-fast README, "Speculative sampling"):
  * d_tokens holds k+1 ids [last accepted token, draft_1 .. draft_k], fed at

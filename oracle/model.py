@@ -50,6 +50,7 @@ class OracleModel:
         self.K = [np.zeros((c["n_kv_heads"], tmax, c["head_dim"])) for _ in range(c["n_layers"])]
         self.V = [np.zeros((c["n_kv_heads"], tmax, c["head_dim"])) for _ in range(c["n_layers"])]
         self._layers = {}
+        self.record = None   # set to a dict to keep the last token's intermediates
         g = weights.glob
         self.embed = g["embed"]
         self.g_final = g["g_final"]
@@ -93,12 +94,16 @@ class OracleModel:
             self.V[l][:, p, :] = Vn[t].reshape(Hkv, hd)
             A[t] = attention(q, self.K[l][:, :p + 1, :], self.V[l][:, :p + 1, :]).reshape(-1)
         A = round_bf16(A)
+        if self.record is not None:
+            self.record.update(q=q.reshape(-1), attn=A[-1], k=k.reshape(-1), v=Vn[-1])
         return X + round_bf16(L["wo"](A))
 
     def _ffn_dense(self, L, M):
         G = round_bf16(L["wg"](M))
         U = round_bf16(L["wu"](M))
         H = np.stack([swiglu(G[t], U[t]) for t in range(M.shape[0])])
+        if self.record is not None:
+            self.record.update(h=H[-1], gate=G[-1], up=U[-1])
         return round_bf16(L["wd"](H))
 
     def route(self, L, m):
@@ -134,6 +139,8 @@ class OracleModel:
         H = self._attn_block(l, L, X, pos0)
         M = np.stack([rmsnorm(H[t], L["g_ffn"], c["eps"]) for t in range(H.shape[0])])
         F = self._ffn_moe(L, M) if "experts" in L else self._ffn_dense(L, M)
+        if self.record is not None:
+            self.record.update(resid_mid=H[-1], m=M[-1], resid=(H + F)[-1])
         return H + F
 
     def forward(self, tokens, pos0):

@@ -57,6 +57,9 @@ def lib():
             "gf_kv_cache_ptrs": ([vp, vp, vp], i32),
             "gf_decode_step": ([vp, vp, vp, vp, vp, vp, vp], i32),
             "gf_verify_k": ([vp, vp, vp, i32, vp, vp, vp, vp, vp], i32),
+            "gf_trace_bytes": ([vp], sz),
+            "gf_kv_activation_ptrs": ([vp, vp, vp, vp, vp], i32),
+            "gf_decode_step_traced": ([vp, vp, vp, vp, vp, vp, vp, vp], i32),
             "gf_device_error": ([], i32),
             "gf_copy_ceiling": ([vp, vp, sz, vp], i32),
         }
@@ -257,6 +260,12 @@ class KV:
         _check(lib().gf_kv_cache_ptrs(self.h, ctypes.byref(k), ctypes.byref(v)), "gf_kv_cache_ptrs")
         return k.value, v.value
 
+    def activation_ptrs(self):
+        q, a, h, r = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+        _check(lib().gf_kv_activation_ptrs(self.h, ctypes.byref(q), ctypes.byref(a), ctypes.byref(h),
+                                           ctypes.byref(r)), "gf_kv_activation_ptrs")
+        return q.value, a.value, h.value, r.value
+
     def close(self):
         if self.h:
             lib().gf_kv_destroy(self.h)
@@ -272,6 +281,17 @@ class KV:
 def decode_step(model, kv, d_token, d_pos, d_logits, d_argmax, stream=None):
     _check(lib().gf_decode_step(model.h, kv.h, _p(d_token), _p(d_pos), _p(d_logits), _p(d_argmax), _s(stream)),
            "gf_decode_step")
+
+
+def trace_bytes(kv):
+    return int(lib().gf_trace_bytes(kv.h))
+
+
+def decode_step_traced(model, kv, d_token, d_pos, d_logits, d_argmax, d_trace, stream=None):
+    """As decode_step, also writing the per-phase, per-CTA trace (int64 tensor
+    of trace_bytes(kv) / 8 words) described in include/gf.h."""
+    _check(lib().gf_decode_step_traced(model.h, kv.h, _p(d_token), _p(d_pos), _p(d_logits), _p(d_argmax),
+                                       _p(d_trace), _s(stream)), "gf_decode_step_traced")
 
 
 def verify_k(model, kv, d_tokens, k, d_pos, d_n, d_next, d_logits=None, stream=None):

@@ -163,11 +163,15 @@ __device__ __forceinline__ const Phase& phase_at(const Params& P, int i) { retur
 struct Prod {
   uint32_t it;
   uint64_t pol;
+  uint32_t blocked;
 };
 
 __device__ __forceinline__ bool prod_slot(const Smem& S, Prod& pr, int* err, uint8_t*& dst, uint64_t*& fb) {
   const uint32_t slot = pr.it % NSLOT, use = pr.it / NSLOT;
-  if (use > 0 && !mbar_wait(&S.empty[slot], (use - 1) & 1u, err, ERR_WAIT_EMPTY)) return false;
+  if (use > 0 && !mbar_test(&S.empty[slot], (use - 1) & 1u)) {
+    ++pr.blocked;
+    if (!mbar_wait_slow(&S.empty[slot], (use - 1) & 1u, err, ERR_WAIT_EMPTY)) return false;
+  }
   dst = S.ring + slot * SLOT_BYTES;
   fb = &S.full[slot];
   ++pr.it;
@@ -177,6 +181,7 @@ __device__ __forceinline__ bool prod_slot(const Smem& S, Prod& pr, int* err, uin
 __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
   Prod pr;
   pr.it = 0;
+  pr.blocked = 0;
   pr.pol = evict_first_policy();
   int* err = P.err;
   const int G = P.nctas;
@@ -219,6 +224,12 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
         }
       }
     }
+    if (P.trace) {
+      unsigned long long* tr = P.trace + ((size_t)pi * G + cta) * TRACE_W;
+      tr[5] = gtimer();
+      tr[7] = pr.blocked;
+      pr.blocked = 0;
+    }
   }
   // Drain: never leave the CTA with bulk copies still writing its shared
   // memory.  The last min(it, NSLOT) slots are the only ones that can be in
@@ -241,6 +252,7 @@ struct Cons {
   uint32_t it;      // ring position
   uint32_t cphase;  // parity of the consumer barrier
   int warp, lane, ctid;
+  uint32_t starved; // slot waits that found the slot not yet filled (warp 0)
 };
 
 // all consumer warps meet; false if the wait gave up
@@ -258,7 +270,10 @@ __device__ __forceinline__ bool cta_sync(const Smem& S, Cons& cs, int* err) {
 __device__ __forceinline__ bool slot_acquire(const Smem& S, Cons& cs, int* err, const uint8_t*& base) {
   const uint32_t slot = cs.it % NSLOT, par = (cs.it / NSLOT) & 1u;
   int ok = 1;
-  if (cs.lane == 0) ok = mbar_wait(&S.full[slot], par, err, ERR_WAIT_FULL);
+  if (cs.lane == 0 && !mbar_test(&S.full[slot], par)) {
+    ++cs.starved;
+    ok = mbar_wait_slow(&S.full[slot], par, err, ERR_WAIT_FULL);
+  }
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok && cs.lane) mbar_test(&S.full[slot], par);
   base = S.ring + slot * SLOT_BYTES;
@@ -745,12 +760,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   cs.warp = warp;
   cs.lane = lane;
   cs.ctid = tid;
+  cs.starved = 0;
   const int G = P.nctas;
   ArgMax am = {-INFINITY, 0x7fffffff};
   bool any_logits = false;
 
   for (int pi = 0; pi < P.nphases; ++pi) {
     const Phase& ph = phase_at(P, pi);
+    unsigned long long* tr = (P.trace && tid == 0) ? P.trace + ((size_t)pi * G + cta) * TRACE_W : nullptr;
+    if (tr) tr[0] = gtimer();
     if (ph.wait_bar >= 0) {
       int ok = 1;
       if (tid == 0) ok = grid_wait(P.bars + ph.wait_bar, (unsigned)G, P.err);
@@ -758,8 +776,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
       if (!ok) return;
       if (!cta_sync(S, cs, P.err)) return;
     }
+    if (tr) tr[1] = gtimer();
     if (ph.kind == PH_GEMV) {
       if (!stage_x(ph, P, S, cs, cta)) return;
+      if (tr) tr[2] = gtimer();
       const int ntiles = (ph.N + TR - 1) / TR;
       for (int t = first_unit(cta, ph.rot, G); t < ntiles; t += G) {
         bool ok;
@@ -780,9 +800,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
         if (!ok) return;
       }
     }
+    if (tr) {
+      if (ph.kind != PH_GEMV) tr[2] = tr[1];
+      tr[3] = gtimer();
+      tr[6] = cs.starved;
+    }
+    cs.starved = 0;
     // every warp of this CTA has finished the phase (its global writes made)
     if (!cta_sync(S, cs, P.err)) return;
     if (ph.signal_bar >= 0 && tid == 0) grid_arrive(P.bars + ph.signal_bar);
+    if (tr) tr[4] = gtimer();
   }
   if (any_logits) argmax_finish(P, S, cs, cta, am);
 }

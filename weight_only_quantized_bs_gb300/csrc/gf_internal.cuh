@@ -137,7 +137,13 @@ struct Params {
   int* pos_inc;        // advanced by one at the end (nullptr: no)
   int vocab;
   int tmax;            // positions must lie in [0, tmax) (0: not checked)
+  unsigned long long* trace;  // [nphases][nctas][TRACE_W] timestamps and counters (nullptr: off)
 };
+// Trace record of one CTA in one phase (ns of %globaltimer, then counters):
+// 0 phase entered, 1 grid barrier passed, 2 input staged, 3 units done,
+// 4 phase closed, 5 producer finished issuing the phase, 6 consumer slot
+// waits that found the slot empty, 7 producer waits that found no free slot.
+constexpr int TRACE_W = 8;
 
 // ------------------------------------------------------------ host side --
 void set_error(const char* fmt, ...);

@@ -328,8 +328,41 @@ int gf_kv_cache_ptrs(gf_kv* kv, void** kcache, void** vcache) {
   return GF_OK;
 }
 
+static int decode_launch(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t* d_pos, float* d_logits,
+                         int32_t* d_argmax, unsigned long long* d_trace, cudaStream_t stream);
+
+size_t gf_trace_bytes(const gf_kv* kv) {
+  return kv ? (size_t)kv->nphases * kv->sms * TRACE_W * sizeof(unsigned long long) : 0;
+}
+
+int gf_kv_activation_ptrs(gf_kv* kv, void** q, void** attn, void** h, void** resid) {
+  if (!kv || !q || !attn || !h || !resid) {
+    set_error("gf_kv_activation_ptrs: null argument");
+    return GF_EINVAL;
+  }
+  *q = kv->qbuf;
+  *attn = kv->attn;
+  *h = kv->h;
+  *resid = kv->resid;
+  return GF_OK;
+}
+
+int gf_decode_step_traced(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t* d_pos, float* d_logits,
+                          int32_t* d_argmax, unsigned long long* d_trace, gf_stream stream) {
+  if (!d_trace || !aligned16(d_trace)) {
+    set_error("gf_decode_step_traced: trace buffer must be a 16-byte aligned device pointer");
+    return GF_EINVAL;
+  }
+  return decode_launch(m, kv, d_token, d_pos, d_logits, d_argmax, d_trace, (cudaStream_t)stream);
+}
+
 int gf_decode_step(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t* d_pos, float* d_logits,
                    int32_t* d_argmax, gf_stream stream) {
+  return decode_launch(m, kv, d_token, d_pos, d_logits, d_argmax, nullptr, (cudaStream_t)stream);
+}
+
+static int decode_launch(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t* d_pos, float* d_logits,
+                         int32_t* d_argmax, unsigned long long* d_trace, cudaStream_t stream) {
   if (!m || !kv || kv->m != m || !d_token || !d_pos || !d_logits || !d_argmax) {
     set_error("gf_decode_step: bad arguments");
     return GF_EINVAL;
@@ -361,6 +394,7 @@ int gf_decode_step(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t* d_po
   p.pos_inc = d_pos;
   p.vocab = m->cfg.vocab;
   p.tmax = kv->Tmax;
+  p.trace = d_trace;
   if (!p.err) {
     set_error("gf_decode_step: cannot resolve the device error word");
     return GF_ECUDA;
