@@ -122,6 +122,24 @@ size_t gf_attn_workspace_bytes(int Hq, int Hkv, int hd);
 int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq, int Hkv, int hd,
                    int Tmax, int pos, void* out, void* ws, size_t ws_bytes, gf_stream stream);
 
+/* Decode attention that allocates nothing: the same computation and result
+ * as gf_decode_attn, for callers that cannot allocate device memory (a
+ * plug-in that only receives tensor pointers from a host framework owning all
+ * device memory, or a latency-critical loop that must not call into the CUDA
+ * allocator, which can synchronise the device).  The pages have no
+ * counterpart of this call; it exists only for such callers.
+ * Scratch: a static device array of GF_NOALLOC_ATTN_SCRATCH bytes in the
+ * library, held by every GPU that loads the library until the process exits.
+ * Shapes needing more (Hq * ceil(SMs / Hkv) * (hd + 2) * 4 + 256 bytes)
+ * return GF_EINVAL with the size in gf_last_error().  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Every call
+ * shares the one array: calls that overlap on the same GPU (for example from two
+ * streams at once) race and give wrong results; serialise them.  No cudaMalloc / cudaFree is made. */
+#define GF_NOALLOC_ATTN_SCRATCH (2 << 20)
+int gf_decode_attn_noalloc(const void* q, const void* kcache, const void* vcache, int Hq, int Hkv, int hd,
+                           int Tmax, int pos, void* out, gf_stream stream);
+
 /* ------------------------------------------------------ decode step ---- */
 typedef struct {
   int d;           /* model width */

@@ -1,0 +1,57 @@
+"""gf_decode_attn_noalloc (for callers that cannot allocate device memory:
+plug-ins that only get tensor pointers from a framework owning all device
+memory, or loops that must not enter the CUDA allocator) against the existing
+gf_decode_attn, called through the C-ABI twice in a row so that the second
+call runs on scratch that still holds the first call's contents.  Also: a
+shape needing more than the static scratch is rejected before any launch."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+import weight_only_quantized_bs_gb300 as gf
+from weight_only_quantized_bs_gb300.weights import to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2   # the decode-attention parity bar of the other GPU tests
+
+
+def _case(Hq, Hkv, hd, Tmax, pos, seed):
+    q = to_dev(synth.normal_bf16(seed, 60, (Hq, hd), 1.0))
+    K = to_dev(synth.normal_bf16(seed, 61, (Hkv, Tmax, hd), 1.0))
+    V = to_dev(synth.normal_bf16(seed, 62, (Hkv, Tmax, hd), 1.0))
+    return q, K, V
+
+
+def test_noalloc_matches_workspace_version_twice():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    L = gf.lib()
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for (Hq, Hkv, hd, Tmax, pos, seed) in [(32, 8, 128, 2048, 1500, 1), (32, 32, 128, 512, 205, 2)]:
+        q, K, V = _case(Hq, Hkv, hd, Tmax, pos, seed)
+        ref = gf.decode_attn(q, K, V, Hq, Hkv, hd, Tmax, pos)
+        out = torch.full((Hq * hd,), float("nan"), dtype=torch.bfloat16, device=q.device)
+        rc = L.gf_decode_attn_noalloc(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(K.data_ptr()),
+                                      ctypes.c_void_p(V.data_ptr()), Hq, Hkv, hd, Tmax, pos,
+                                      ctypes.c_void_p(out.data_ptr()), s)
+        assert rc == 0, L.gf_last_error()
+        torch.cuda.synchronize()
+        a, b = out.float().cpu().numpy(), ref.float().cpu().numpy()
+        assert np.all(np.isfinite(a))
+        assert np.abs(a - b).max() <= TOL * np.abs(b).max()
+    assert gf.device_error() == 0
+
+
+def test_noalloc_rejects_shapes_beyond_the_scratch():
+    L = gf.lib()
+    dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    p = ctypes.c_void_p(dummy.data_ptr())
+    # 4096 query heads over 512 kv heads need 4096 * 130 * 4 bytes (> 2 MiB)
+    rc = L.gf_decode_attn_noalloc(p, p, p, 4096, 512, 128, 16, 0, p, None)
+    assert rc == 1
+    assert b"static scratch" in L.gf_last_error()

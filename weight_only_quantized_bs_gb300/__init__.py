@@ -49,6 +49,7 @@ def lib():
             "gf_gemv_w4g": ([vp, vp, i32, i32, i32, vp, i32, vp], i32),
             "gf_attn_workspace_bytes": ([i32, i32, i32], sz),
             "gf_decode_attn": ([vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, sz, vp], i32),
+            "gf_decode_attn_noalloc": ([vp, vp, vp, i32, i32, i32, i32, i32, vp, vp], i32),
             "gf_model_create": ([vp, i32, vp, vp], i32),
             "gf_model_destroy": ([vp], i32),
             "gf_model_weight_bytes": ([vp], i64),
