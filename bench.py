@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--dtype", default="int4", choices=["int4", "int8", "bf16"])
-    ap.add_argument("--workload", default="llama2-7b", choices=["llama2-7b", "llama3.1-8b"])
+    ap.add_argument("--workload", default="llama2-7b", choices=["llama2-7b", "llama3.1-8b", "gemv-set", "gemv"])
     ap.add_argument("--only-headline", action="store_true", help="skip the other two weight dtypes")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
@@ -327,6 +327,78 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------- GEMV workloads ---
+GEMV_SET = [("qkv", 12288, 4096), ("o", 4096, 4096), ("gate_up", 22016, 4096), ("down", 4096, 11008),
+            ("lm_head", 32000, 4096)]
+
+
+def run_gemv(args):
+    """Standalone GEMVs: the Llama-2-7B layer set (gemv-set) or the single
+    4096 x 4096 GEMV (gemv), x ~ N(0,1), W ~ N(0,0.02).  Distinct weight copies
+    totalling at least 4x L2 rotate through the timed loop."""
+    import torch
+    import __graft_entry__
+    import synth
+    import weight_only_quantized_bs_gb300 as gf
+    from weight_only_quantized_bs_gb300.weights import to_dev
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    shapes = GEMV_SET if args.workload == "gemv-set" else [("single", 4096, 4096)]
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    dt = gf.DTYPE_NAMES[args.dtype]
+    per = []
+    for name, N, K in shapes:
+        W = to_dev(synth.normal_bf16(args.seed, 700 + N % 97, (N, K), 0.02))
+        if dt == gf.W_INT8:
+            qp, s8 = gf.quantize_w8(W)
+        elif dt == gf.W_INT4G32:
+            qp, s8 = gf.quantize_w4g(W), None
+        else:
+            qp, s8 = gf.repack_bf16(W), None
+        del W
+        nbytes = qp.numel() + (s8.numel() * 2 if s8 is not None else 0) + 2 * K + 4 * N
+        copies = max(1, -(-4 * l2 // nbytes))
+        packs = [qp] + [qp.clone() for _ in range(copies - 1)]
+        x = to_dev(synth.normal_bf16(args.seed, 5, (K,), 1.0))
+        y = torch.empty(N, dtype=torch.float32, device=dev)
+
+        def call(i):
+            p = packs[i % copies]
+            if dt == gf.W_INT8:
+                gf.gemv_w8(x, p, s8, N, K, gf.Y_F32, out=y)
+            elif dt == gf.W_INT4G32:
+                gf.gemv_w4g(x, p, N, K, gf.Y_F32, out=y)
+            else:
+                gf.gemv_bf16(x, p, N, K, gf.Y_F32, out=y)
+        for i in range(args.warmup):
+            call(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        e0.record()
+        for i in range(args.steps):
+            call(i)
+        e1.record()
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        per.append({"name": name, "N": N, "K": K, "bytes": nbytes, "us": round(us, 2),
+                    "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "copies": copies})
+        del packs
+    tot_b = sum(p["bytes"] for p in per)
+    tot_us = sum(p["us"] for p in per)
+    hbm_peak, kind = measured_peaks()
+    gbs = tot_b / (tot_us * 1e-6) / 1e9
+    print(json.dumps({
+        "metric": "standalone GEMV GB/s (%s)" % args.workload, "value": round(gbs, 1), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_us / 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": args.workload, "weights": args.dtype,
+                                        "l2": "weights rotate through copies totalling >= 4x L2"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "traffic": None},
+        "per_gemv": per, "gpu_launches": args.steps * len(shapes)}))
+
+
 # ------------------------------------------------------ reference arm -----
 def run_reference(args):
     rank, world, _ = dist_env()
@@ -363,5 +435,7 @@ if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.workload in ("gemv-set", "gemv"):
+        run_gemv(a)
     else:
         run_ours(a)

@@ -194,14 +194,15 @@ int gf_kv_destroy(gf_kv* kv);
 /* Device pointers of the K and V caches (for tests that pre-fill them). */
 int gf_kv_cache_ptrs(gf_kv* kv, void** kcache, void** vcache);
 
-/* Device pointers of the step's activations after the last layer that ran:
- * q bf16 [Hq hd] (after RoPE), attention output bf16 [Hq hd], SwiGLU output
- * bf16 [ffn], residual fp32 [d] (for tests of intermediate values). */
+/* Device pointers of the step's activations after the last layer that ran,
+ * all fp32: q [Hq hd] (after RoPE), attention output [Hq hd], SwiGLU output
+ * [ffn], residual [d] (for tests of intermediate values). */
 int gf_kv_activation_ptrs(gf_kv* kv, void** q, void** attn, void** h, void** resid);
 
 /* One decode step at position *d_pos (device int32): embeds *d_token, runs
  * every layer (RMSNorm, q/k/v, RoPE, KV append, attention, o, residual,
  * RMSNorm, SwiGLU or top-2 MoE, residual), the final RMSNorm and lm_head,
+ * with fp32 activations and a bf16 KV cache,
  * writes fp32 logits [vocab] to d_logits and their argmax (lowest index on
  * ties) to *d_argmax, then advances *d_pos by one.  One kernel launch on
  * every SM; nothing is copied to the host. */

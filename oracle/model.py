@@ -7,10 +7,12 @@ with gpt-fast"): embed -> per layer (RMSNorm, q/k/v, RoPE, KV append,
 attention, o, residual, RMSNorm, SwiGLU FFN or top-2 MoE, residual) ->
 RMSNorm -> lm_head -> fp32 logits -> greedy argmax.
 
-READING of the rounding points (the pages give none): the residual stream is
-kept at full precision (fp64 here, fp32 on the GPU); every linear output, q,
-k, v (and so the KV cache), the attention output, the SwiGLU product and the
-MoE combination are rounded to bf16; logits are not rounded.  Speculative
+READING of the precision (the pages give none): only the weights are
+quantised or kept in bf16, and the KV cache holds bf16 (the decode configs
+name it so): k after RoPE and v are rounded to bf16 when they are written to
+the cache.  Every other activation -- RMSNorm outputs, q, attention output,
+SwiGLU product, linear outputs, the residual stream, logits -- stays at full
+precision (fp64 here, fp32 on the GPU).  Speculative
 verification (gpt-fast README, "Speculative sampling") accepts the longest
 prefix of draft tokens that equals the target's own greedy choices.
 """
@@ -82,29 +84,28 @@ class OracleModel:
         T = X.shape[0]
         hd, Hq, Hkv = c["head_dim"], c["n_heads"], c["n_kv_heads"]
         Nrm = np.stack([rmsnorm(X[t], L["g_attn"], c["eps"]) for t in range(T)])
-        Q = round_bf16(L["wq"](Nrm))
-        Kn = round_bf16(L["wk"](Nrm))
+        Q = L["wq"](Nrm)
+        Kn = L["wk"](Nrm)
         Vn = round_bf16(L["wv"](Nrm))
         A = np.empty((T, Hq * hd))
         for t in range(T):
             p = pos0 + t
             q = rope(Q[t], Hq, hd, p, c["theta"]).reshape(Hq, hd)
-            k = rope(Kn[t], Hkv, hd, p, c["theta"]).reshape(Hkv, hd)
+            k = round_bf16(rope(Kn[t], Hkv, hd, p, c["theta"])).reshape(Hkv, hd)
             self.K[l][:, p, :] = k
             self.V[l][:, p, :] = Vn[t].reshape(Hkv, hd)
             A[t] = attention(q, self.K[l][:, :p + 1, :], self.V[l][:, :p + 1, :]).reshape(-1)
-        A = round_bf16(A)
         if self.record is not None:
             self.record.update(q=q.reshape(-1), attn=A[-1], k=k.reshape(-1), v=Vn[-1])
-        return X + round_bf16(L["wo"](A))
+        return X + L["wo"](A)
 
     def _ffn_dense(self, L, M):
-        G = round_bf16(L["wg"](M))
-        U = round_bf16(L["wu"](M))
+        G = L["wg"](M)
+        U = L["wu"](M)
         H = np.stack([swiglu(G[t], U[t]) for t in range(M.shape[0])])
         if self.record is not None:
             self.record.update(h=H[-1], gate=G[-1], up=U[-1])
-        return round_bf16(L["wd"](H))
+        return L["wd"](H)
 
     def route(self, L, m):
         """Top-2 of the router logits (lower index first on ties) and the
@@ -126,11 +127,9 @@ class OracleModel:
             acc = 0.0
             for e, w in ((e1, w1), (e2, w2)):
                 E = L["experts"][e]
-                g = round_bf16(E["wg"](M[t]))
-                u = round_bf16(E["wu"](M[t]))
-                y = round_bf16(E["wd"](swiglu(g, u)))
+                y = E["wd"](swiglu(E["wg"](M[t]), E["wu"](M[t])))
                 acc = acc + w * y
-            out[t] = round_bf16(acc)
+            out[t] = acc
         return out
 
     def layer_forward(self, l, X, pos0):

@@ -312,18 +312,17 @@ void orc_attention(int Hq, int Hkv, int hd, long T, const double* q, const doubl
 }
 
 /* ------------------------------------------------ elementwise steps ---- */
-/* RMSNorm: out = bf16( x * (mean(x^2) + eps)^(-1/2) * g ). */
+/* RMSNorm: out = x * (mean(x^2) + eps)^(-1/2) * g. */
 void orc_rmsnorm(const double* x, const uint16_t* g, long d, double eps, double* out) {
   double ss = 0.0;
   for (long i = 0; i < d; ++i) ss += x[i] * x[i];
   double r = 1.0 / sqrt(ss / (double)d + eps);
   for (long i = 0; i < d; ++i) out[i] = x[i] * r * (double)orc_f32_from_bf16(g[i]);
-  orc_round_bf16(out, d);
 }
 
 /* Rotary position embedding at position pos, applied in place to nheads heads
  * of hd values.  READING: adjacent pairs (2i, 2i+1) rotate by the angle
- * pos * theta^(-2i/hd); the result is rounded to bf16. */
+ * pos * theta^(-2i/hd). */
 void orc_rope(double* v, int nheads, int hd, long pos, double theta) {
   for (int h = 0; h < nheads; ++h) {
     double* x = v + (long)h * hd;
@@ -335,11 +334,9 @@ void orc_rope(double* v, int nheads, int hd, long pos, double theta) {
       x[2 * i + 1] = x0 * s + x1 * c;
     }
   }
-  orc_round_bf16(v, (long)nheads * hd);
 }
 
-/* SwiGLU gate: h = bf16( silu(gate) * up ), silu(a) = a / (1 + e^(-a)). */
+/* SwiGLU gate: h = silu(gate) * up, silu(a) = a / (1 + e^(-a)). */
 void orc_swiglu(const double* gate, const double* up, long n, double* h) {
   for (long i = 0; i < n; ++i) h[i] = gate[i] / (1.0 + exp(-gate[i])) * up[i];
-  orc_round_bf16(h, n);
 }

@@ -20,16 +20,16 @@ def _bf(x):
 
 
 def brute_forward(cfg, W, tokens):
-    """Plain-loop restatement of the Llama-style step for bf16 weights:
-    written separately from oracle/model.py and sharing only the bf16
-    rounding helper."""
+    """Plain-loop restatement of the Llama-style step for bf16 weights
+    (fp64 activations, bf16 KV cache): written separately from
+    oracle/model.py and sharing only the bf16 rounding helper."""
     d, hd, Hq, Hkv = cfg["d"], cfg["head_dim"], cfg["n_heads"], cfg["n_kv_heads"]
     eps, theta = cfg["eps"], cfg["theta"]
     glob = W.glob
 
     def norm(x, g):
         r = 1.0 / math.sqrt(sum(v * v for v in x) / len(x) + eps)
-        return _bf(np.array([x[i] * r * g[i] for i in range(len(x))]))
+        return np.array([x[i] * r * g[i] for i in range(len(x))])
 
     def mat(Wb, x):
         M = f64(Wb)
@@ -43,7 +43,7 @@ def brute_forward(cfg, W, tokens):
                 x0, x1 = v[h * hd + 2 * i], v[h * hd + 2 * i + 1]
                 out[h * hd + 2 * i] = x0 * math.cos(a) - x1 * math.sin(a)
                 out[h * hd + 2 * i + 1] = x0 * math.sin(a) + x1 * math.cos(a)
-        return _bf(out)
+        return out
 
     Kc = [[] for _ in range(cfg["n_layers"])]
     Vc = [[] for _ in range(cfg["n_layers"])]
@@ -53,8 +53,8 @@ def brute_forward(cfg, W, tokens):
         for l in range(cfg["n_layers"]):
             w = W.layer(l)
             n = norm(x, f64(w["g_attn"]))
-            q = rot(_bf(mat(w["wq"], n)), Hq, pos)
-            k = rot(_bf(mat(w["wk"], n)), Hkv, pos)
+            q = rot(mat(w["wq"], n), Hq, pos)
+            k = _bf(rot(mat(w["wk"], n), Hkv, pos))   # the KV cache holds bf16
             v = _bf(mat(w["wv"], n))
             Kc[l].append(k)
             Vc[l].append(v)
@@ -66,12 +66,12 @@ def brute_forward(cfg, W, tokens):
                 e = [math.exp(s - m) for s in sc]
                 for i in range(hd):
                     att[h * hd + i] = sum(e[t] * Vc[l][t][g * hd + i] for t in range(len(e))) / sum(e)
-            x = x + _bf(mat(w["wo"], _bf(att)))
+            x = x + mat(w["wo"], att)
             mm = norm(x, f64(w["g_ffn"]))
-            gt = _bf(mat(w["wg"], mm))
-            up = _bf(mat(w["wu"], mm))
-            hh = _bf(np.array([gt[i] / (1 + math.exp(-gt[i])) * up[i] for i in range(len(gt))]))
-            x = x + _bf(mat(w["wd"], hh))
+            gt = mat(w["wg"], mm)
+            up = mat(w["wu"], mm)
+            hh = np.array([gt[i] / (1 + math.exp(-gt[i])) * up[i] for i in range(len(gt))])
+            x = x + mat(w["wd"], hh)
         xn = norm(x, f64(glob["g_final"]))
         logits.append(mat(glob["lm_head"], xn))
     return np.array(logits)
@@ -136,9 +136,9 @@ def test_moe_zero_expert_leaves_weighted_other():
     # zero the second expert's down projection: output = w1 * y1 (rounded)
     L["experts"][e2]["wd"] = oracle.model._Mat(oracle.BF16, np.zeros_like(base.layer(0)["experts"][e2]["wd"]))
     E = L["experts"][e1]
-    y1 = _bf(E["wd"](oracle.swiglu(_bf(E["wg"](m)), _bf(E["wu"](m)))))
+    y1 = E["wd"](oracle.swiglu(E["wg"](m), E["wu"](m)))
     out = om._ffn_moe(L, m[None, :])[0]
-    assert np.array_equal(out, _bf(w1 * y1))
+    assert np.array_equal(out, w1 * y1)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "int4"])

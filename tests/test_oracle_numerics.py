@@ -284,25 +284,29 @@ def test_rmsnorm_constant_input_closed_form():
     g = synth.normal_bf16(0, 97, (64,), 0.02, mu=1.0)
     for c in (0.5, -3.0, 1e-3):
         y = oracle.rmsnorm(np.full(64, c), g, 1e-5)
-        ref = oracle.round_bf16(f32(g) * c / math.sqrt(c * c + 1e-5))
-        assert np.array_equal(y, ref)
+        ref = f32(g) * c / math.sqrt(c * c + 1e-5)
+        assert np.allclose(y, ref, rtol=1e-15, atol=0)
 
 
 def test_rope_identity_rotation_and_relative_position():
     rng = np.random.default_rng(5)
     hd, H = 16, 3
-    v = oracle.round_bf16(rng.standard_normal(H * hd))
+    v = rng.standard_normal(H * hd)
     assert np.array_equal(oracle.rope(v, H, hd, 0, 1e4), v)
     p = 7
     r = oracle.rope(v, H, hd, p, 1e4)
     # pair 0 turns by exactly p radians (frequency theta^0 = 1)
     x0, x1 = v[0], v[1]
-    assert abs(r[0] - (x0 * math.cos(p) - x1 * math.sin(p))) <= abs(r[0]) * 2 ** -8 + 1e-30
-    assert abs(r[1] - (x0 * math.sin(p) + x1 * math.cos(p))) <= abs(r[1]) * 2 ** -8 + 1e-30
-    # each pair keeps its length (up to the final bf16 rounding)
+    assert abs(r[0] - (x0 * math.cos(p) - x1 * math.sin(p))) <= 1e-15
+    assert abs(r[1] - (x0 * math.sin(p) + x1 * math.cos(p))) <= 1e-15
+    # the last pair of a head turns by p * theta^(-2(hd/2-1)/hd)
+    f = 1e4 ** (-2.0 * (hd // 2 - 1) / hd)
+    y0, y1 = v[hd - 2], v[hd - 1]
+    assert abs(r[hd - 2] - (y0 * math.cos(p * f) - y1 * math.sin(p * f))) <= 1e-15
+    # each pair keeps its length
     a = v.reshape(-1, 2)
     b = r.reshape(-1, 2)
-    assert np.allclose(np.hypot(a[:, 0], a[:, 1]), np.hypot(b[:, 0], b[:, 1]), rtol=2 ** -7)
+    assert np.allclose(np.hypot(a[:, 0], a[:, 1]), np.hypot(b[:, 0], b[:, 1]), rtol=1e-14)
     # <R(p)q, R(p')k> depends on p - p' only
     q = rng.standard_normal(hd)
     k = rng.standard_normal(hd)
@@ -316,6 +320,6 @@ def test_swiglu_closed_forms():
     u = np.array([5.0, 2.0, 0.5, 1.0])
     h = oracle.swiglu(g, u)
     assert h[0] == 0.0
-    assert h[1] == oracle.round_bf16([2.0 / (1 + math.exp(-1))])[0]
-    assert h[2] == 15.0                 # silu(30) = 30 to far below bf16 precision
+    assert abs(h[1] - 2.0 / (1 + math.exp(-1))) < 1e-15
+    assert abs(h[2] - 15.0) < 1e-11      # silu(30) = 30 (1 - 9e-14)
     assert abs(h[3]) < 1e-11

@@ -83,10 +83,10 @@ int gf_decode_attn_noalloc(const void* q, const void* kcache, const void* vcache
   ph.kind = PH_ATTN;
   ph.wait_bar = -1;
   ph.signal_bar = -1;
-  ph.qbuf = (const uint16_t*)q;
+  ph.qbuf = const_cast<void*>(q);
   ph.kc = (uint16_t*)kcache;
   ph.vc = (uint16_t*)vcache;
-  ph.attn_out = (uint16_t*)out;
+  ph.attn_out = out;
   ph.Hq = Hq;
   ph.Hkv = Hkv;
   ph.hd = hd;
@@ -97,11 +97,8 @@ int gf_decode_attn_noalloc(const void* q, const void* kcache, const void* vcache
   // The array keeps the previous call's contents: the combine tickets must
   // start at zero (the partials are always written before they are read).
   GF_CUDA(cudaMemsetAsync(ph.tick, 0, (size_t)Hkv * sizeof(unsigned), (cudaStream_t)stream));
-  const int T = pos + 1;
-  int want = (sms + Hkv - 1) / Hkv, maxch = (T + 31) / 32;
-  int nch = want < maxch ? want : maxch;
-  const int CH = ((T + nch - 1) / nch + 31) / 32 * 32;
-  nch = (T + CH - 1) / CH;
+  int CH, nch;
+  attn_split(pos + 1, Hkv, sms, CH, nch);
   const int units = Hkv * nch;
   const int grid = units < sms ? units : sms;
   p.nctas = grid;

@@ -2,16 +2,19 @@
 //
 // One CTA per SM runs a program of phases (a single GEMV or attention for the
 // standalone calls; every layer of a decode step for gf_decode_step).  In
-// each CTA one producer thread streams the CTA's weight blocks (and KV-cache
-// rows) from HBM into a ring of shared-memory slots with bulk asynchronous
-// copies (cp.async.bulk, completion counted on an mbarrier, L2 evict-first
-// hint), running ahead across phase boundaries because the weight stream does
-// not depend on activations.  Eight consumer warps wait for each slot,
-// dequantise int8 / int4 codes in registers against an fp32 copy of the input
-// vector held in shared memory, and release the slot.  Dependent phases are
-// separated by grid barriers (cooperative launch); every wait in the kernel is
-// bounded by a 2-second clock, after which the kernel records an error code,
-// drains its own copies in flight and returns.
+// each CTA one producer thread streams the CTA's weight half-tiles (16 rows x
+// one K-block) and KV-cache rows from HBM into a ring of 14 shared-memory
+// slots with bulk asynchronous copies (cp.async.bulk, completion counted on
+// an mbarrier, L2 evict-first hint), running ahead across phase boundaries
+// because the weight stream does not depend on activations.  Each slot
+// belongs to one of eight consumer warps (round robin), which dequantises the
+// int8 / int4 codes of its 16 rows in registers against an fp32 copy of the
+// input vector held in shared memory and releases the slot; the K-block
+// partial sums of a half-tile meet in shared memory, where the last warp to
+// arrive adds them in a fixed order and runs the epilogue.  Dependent phases
+// are separated by grid barriers (cooperative launch); every wait in the
+// kernel is bounded by a 2-second clock, after which the kernel records an
+// error code, drains its own copies in flight and returns.
 //
 // The decode step computed here is the batch-size-1 autoregressive step of
 // the gpt-fast README ("Benchmarks", "Quantization"): RMSNorm, q/k/v, RoPE,
@@ -41,6 +44,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// non-blocking probe (never suspends), used only to count stalls for the trace
+__device__ __forceinline__ bool mbar_probe(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_u32(b)), "r"(parity)
       : "memory");
@@ -124,20 +137,24 @@ __device__ __forceinline__ float rbf(float f) { return bf2f(f2bf(f)); }
 // ---------------------------------------------------------- shared state --
 struct Smem {
   uint8_t* ring;
-  float* xs;       // fp32 input vector, swizzled per chunk
-  float4* xsum;    // per-chunk sums of the input vector
-  uint64_t* full;  // [NSLOT]
-  uint64_t* empty; // [NSLOT]
-  uint64_t* cbar;  // consumer-warps barrier
-  float* red;      // [64] reduction scratch
-  int* bcast;      // [8] broadcast ints
+  float* xs;        // fp32 input vector, swizzled per chunk
+  float* xsum;      // sum of x over each 32-wide group (int4 zero offsets)
+  float* tb;        // [NTB][NCW][HROWS] partial row sums of half-tiles
+  int* tbc;         // [NTB] arrival counters
+  uint64_t* full;   // [NSLOT]
+  uint64_t* empty;  // [NSLOT]
+  uint64_t* cbar;   // consumer-warps barrier
+  float* red;       // [64] reduction scratch
+  int* bcast;       // [64] broadcast ints
 };
 
 __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
   Smem s;
   s.ring = base + OFF_RING;
   s.xs = reinterpret_cast<float*>(base + OFF_X);
-  s.xsum = reinterpret_cast<float4*>(base + OFF_XSUM);
+  s.xsum = reinterpret_cast<float*>(base + OFF_XSUM);
+  s.tb = reinterpret_cast<float*>(base + OFF_TB);
+  s.tbc = reinterpret_cast<int*>(base + OFF_TBC);
   s.full = reinterpret_cast<uint64_t*>(base + OFF_BAR);
   s.empty = s.full + NSLOT;
   s.cbar = s.empty + NSLOT;
@@ -147,15 +164,6 @@ __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
 }
 
 __device__ __forceinline__ int first_unit(int cta, int rot, int G) { return ((cta - rot) % G + G) % G; }
-
-__device__ __forceinline__ void attn_split(int T, int Hkv, int target, int& CH, int& nch) {
-  int want = (target + Hkv - 1) / Hkv;
-  if (want < 1) want = 1;
-  int maxch = (T + 31) / 32;
-  nch = want < maxch ? want : maxch;
-  CH = ((T + nch - 1) / nch + 31) / 32 * 32;
-  nch = (T + CH - 1) / CH;
-}
 
 __device__ __forceinline__ const Phase& phase_at(const Params& P, int i) { return P.prog ? P.prog[i] : P.single; }
 
@@ -168,9 +176,9 @@ struct Prod {
 
 __device__ __forceinline__ bool prod_slot(const Smem& S, Prod& pr, int* err, uint8_t*& dst, uint64_t*& fb) {
   const uint32_t slot = pr.it % NSLOT, use = pr.it / NSLOT;
-  if (use > 0 && !mbar_test(&S.empty[slot], (use - 1) & 1u)) {
-    ++pr.blocked;
-    if (!mbar_wait_slow(&S.empty[slot], (use - 1) & 1u, err, ERR_WAIT_EMPTY)) return false;
+  if (use > 0) {
+    if (!mbar_probe(&S.empty[slot], (use - 1) & 1u)) ++pr.blocked;
+    if (!mbar_wait(&S.empty[slot], (use - 1) & 1u, err, ERR_WAIT_EMPTY)) return false;
   }
   dst = S.ring + slot * SLOT_BYTES;
   fb = &S.full[slot];
@@ -178,6 +186,9 @@ __device__ __forceinline__ bool prod_slot(const Smem& S, Prod& pr, int* err, uin
   return true;
 }
 
+// Slot order of a GEMV phase (producer and consumers walk it identically):
+// for each of the CTA's tiles t, for each half h of the tile's rows, the
+// K-blocks b in order.
 __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
   Prod pr;
   pr.it = 0;
@@ -193,14 +204,20 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
       const int ntiles = (ph.N + TR - 1) / TR, nb = (C + KBLK - 1) / KBLK;
       for (int t = first_unit(cta, ph.rot, G); t < ntiles && ok; t += G) {
         const int Rt = min(TR, ph.N - t * TR);
-        for (int b = 0; b < nb; ++b) {
-          const int Lb = min(KBLK, C - b * KBLK);
-          const uint32_t bytes = (uint32_t)block_bytes(dt, Rt, Lb);
-          uint8_t* dst;
-          uint64_t* fb;
-          if (!(ok = prod_slot(S, pr, err, dst, fb))) break;
-          mbar_expect_tx(fb, bytes);
-          bulk_g2s(dst, ph.W + block_offset(dt, C, t, Rt, b), bytes, fb, pr.pol);
+        for (int h = 0; h * HROWS < Rt && ok; ++h) {
+          const int r0 = h * HROWS, rh = min(HROWS, Rt - r0);
+          for (int b = 0; b < nb; ++b) {
+            const int Lb = min(KBLK, C - b * KBLK);
+            const uint8_t* blk = ph.W + block_offset(dt, C, t, Rt, b);
+            const uint32_t cb = (uint32_t)(rh * Lb * 16);
+            const uint32_t sb = dt == DT_INT4 ? (uint32_t)((rh * Lb * 4 + 15) / 16 * 16) : 0u;
+            uint8_t* dst;
+            uint64_t* fb;
+            if (!(ok = prod_slot(S, pr, err, dst, fb))) break;
+            mbar_expect_tx(fb, cb + sb);
+            bulk_g2s(dst, blk + (size_t)r0 * Lb * 16, cb, fb, pr.pol);
+            if (sb) bulk_g2s(dst + SLOT_SZ_OFF, blk + (size_t)Rt * Lb * 16 + (size_t)r0 * Lb * 4, sb, fb, pr.pol);
+          }
         }
       }
     } else if (ph.kind == PH_ATTN) {
@@ -210,14 +227,14 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
       const int nunits = ph.Hkv * nch;
       const uint32_t rowb = (uint32_t)ph.hd * 2;
       for (int u = first_unit(cta, ph.rot, G); u < nunits && ok; u += G) {
-        const int h = u / nch, c = u % nch;
+        const int hh = u / nch, c = u % nch;
         const int p0 = c * CH, p1 = min(p0 + CH, T), pe = min(p1, Ts);
         for (int p = p0; p < pe; p += ATT_POS_PER_SLOT) {
           const int np = min(ATT_POS_PER_SLOT, pe - p);
           uint8_t* dst;
           uint64_t* fb;
           if (!(ok = prod_slot(S, pr, err, dst, fb))) break;
-          const size_t off = ((size_t)h * ph.Tmax + p) * ph.hd;
+          const size_t off = ((size_t)hh * ph.Tmax + p) * ph.hd;
           mbar_expect_tx(fb, 2u * np * rowb);
           bulk_g2s(dst, ph.kc + off, np * rowb, fb, pr.pol);
           bulk_g2s(dst + ATT_POS_PER_SLOT * rowb, ph.vc + off, np * rowb, fb, pr.pol);
@@ -249,10 +266,11 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
 
 // ============================================================ consumers ===
 struct Cons {
-  uint32_t it;      // ring position
-  uint32_t cphase;  // parity of the consumer barrier
+  uint32_t it;       // ring position of the phase's first slot
+  uint32_t cphase;   // parity of the consumer barrier
+  uint32_t useq;     // half-tiles seen so far (combine-buffer index)
   int warp, lane, ctid;
-  uint32_t starved; // slot waits that found the slot not yet filled (warp 0)
+  uint32_t starved;  // slot waits that found the slot still in flight (warp 0)
 };
 
 // all consumer warps meet; false if the wait gave up
@@ -267,96 +285,151 @@ __device__ __forceinline__ bool cta_sync(const Smem& S, Cons& cs, int* err) {
   return ok != 0;
 }
 
-__device__ __forceinline__ bool slot_acquire(const Smem& S, Cons& cs, int* err, const uint8_t*& base) {
-  const uint32_t slot = cs.it % NSLOT, par = (cs.it / NSLOT) & 1u;
+__device__ __forceinline__ bool slot_acquire(const Smem& S, Cons& cs, uint32_t it, int* err, const uint8_t*& base) {
+  const uint32_t slot = it % NSLOT, par = (it / NSLOT) & 1u;
   int ok = 1;
-  if (cs.lane == 0 && !mbar_test(&S.full[slot], par)) {
-    ++cs.starved;
-    ok = mbar_wait_slow(&S.full[slot], par, err, ERR_WAIT_FULL);
+  if (cs.lane == 0) {
+    if (cs.warp == 0 && !mbar_probe(&S.full[slot], par)) ++cs.starved;
+    ok = mbar_wait(&S.full[slot], par, err, ERR_WAIT_FULL);
   }
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok && cs.lane) mbar_test(&S.full[slot], par);
   base = S.ring + slot * SLOT_BYTES;
   return ok != 0;
 }
-__device__ __forceinline__ void slot_release(const Smem& S, Cons& cs) {
+__device__ __forceinline__ void slot_release(const Smem& S, const Cons& cs, uint32_t it) {
   __syncwarp();
-  if (cs.lane == 0) mbar_arrive(&S.empty[cs.it % NSLOT]);
-  ++cs.it;
+  if (cs.lane == 0) mbar_arrive(&S.empty[it % NSLOT]);
 }
 
 // ------------------------------------------------------ input staging ----
 __device__ __forceinline__ int swz(int g, int U) { return ((g * U) >> 3) & (U - 1); }
 
-// Stages the phase's input vector into shared memory (fp32, swizzled per
-// chunk) with per-chunk sums used by the int8 / int4 dequantisation.
-__device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
-  const int K = ph.K, dt = ph.dtype, E = per_chunk(dt), U = E / 4, C = K / E;
-  const int NT = NCW * 32;
-  float r = 1.0f;
-  const float* res = nullptr;
-  const uint16_t* emb = nullptr;
-  if (ph.xsrc == X_NORM || ph.xsrc == X_EMBED_NORM) {
-    if (ph.xsrc == X_NORM) {
-      res = reinterpret_cast<const float*>(ph.xptr);
-    } else {
-      emb = P.embed + (size_t)(*P.token) * K;
-    }
-    float ss = 0.0f;
-    for (int k = cs.ctid * 4; k < K; k += NT * 4) {
-      float4 v;
-      if (res) {
-        v = __ldcg(reinterpret_cast<const float4*>(res + k));
-      } else {
-        const uint2 h = *reinterpret_cast<const uint2*>(emb + k);
-        v = make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xFFFF0000u), __uint_as_float(h.y << 16),
-                        __uint_as_float(h.y & 0xFFFF0000u));
-        if (cta == 0) *reinterpret_cast<float4*>(P.resid + k) = v;
-      }
-      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (cs.lane == 0) S.red[cs.warp] = ss;
-    if (!cta_sync(S, cs, P.err)) return false;
-    float tot = 0.0f;
-#pragma unroll
-    for (int w = 0; w < NCW; ++w) tot += S.red[w];
-    r = 1.0f / sqrtf(tot / (float)K + ph.eps);
+__device__ __forceinline__ float4 bf4(uint2 h) {
+  return make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xFFFF0000u), __uint_as_float(h.y << 16),
+                     __uint_as_float(h.y & 0xFFFF0000u));
+}
+
+// Stores float4 number k4 of x (swizzled per chunk so that the 32 lanes of a
+// warp read their chunks without bank conflicts) and, for int4, the sum of
+// each 32-wide group (8 consecutive threads hold one group).
+__device__ __forceinline__ void stage_store(const Smem& S, const Cons& cs, int dt, int U, int k4, bool ok, float4 a) {
+  const int g = k4 / U, u = k4 % U;
+  if (ok) reinterpret_cast<float4*>(S.xs)[g * U + (u ^ swz(g, U))] = a;
+  if (dt == DT_INT4) {
+    float sg = a.x + a.y + a.z + a.w;
+    sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+    sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+    sg += __shfl_xor_sync(0xffffffffu, sg, 4);
+    if (ok && (cs.lane & 7) == 0) S.xsum[g] = sg;
   }
-  float4* xs4 = reinterpret_cast<float4*>(S.xs);
-  for (int g = cs.ctid; g < C; g += NT) {
-    const int k0 = g * E;
-    float se = 0.0f, so = 0.0f;
-    for (int u = 0; u < U; ++u) {
-      float v[4];
-      if (ph.xsrc == X_BF16) {
-        const uint2 h = __ldcg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(ph.xptr) + k0 + 4 * u));
-        v[0] = __uint_as_float(h.x << 16);
-        v[1] = __uint_as_float(h.x & 0xFFFF0000u);
-        v[2] = __uint_as_float(h.y << 16);
-        v[3] = __uint_as_float(h.y & 0xFFFF0000u);
-      } else {
-        float4 a;
-        if (res) {
-          a = __ldcg(reinterpret_cast<const float4*>(res + k0 + 4 * u));
-        } else {
-          const uint2 h = *reinterpret_cast<const uint2*>(emb + k0 + 4 * u);
-          a = make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xFFFF0000u), __uint_as_float(h.y << 16),
-                          __uint_as_float(h.y & 0xFFFF0000u));
-        }
-        const uint2 gg = *reinterpret_cast<const uint2*>(ph.gain + k0 + 4 * u);
-        v[0] = rbf(a.x * r * __uint_as_float(gg.x << 16));
-        v[1] = rbf(a.y * r * __uint_as_float(gg.x & 0xFFFF0000u));
-        v[2] = rbf(a.z * r * __uint_as_float(gg.y << 16));
-        v[3] = rbf(a.w * r * __uint_as_float(gg.y & 0xFFFF0000u));
+}
+
+// Stages the phase's input vector into shared memory as fp32.  Thread t
+// handles float4 number t + 256 j; every load of a batch is issued before any
+// is used, so a phase pays about one L2 round trip per batch.
+__device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
+  const int K = ph.K, dt = ph.dtype, E = per_chunk(dt), U = E / 4;
+  const int K4 = K / 4, NT = NCW * 32;
+  const int nit = (K4 + NT - 1) / NT;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (ph.xsrc == X_BF16) {
+    const uint2* xb = reinterpret_cast<const uint2*>(ph.xptr);
+    for (int j0 = 0; j0 < nit; j0 += 8) {
+      uint2 h[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int k4 = cs.ctid + (j0 + t) * NT;
+        h[t] = make_uint2(0u, 0u);
+        if (j0 + t < nit && k4 < K4) h[t] = __ldcg(xb + k4);
       }
-      se += v[0] + v[2];
-      so += v[1] + v[3];
-      xs4[g * U + (u ^ swz(g, U))] = make_float4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        if (j0 + t < nit) stage_store(S, cs, dt, U, cs.ctid + (j0 + t) * NT, cs.ctid + (j0 + t) * NT < K4, bf4(h[t]));
     }
-    if (dt == DT_INT4) S.xsum[g] = make_float4(-se, -so, se + so, 0.0f);
-    else if (dt == DT_INT8) S.xsum[g] = make_float4(-1.5f * se, -1.5f * so, 0.0f, 0.0f);
+    return cta_sync(S, cs, P.err);
+  }
+  if (ph.xsrc == X_F32) {
+    const float4* xf = reinterpret_cast<const float4*>(ph.xptr);
+    for (int j0 = 0; j0 < nit; j0 += 8) {
+      float4 a[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int k4 = cs.ctid + (j0 + t) * NT;
+        a[t] = zero;
+        if (j0 + t < nit && k4 < K4) a[t] = __ldcg(xf + k4);
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        if (j0 + t < nit) stage_store(S, cs, dt, U, cs.ctid + (j0 + t) * NT, cs.ctid + (j0 + t) * NT < K4, a[t]);
+    }
+    return cta_sync(S, cs, P.err);
+  }
+  // RMSNorm of the fp32 residual (or of the embedding row for the first layer)
+  const float* res = ph.xsrc == X_NORM ? reinterpret_cast<const float*>(ph.xptr) : nullptr;
+  const uint16_t* emb = ph.xsrc == X_EMBED_NORM ? P.embed + (size_t)(*P.token) * K : nullptr;
+  const uint2* gain = reinterpret_cast<const uint2*>(ph.gain);
+  float4 keep[4];
+  uint2 gk[4];
+  float ss = 0.0f;
+  for (int j0 = 0; j0 < nit; j0 += 4) {
+    float4 a[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int k4 = cs.ctid + (j0 + t) * NT;
+      a[t] = zero;
+      if (j0 + t < nit && k4 < K4) {
+        if (res) {
+          a[t] = __ldcg(reinterpret_cast<const float4*>(res) + k4);
+        } else {
+          a[t] = bf4(*reinterpret_cast<const uint2*>(emb + 4 * k4));
+          if (cta == 0) reinterpret_cast<float4*>(P.resid)[k4] = a[t];
+        }
+        if (j0 == 0) gk[t] = gain[k4];
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      ss += a[t].x * a[t].x + a[t].y * a[t].y + a[t].z * a[t].z + a[t].w * a[t].w;
+      if (j0 == 0) keep[t] = a[t];
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (cs.lane == 0) S.red[cs.warp] = ss;
+  if (!cta_sync(S, cs, P.err)) return false;
+  float tot = 0.0f;
+#pragma unroll
+  for (int w = 0; w < NCW; ++w) tot += S.red[w];
+  const float r = 1.0f / sqrtf(tot / (float)K + ph.eps);
+  for (int j0 = 0; j0 < nit; j0 += 4) {
+    float4 a[4];
+    uint2 gg[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int k4 = cs.ctid + (j0 + t) * NT;
+      a[t] = zero;
+      gg[t] = make_uint2(0u, 0u);
+      if (j0 + t < nit && k4 < K4) {
+        if (j0 == 0) {
+          a[t] = keep[t];
+          gg[t] = gk[t];
+        } else {
+          a[t] = res ? __ldcg(reinterpret_cast<const float4*>(res) + k4)
+                     : bf4(*reinterpret_cast<const uint2*>(emb + 4 * k4));
+          gg[t] = gain[k4];
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (j0 + t < nit) {
+        const int k4 = cs.ctid + (j0 + t) * NT;
+        const float4 g = bf4(gg[t]);
+        const float4 v = make_float4(a[t].x * r * g.x, a[t].y * r * g.y, a[t].z * r * g.z, a[t].w * r * g.w);
+        stage_store(S, cs, dt, U, k4, k4 < K4, v);
+      }
+    }
   }
   return cta_sync(S, cs, P.err);
 }
@@ -364,65 +437,84 @@ __device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& c
 // ------------------------------------------------------ GEMV compute -----
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-// int4: view i of a code word (rotated right by 8i) carries code k = 8j+2i in
-// bits 15..18 and k = 8j+2i+1 in bits 19..22.  OR-ing the exponent of 1.0f
-// turns them into 1 + q/256 and 1 + q/16 exactly; the per-group offsets are
-// removed through the staged sums (accumulator initialised to -sum x).
-__device__ __forceinline__ float2 dot_int4(const uint4 c, const float2* x2, float2 acc) {
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t v = i ? __funnelshift_r(w[j], w[j], 8 * i) : w[j];
-      const float lo = __uint_as_float((v & 0x00078000u) | 0x3F800000u);
-      const float hi = __uint_as_float((v & 0x00780000u) | 0x3F800000u);
-      acc = ffma2(make_float2(lo, hi), x2[4 * j + i], acc);
-    }
-  }
-  return acc;
-}
-// int8: view i carries code k = 4j+i in bits 15..22; XOR with 0x3FC00000 sets
-// the exponent of 1.0f and flips the sign bit, giving 1 + (q + 128)/256.
-__device__ __forceinline__ float2 dot_int8(const uint4 c, const float2* x2, float2 acc) {
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float f[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t v = i ? __funnelshift_r(w[j], w[j], 8 * i) : w[j];
-      f[i] = __uint_as_float((v & 0x007F8000u) ^ 0x3FC00000u);
-    }
-    acc = ffma2(make_float2(f[0], f[1]), x2[2 * j], acc);
-    acc = ffma2(make_float2(f[2], f[3]), x2[2 * j + 1], acc);
-  }
-  return acc;
-}
-__device__ __forceinline__ float2 dot_bf16(const uint4 c, const float2* x2, float2 acc) {
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    acc = ffma2(make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u)), x2[j], acc);
-  return acc;
+__device__ __forceinline__ uint32_t word_of(const uint4& c, int j) {
+  return j == 0 ? c.x : j == 1 ? c.y : j == 2 ? c.z : c.w;
 }
 
-// Sum of each of the warp's 4 rows over the 32 lanes; lane l ends with row
-// 2*bit4(l) + bit3(l).
-__device__ __forceinline__ float warp_rows4(const float v[4], int lane) {
-  const bool h16 = lane & 16;
-  float k0 = h16 ? v[2] : v[0], k1 = h16 ? v[3] : v[1];
-  const float s0 = h16 ? v[0] : v[2], s1 = h16 ? v[1] : v[3];
-  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-  const bool h8 = lane & 8;
-  float keep = h8 ? k1 : k0;
-  const float send = h8 ? k0 : k1;
-  keep += __shfl_xor_sync(0xffffffffu, send, 8);
-  keep += __shfl_xor_sync(0xffffffffu, keep, 4);
-  keep += __shfl_xor_sync(0xffffffffu, keep, 2);
-  keep += __shfl_xor_sync(0xffffffffu, keep, 1);
-  return keep;
+// int4: view i of a code word (rotated right by 8i) carries code k = 8j+2i in
+// bits 15..18 and k = 8j+2i+1 in bits 19..22.  OR-ing the exponent of 1.0f
+// turns them into 1 + q/256 and 1 + q/16 exactly (one LOP3 each); subtracting
+// 1 (exact) leaves q/256 and q/16, which multiply the fp32 input pair with one
+// packed FMA.  R rows are interleaved so that their accumulator chains
+// overlap.  Result per row: (sum_even q x / 256, sum_odd q x / 16) over the
+// lane's 32-wide group.
+template <int R>
+__device__ __forceinline__ void dotR_int4(const uint4* c, const float2* x2, float2* acc) {
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const uint32_t wj = word_of(c[r], j);
+        const uint32_t v = i ? __funnelshift_r(wj, wj, 8 * i) : wj;
+        const float lo = __uint_as_float((v & 0x00078000u) | 0x3F800000u);
+        const float hi = __uint_as_float((v & 0x00780000u) | 0x3F800000u);
+        acc[r] = ffma2(__fadd2_rn(make_float2(lo, hi), m1), x2[4 * j + i], acc[r]);
+      }
+    }
+  }
+}
+// int8: view i carries code k = 4j+i in bits 15..22; XOR with 0x3FC00000 sets
+// the exponent of 1.0f and flips the sign bit, giving 1 + (q + 128)/256;
+// subtracting 1.5 (exact) leaves q/256.  Result per row: q x / 256 by parity
+// of k.
+template <int R>
+__device__ __forceinline__ void dotR_int8(const uint4* c, const float2* x2, float2* acc) {
+  const float2 off = make_float2(-1.5f, -1.5f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const uint32_t wj = word_of(c[r], j);
+      float f[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t v = i ? __funnelshift_r(wj, wj, 8 * i) : wj;
+        f[i] = __uint_as_float((v & 0x007F8000u) ^ 0x3FC00000u);
+      }
+      acc[r] = ffma2(__fadd2_rn(make_float2(f[0], f[1]), off), x2[2 * j], acc[r]);
+      acc[r] = ffma2(__fadd2_rn(make_float2(f[2], f[3]), off), x2[2 * j + 1], acc[r]);
+    }
+  }
+}
+template <int R>
+__device__ __forceinline__ void dotR_bf16(const uint4* c, const float2* x2, float2* acc) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const uint32_t wj = word_of(c[r], j);
+      acc[r] = ffma2(make_float2(__uint_as_float(wj << 16), __uint_as_float(wj & 0xFFFF0000u)), x2[j], acc[r]);
+    }
+  }
+}
+
+// Sums each of 16 per-lane values over the 32 lanes; afterwards lane l holds
+// the total of value l >> 1.
+__device__ __forceinline__ float warp_rows16(float v[16], int lane) {
+#pragma unroll
+  for (int s = 16, n = 16; s >= 2; s >>= 1, n >>= 1) {
+    const bool hi = lane & s;
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float keep = hi ? v[k + n / 2] : v[k];
+      const float send = hi ? v[k] : v[k + n / 2];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
 struct ArgMax {
@@ -436,74 +528,10 @@ __device__ __forceinline__ void amax_merge(ArgMax& a, float v, int i) {
   }
 }
 
-template <int DT>
-__device__ bool gemv_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int t, int pos, ArgMax& am) {
-  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
-  constexpr int U = E / 4;
-  const int C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
-  const int Rt = min(TR, ph.N - t * TR);
-  const int lane = cs.lane, w = cs.warp;
-  float yacc[RPW] = {0.f, 0.f, 0.f, 0.f};
-  float2 acc2[RPW];
-#pragma unroll
-  for (int i = 0; i < RPW; ++i) acc2[i] = make_float2(0.f, 0.f);
-  const float4* xs4 = reinterpret_cast<const float4*>(S.xs);
-
-  for (int b = 0; b < nb; ++b) {
-    const int Lb = min(KBLK, C - b * KBLK);
-    const uint8_t* base;
-    if (!slot_acquire(S, cs, P.err, base)) return false;
-    if (lane < Lb) {
-      const int g = b * KBLK + lane;
-      float4 xv[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) xv[u] = xs4[g * U + (u ^ swz(g, U))];
-      const float2* x2 = reinterpret_cast<const float2*>(xv);
-      float4 xsm = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (DT != DT_BF16) xsm = S.xsum[g];
-      uint4 code[RPW];
-      uint32_t sz[RPW];
-#pragma unroll
-      for (int i = 0; i < RPW; ++i) {
-        const int r = w * RPW + i;
-        if (r < Rt) {
-          code[i] = *reinterpret_cast<const uint4*>(base + (r * Lb + lane) * 16);
-          if (DT == DT_INT4) sz[i] = *reinterpret_cast<const uint32_t*>(base + Rt * Lb * 16 + (r * Lb + lane) * 4);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < RPW; ++i) {
-        const int r = w * RPW + i;
-        if (r < Rt) {
-          if (DT == DT_INT4) {
-            const float2 a = dot_int4(code[i], x2, make_float2(xsm.x, xsm.y));
-            const float Sq = fmaf(256.0f, a.x, 16.0f * a.y);
-            const float s = __uint_as_float(sz[i] << 16), z = __uint_as_float(sz[i] & 0xFFFF0000u);
-            yacc[i] = fmaf(s, Sq, fmaf(z, xsm.z, yacc[i]));
-          } else if (DT == DT_INT8) {
-            acc2[i] = __fadd2_rn(acc2[i], make_float2(xsm.x, xsm.y));
-            acc2[i] = dot_int8(code[i], x2, acc2[i]);
-          } else {
-            acc2[i] = dot_bf16(code[i], x2, acc2[i]);
-          }
-        }
-      }
-    }
-    slot_release(S, cs);
-  }
-
-  float v[RPW];
-#pragma unroll
-  for (int i = 0; i < RPW; ++i) v[i] = DT == DT_INT4 ? yacc[i] : acc2[i].x + acc2[i].y;
-  float y = warp_rows4(v, lane);
-  const int ri = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-  const int row = w * RPW + ri;
-  const int n = t * TR + row;
-  const bool own = (lane & 7) == 0 && row < Rt;
-  if (DT == DT_INT8 && own) y *= 256.0f * bf2f(ph.s8[n]);
-  // pair partner (rows 2i, 2i+1 sit in lanes l and l^8)
-  const float yp = __shfl_xor_sync(0xffffffffu, y, 8);
-  if (!own) return true;
+// Epilogue of one output row n (value y); lanes 0..15 call it together, each
+// with its own row of the half-tile; yp is the value of row n ^ 1.
+__device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, int n, float y, float yp, int pos,
+                                              ArgMax& am) {
   switch (ph.epi) {
     case EPI_STORE_BF16:
       reinterpret_cast<uint16_t*>(ph.out)[n] = f2bf(y);
@@ -513,37 +541,34 @@ __device__ bool gemv_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
       break;
     case EPI_RESID: {
       float* res = reinterpret_cast<float*>(ph.out);
-      res[n] = __ldcg(res + n) + rbf(y);
+      res[n] = __ldcg(res + n) + y;
       break;
     }
-    case EPI_SWIGLU: {
-      if ((ri & 1) == 0) {  // even row = gate j, odd row = up j
-        const float gt = rbf(y), up = rbf(yp);
-        const float h = gt / (1.0f + expf(-gt)) * up;
-        reinterpret_cast<uint16_t*>(ph.out)[n >> 1] = f2bf(h);
-      }
+    case EPI_SWIGLU:
+      if ((n & 1) == 0) reinterpret_cast<float*>(ph.out)[n >> 1] = y / (1.0f + expf(-y)) * yp;  // gate, up
       break;
-    }
     case EPI_QKV: {
       const int hd = ph.hd;
       if (n < ph.q_rows + ph.kv_rows) {
-        if ((ri & 1) == 0) {
+        if ((n & 1) == 0) {
           const bool isq = n < ph.q_rows;
           const int nn = isq ? n : n - ph.q_rows;
           const int d = nn % hd;
-          const float2 cssn = P.rope[(size_t)pos * (hd / 2) + d / 2];
-          const float a = rbf(y), bq = rbf(yp);
-          const uint16_t o0 = f2bf(a * cssn.x - bq * cssn.y);
-          const uint16_t o1 = f2bf(a * cssn.y + bq * cssn.x);
-          uint16_t* dst = isq ? const_cast<uint16_t*>(ph.qbuf) + n
-                              : ph.kc + (((size_t)(nn / hd)) * ph.Tmax + pos) * hd + d;
-          dst[0] = o0;
-          dst[1] = o1;
+          const float2 cs = P.rope[(size_t)pos * (hd / 2) + d / 2];
+          const float o0 = y * cs.x - yp * cs.y, o1 = y * cs.y + yp * cs.x;
+          if (isq) {
+            float* q = reinterpret_cast<float*>(ph.qbuf) + n;
+            q[0] = o0;
+            q[1] = o1;
+          } else {
+            uint16_t* k = ph.kc + ((size_t)(nn / hd) * ph.Tmax + pos) * hd + d;
+            k[0] = f2bf(o0);
+            k[1] = f2bf(o1);
+          }
         }
       } else {
         const int nn = n - ph.q_rows - ph.kv_rows;
-        const int d = nn % hd;
-        ph.vc[(((size_t)(nn / hd)) * ph.Tmax + pos) * hd + d] = f2bf(y);
+        ph.vc[((size_t)(nn / hd) * ph.Tmax + pos) * hd + nn % hd] = f2bf(y);
       }
       break;
     }
@@ -554,12 +579,122 @@ __device__ bool gemv_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
     default:
       break;
   }
+}
+
+// One GEMV phase for this CTA.  Slot j of the phase (in producer order)
+// belongs to warp j % NCW.  A warp accumulates its K-blocks of a half-tile in
+// registers (16 rows per lane), reduces them over the lanes, and deposits the
+// 16 row sums in the half-tile's combine buffer; the last contributing warp
+// adds the deposits in warp order and runs the epilogue.
+template <int DT>
+__device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta, int pos, ArgMax& am) {
+  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
+  constexpr int U = E / 4;
+  const int G = P.nctas;
+  const int C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
+  const int ntiles = (ph.N + TR - 1) / TR;
+  const int lane = cs.lane, w = cs.warp;
+  const float4* xs4 = reinterpret_cast<const float4*>(S.xs);
+  uint32_t j = 0;  // slot index within the phase
+  for (int t = first_unit(cta, ph.rot, G); t < ntiles; t += G) {
+    const int Rt = min(TR, ph.N - t * TR);
+    for (int h = 0; h * HROWS < Rt; ++h, ++cs.useq) {
+      const int r0 = h * HROWS;
+      const int bfirst = (int)((uint32_t)(w - (int)(j % NCW) + NCW) % NCW);  // this warp's first K-block
+      const int ncontrib = nb < NCW ? nb : NCW;
+      if (bfirst < nb) {
+        float v[HROWS];
+#pragma unroll
+        for (int r = 0; r < HROWS; ++r) v[r] = 0.0f;
+        for (int b = bfirst; b < nb; b += NCW) {
+          const uint32_t it = cs.it + j + (uint32_t)b;
+          const uint8_t* base;
+          if (!slot_acquire(S, cs, it, P.err, base)) return false;
+          const int Lb = min(KBLK, C - b * KBLK);
+          // lanes past the block width (and rows past the tile) read in-bounds
+          // stale bytes of the slot and are masked out
+          const bool lane_ok = lane < Lb;
+          const int g = b * KBLK + lane;
+          float4 xv[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) xv[u] = xs4[g * U + (u ^ swz(g, U))];
+          const float2* x2 = reinterpret_cast<const float2*>(xv);
+          float xg = 0.f;
+          if (DT == DT_INT4) xg = S.xsum[g];
+#pragma unroll
+          for (int r8 = 0; r8 < HROWS; r8 += 4) {
+            uint4 code[4];
+            uint32_t sz[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              code[r] = *reinterpret_cast<const uint4*>(base + ((r8 + r) * Lb + lane) * 16);
+              if (DT == DT_INT4) sz[r] = *reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF + ((r8 + r) * Lb + lane) * 4);
+            }
+            float2 a[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) a[r] = make_float2(0.f, 0.f);
+            if (DT == DT_INT4) dotR_int4<4>(code, x2, a);
+            else if (DT == DT_INT8) dotR_int8<4>(code, x2, a);
+            else dotR_bf16<4>(code, x2, a);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              float contrib;
+              if (DT == DT_INT4) {
+                const float Sq = fmaf(256.0f, a[r].x, 16.0f * a[r].y);
+                contrib = fmaf(__uint_as_float(sz[r] << 16), Sq, __uint_as_float(sz[r] & 0xFFFF0000u) * xg);
+              } else {
+                contrib = a[r].x + a[r].y;
+              }
+              v[r8 + r] += lane_ok ? contrib : 0.0f;
+            }
+          }
+          slot_release(S, cs, it);
+        }
+        // deposit this warp's 16 row sums, then the last contributor combines
+        const float y = warp_rows16(v, lane);
+        const int buf = (int)(cs.useq % NTB);
+        float* tb = S.tb + (size_t)buf * NCW * HROWS;
+        if ((lane & 1) == 0) tb[w * HROWS + (lane >> 1)] = y;
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          __threadfence_block();
+          last = atomicAdd(S.tbc + buf, 1) == ncontrib - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence_block();
+          float tot = 0.0f;
+          if (lane < HROWS) {
+            for (int ww = 0; ww < NCW; ++ww) {
+              const int bw = (int)((uint32_t)(ww - (int)(j % NCW) + NCW) % NCW);
+              if (bw < nb) tot += tb[ww * HROWS + lane];
+            }
+          }
+          if (lane == 0) S.tbc[buf] = 0;
+          const int r = r0 + lane, n = t * TR + r;
+          if (DT == DT_INT8 && lane < HROWS && r < Rt) tot *= 256.0f * bf2f(ph.s8[n]);
+          const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
+          if (lane < HROWS && r < Rt) gemv_epilogue(ph, P, n, tot, yp, pos, am);
+        }
+      }
+      j += (uint32_t)nb;
+    }
+  }
+  cs.it += j;
   return true;
 }
 
 // ----------------------------------------------------------- attention ---
+// One unit = one kv head x one chunk of positions.  Slot k of the phase (16
+// positions of K and V) belongs to warp k % NCW; lane l owns dims
+// l*DPL..l*DPL+DPL-1.  Each warp keeps an online softmax (m, l, o) per q head
+// of the group; the warps merge in shared memory; a head split over several
+// chunks merges its chunks' (m, l, o) in the CTA that finishes last
+// (log-sum-exp combine).
 template <int HD>
-__device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int u, int nch, int CH, int pos) {
+__device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int u, int nch, int CH, int pos,
+                          uint32_t& j) {
   constexpr int DPL = HD / 32;
   const int gq = ph.Hq / ph.Hkv;
   const int kvh = u / nch, c = u % nch;
@@ -568,100 +703,124 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   const int lane = cs.lane, w = cs.warp;
   float* qs = S.xs;                       // [gq][HD], pre-scaled by 1/sqrt(HD)
   float* sc = S.xs + MAX_GQ * HD;         // [NCW][gq][HD + 2]
+  const int nslots = pe > p0 ? (pe - p0 + ATT_POS_PER_SLOT - 1) / ATT_POS_PER_SLOT : 0;
+  // positions not streamed (the row written by this step) go to the warp
+  // after the last slot's owner; its loads are issued first
+  const int pg = max(pe, p0);
+  const int gw = (int)((j + (uint32_t)nslots) % NCW);
+  uint32_t kpre[DPL / 2], vpre[DPL / 2];
+  const bool has_g = (w == gw) && pg < p1;
+  if (has_g) {
+    const size_t off = ((size_t)kvh * ph.Tmax + pg) * HD + lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL / 2; ++d) {
+      kpre[d] = __ldcg(reinterpret_cast<const unsigned*>(ph.kc + off) + d);
+      vpre[d] = __ldcg(reinterpret_cast<const unsigned*>(ph.vc + off) + d);
+    }
+  }
   const float scale = rsqrtf((float)HD);
-  for (int i = cs.ctid; i < gq * HD; i += NCW * 32)
-    qs[i] = bf2f(__ldcg(ph.qbuf + (size_t)kvh * gq * HD + i)) * scale;
+  for (int i = cs.ctid; i < gq * HD; i += NCW * 32) {
+    const size_t qi = (size_t)kvh * gq * HD + i;
+    const float qv = ph.q_f32 ? __ldcg(reinterpret_cast<const float*>(ph.qbuf) + qi)
+                              : bf2f(__ldcg(reinterpret_cast<const uint16_t*>(ph.qbuf) + qi));
+    qs[i] = qv * scale;
+  }
   if (!cta_sync(S, cs, P.err)) return false;
 
   float m[MAX_GQ], l[MAX_GQ], o[MAX_GQ][DPL];
 #pragma unroll
-  for (int j = 0; j < MAX_GQ; ++j) {
-    m[j] = -INFINITY;
-    l[j] = 0.f;
+  for (int jj = 0; jj < MAX_GQ; ++jj) {
+    m[jj] = -INFINITY;
+    l[jj] = 0.f;
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) o[j][d] = 0.f;
+    for (int d = 0; d < DPL; ++d) o[jj][d] = 0.f;
   }
-  auto consume = [&](const uint16_t* krow, const uint16_t* vrow, bool global) {
+  auto consume = [&](const uint32_t* kk, const uint32_t* vv) {
     float kf[DPL], vf[DPL];
 #pragma unroll
-    for (int d = 0; d < DPL; d += 2) {
-      const uint32_t kk = global ? __ldcg(reinterpret_cast<const unsigned*>(krow + lane * DPL + d))
-                                 : *reinterpret_cast<const uint32_t*>(krow + lane * DPL + d);
-      const uint32_t vv = global ? __ldcg(reinterpret_cast<const unsigned*>(vrow + lane * DPL + d))
-                                 : *reinterpret_cast<const uint32_t*>(vrow + lane * DPL + d);
-      kf[d] = __uint_as_float(kk << 16);
-      kf[d + 1] = __uint_as_float(kk & 0xFFFF0000u);
-      vf[d] = __uint_as_float(vv << 16);
-      vf[d + 1] = __uint_as_float(vv & 0xFFFF0000u);
+    for (int d = 0; d < DPL / 2; ++d) {
+      kf[2 * d] = __uint_as_float(kk[d] << 16);
+      kf[2 * d + 1] = __uint_as_float(kk[d] & 0xFFFF0000u);
+      vf[2 * d] = __uint_as_float(vv[d] << 16);
+      vf[2 * d + 1] = __uint_as_float(vv[d] & 0xFFFF0000u);
     }
 #pragma unroll
-    for (int j = 0; j < MAX_GQ; ++j) {
-      if (j < gq) {
+    for (int jj = 0; jj < MAX_GQ; ++jj) {
+      if (jj < gq) {
         float dot = 0.f;
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) dot = fmaf(qs[j * HD + lane * DPL + d], kf[d], dot);
+        for (int d = 0; d < DPL; ++d) dot = fmaf(qs[jj * HD + lane * DPL + d], kf[d], dot);
 #pragma unroll
         for (int of = 16; of; of >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, of);
-        const float mn = fmaxf(m[j], dot);
-        const float corr = expf(m[j] - mn), p = expf(dot - mn);
-        l[j] = fmaf(l[j], corr, p);
+        const float mn = fmaxf(m[jj], dot);
+        const float corr = expf(m[jj] - mn), p = expf(dot - mn);
+        l[jj] = fmaf(l[jj], corr, p);
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) o[j][d] = fmaf(o[j][d], corr, p * vf[d]);
-        m[j] = mn;
+        for (int d = 0; d < DPL; ++d) o[jj][d] = fmaf(o[jj][d], corr, p * vf[d]);
+        m[jj] = mn;
       }
     }
   };
-  const uint32_t rowe = HD;  // elements per cache row
-  for (int p = p0; p < pe; p += ATT_POS_PER_SLOT) {
-    const int np = min(ATT_POS_PER_SLOT, pe - p);
+  for (int k = (int)((uint32_t)(w - (int)(j % NCW) + NCW) % NCW); k < nslots; k += NCW) {
+    const uint32_t it = cs.it + j + (uint32_t)k;
+    const int np = min(ATT_POS_PER_SLOT, pe - (p0 + k * ATT_POS_PER_SLOT));
     const uint8_t* base;
-    if (!slot_acquire(S, cs, P.err, base)) return false;
+    if (!slot_acquire(S, cs, it, P.err, base)) return false;
     const uint16_t* kb = reinterpret_cast<const uint16_t*>(base);
-    const uint16_t* vb = kb + ATT_POS_PER_SLOT * rowe;
-    for (int q = w * 4; q < w * 4 + 4; ++q)
-      if (q < np) consume(kb + q * rowe, vb + q * rowe, false);
-    slot_release(S, cs);
-  }
-  if (w == 0) {
-    for (int p = max(pe, p0); p < p1; ++p) {
-      const size_t off = ((size_t)kvh * ph.Tmax + p) * HD;
-      consume(ph.kc + off, ph.vc + off, true);
+    const uint16_t* vb = kb + ATT_POS_PER_SLOT * HD;
+    for (int q = 0; q < np; ++q) {
+      uint32_t kk[DPL / 2], vv[DPL / 2];
+#pragma unroll
+      for (int d = 0; d < DPL / 2; ++d) {
+        kk[d] = reinterpret_cast<const uint32_t*>(kb + q * HD + lane * DPL)[d];
+        vv[d] = reinterpret_cast<const uint32_t*>(vb + q * HD + lane * DPL)[d];
+      }
+      consume(kk, vv);
     }
+    slot_release(S, cs, it);
   }
-  // combine the warps of this CTA
+  j += (uint32_t)nslots;
+  if (has_g) consume(kpre, vpre);
+  // merge the warps of this CTA
 #pragma unroll
-  for (int j = 0; j < MAX_GQ; ++j) {
-    if (j < gq) {
-      float* dst = sc + (w * gq + j) * (HD + 2);
+  for (int jj = 0; jj < MAX_GQ; ++jj) {
+    if (jj < gq) {
+      float* dst = sc + (w * gq + jj) * (HD + 2);
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) dst[2 + lane * DPL + d] = o[j][d];
+      for (int d = 0; d < DPL; ++d) dst[2 + lane * DPL + d] = o[jj][d];
       if (lane == 0) {
-        dst[0] = m[j];
-        dst[1] = l[j];
+        dst[0] = m[jj];
+        dst[1] = l[jj];
       }
     }
   }
   if (!cta_sync(S, cs, P.err)) return false;
   const int stride = HD + 2;
   for (int i = cs.ctid; i < gq * HD; i += NCW * 32) {
-    const int j = i / HD, d = i % HD;
+    const int jj = i / HD, d = i % HD;
     float M = -INFINITY;
-    for (int ww = 0; ww < NCW; ++ww) M = fmaxf(M, sc[(ww * gq + j) * stride]);
+    for (int ww = 0; ww < NCW; ++ww) M = fmaxf(M, sc[(ww * gq + jj) * stride]);
     float L = 0.f, O = 0.f;
     for (int ww = 0; ww < NCW; ++ww) {
-      const float* s = sc + (ww * gq + j) * stride;
+      const float* s = sc + (ww * gq + jj) * stride;
       const float e = s[1] > 0.f ? expf(s[0] - M) : 0.f;
       L = fmaf(s[1], e, L);
       O = fmaf(s[2 + d], e, O);
     }
-    const int h = kvh * gq + j;
-    float* part = ph.part + ((size_t)h * nch + c) * stride;
-    part[2 + d] = O;
-    if (d == 0) {
-      part[0] = M;
-      part[1] = L;
+    const int hq = kvh * gq + jj;
+    if (nch == 1) {  // the whole head was here
+      if (ph.out_f32) reinterpret_cast<float*>(ph.attn_out)[(size_t)hq * HD + d] = O / L;
+      else reinterpret_cast<uint16_t*>(ph.attn_out)[(size_t)hq * HD + d] = f2bf(O / L);
+    } else {
+      float* part = ph.part + ((size_t)hq * nch + c) * stride;
+      part[2 + d] = O;
+      if (d == 0) {
+        part[0] = M;
+        part[1] = L;
+      }
     }
   }
+  if (nch == 1) return true;
   __threadfence();
   if (!cta_sync(S, cs, P.err)) return false;
   if (cs.ctid == 0) {
@@ -672,8 +831,8 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   if (S.bcast[0]) {
     __threadfence();
     for (int i = cs.ctid; i < gq * HD; i += NCW * 32) {
-      const int j = i / HD, d = i % HD, h = kvh * gq + j;
-      const float* pb = ph.part + (size_t)h * nch * stride;
+      const int jj = i / HD, d = i % HD, hq = kvh * gq + jj;
+      const float* pb = ph.part + (size_t)hq * nch * stride;
       float M = -INFINITY;
       for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(pb + cc * stride));
       float L = 0.f, O = 0.f;
@@ -682,7 +841,8 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
         L = fmaf(__ldcg(pb + cc * stride + 1), e, L);
         O = fmaf(__ldcg(pb + cc * stride + 2 + d), e, O);
       }
-      ph.attn_out[(size_t)h * HD + d] = f2bf(O / L);
+      if (ph.out_f32) reinterpret_cast<float*>(ph.attn_out)[(size_t)hq * HD + d] = O / L;
+      else reinterpret_cast<uint16_t*>(ph.attn_out)[(size_t)hq * HD + d] = f2bf(O / L);
     }
     if (cs.ctid == 0) ph.tick[kvh] = 0u;
   }
@@ -700,7 +860,7 @@ __device__ bool argmax_finish(const Params& P, const Smem& S, Cons& cs, int cta,
   }
   if (cs.lane == 0) {
     S.red[cs.warp] = am.v;
-    S.bcast[cs.warp] = am.i;  // bcast has room for 8 ints
+    S.bcast[cs.warp] = am.i;
   }
   if (!cta_sync(S, cs, P.err)) return false;
   if (cs.ctid == 0) {
@@ -730,11 +890,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   if (tid == 0) {
     for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&S.full[i], 1);
-      mbar_init(&S.empty[i], NCW);
+      mbar_init(&S.empty[i], 1);
     }
     mbar_init(S.cbar, NCW * 32);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (tid < NTB) S.tbc[tid] = 0;
   __syncthreads();
   const int pos = P.d_pos ? *P.d_pos : P.pos_const;
   // Reject a position or token that would index outside the cache, the RoPE
@@ -757,6 +918,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   Cons cs;
   cs.it = 0;
   cs.cphase = 0;
+  cs.useq = 0;
   cs.warp = warp;
   cs.lane = lane;
   cs.ctid = tid;
@@ -780,28 +942,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     if (ph.kind == PH_GEMV) {
       if (!stage_x(ph, P, S, cs, cta)) return;
       if (tr) tr[2] = gtimer();
-      const int ntiles = (ph.N + TR - 1) / TR;
-      for (int t = first_unit(cta, ph.rot, G); t < ntiles; t += G) {
-        bool ok;
-        if (ph.dtype == DT_INT4) ok = gemv_unit<DT_INT4>(ph, P, S, cs, t, pos, am);
-        else if (ph.dtype == DT_INT8) ok = gemv_unit<DT_INT8>(ph, P, S, cs, t, pos, am);
-        else ok = gemv_unit<DT_BF16>(ph, P, S, cs, t, pos, am);
-        if (!ok) return;
-      }
+      bool ok;
+      if (ph.dtype == DT_INT4) ok = gemv_phase<DT_INT4>(ph, P, S, cs, cta, pos, am);
+      else if (ph.dtype == DT_INT8) ok = gemv_phase<DT_INT8>(ph, P, S, cs, cta, pos, am);
+      else ok = gemv_phase<DT_BF16>(ph, P, S, cs, cta, pos, am);
+      if (!ok) return;
       if (ph.epi == EPI_LOGITS) any_logits = true;
     } else if (ph.kind == PH_ATTN) {
+      if (tr) tr[2] = tr[1];
       const int T = pos + 1;
       int CH, nch;
       attn_split(T, ph.Hkv, P.unit_target, CH, nch);
       const int nunits = ph.Hkv * nch;
+      uint32_t j = 0;
       for (int u = first_unit(cta, ph.rot, G); u < nunits; u += G) {
-        const bool ok = ph.hd == 128 ? attn_unit<128>(ph, P, S, cs, u, nch, CH, pos)
-                                     : attn_unit<64>(ph, P, S, cs, u, nch, CH, pos);
+        const bool ok = ph.hd == 128 ? attn_unit<128>(ph, P, S, cs, u, nch, CH, pos, j)
+                                     : attn_unit<64>(ph, P, S, cs, u, nch, CH, pos, j);
         if (!ok) return;
       }
+      cs.it += j;
     }
     if (tr) {
-      if (ph.kind != PH_GEMV) tr[2] = tr[1];
       tr[3] = gtimer();
       tr[6] = cs.starved;
     }
@@ -940,10 +1101,10 @@ int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq
   Params p = base_params();
   Phase& ph = p.single;
   ph.kind = PH_ATTN;
-  ph.qbuf = (const uint16_t*)q;
+  ph.qbuf = const_cast<void*>(q);
   ph.kc = (uint16_t*)kcache;
   ph.vc = (uint16_t*)vcache;
-  ph.attn_out = (uint16_t*)out;
+  ph.attn_out = out;
   ph.Hq = Hq;
   ph.Hkv = Hkv;
   ph.hd = hd;
@@ -953,12 +1114,8 @@ int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq
   ph.part = (float*)ws;
   ph.tick = (unsigned*)((uint8_t*)ws + part_bytes);
   GF_CUDA(cudaMemsetAsync(ph.tick, 0, Hkv * sizeof(unsigned), (cudaStream_t)stream));
-  // same split rule as the kernel: units = Hkv * nch
-  const int T = pos + 1;
-  int want = (sms + Hkv - 1) / Hkv, maxch = (T + 31) / 32;
-  int nch = want < maxch ? want : maxch;
-  const int CH = ((T + nch - 1) / nch + 31) / 32 * 32;
-  nch = (T + CH - 1) / CH;
+  int CH, nch;
+  attn_split(pos + 1, Hkv, sms, CH, nch);
   const int units = Hkv * nch;
   const int grid = units < sms ? units : sms;
   p.nctas = grid;

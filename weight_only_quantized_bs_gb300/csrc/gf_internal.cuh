@@ -48,31 +48,33 @@ __host__ __device__ inline long long block_offset(int dt, int C, int t, int Rt, 
 // ------------------------------------------------------- engine sizes ----
 constexpr int NCW = 8;                       // consumer warps per CTA
 constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp
-constexpr int RPW = TR / NCW;                // rows per consumer warp (4)
-constexpr int SLOT_BYTES = 20480;            // one int4 K-block of a full tile
-constexpr int NSLOT = 7;
+constexpr int HROWS = 16;                    // rows of a slot: half a tile
+constexpr int SLOT_BYTES = 10240;            // codes of 16 rows x 32 chunks + int4 scale words
+constexpr int SLOT_SZ_OFF = 8192;            // int4 scale words inside a slot
+constexpr int NSLOT = 14;
+constexpr int NTB = 32;                      // tile-half combine buffers
 constexpr int OFF_RING = 0;
 constexpr int OFF_X = OFF_RING + NSLOT * SLOT_BYTES;     // fp32 x, swizzled
-constexpr int OFF_XSUM = OFF_X + KMAX * 4;               // float4 per chunk
-constexpr int OFF_BAR = OFF_XSUM + (KMAX / 16) * 16;     // mbarriers
-constexpr int OFF_MISC = OFF_BAR + 128;
+constexpr int OFF_XSUM = OFF_X + KMAX * 4;               // fp32 sum of x per 32-wide group
+constexpr int OFF_TB = OFF_XSUM + (KMAX / 32) * 4 + 256;  // [NTB][NCW][HROWS] partial row sums
+constexpr int OFF_TBC = OFF_TB + NTB * NCW * HROWS * 4;  // [NTB] arrival counters
+constexpr int OFF_BAR = OFF_TBC + NTB * 4;               // mbarriers
+constexpr int OFF_MISC = OFF_BAR + 256;
 constexpr int SMEM_BYTES = OFF_MISC + 512;
-constexpr int ATT_POS_PER_SLOT = 32;
+constexpr int ATT_POS_PER_SLOT = 16;
 constexpr int MAX_GQ = 8;                    // q heads per kv head
 constexpr int MAX_M = 8;                     // rows of a verify pass
 
 // --------------------------------------------------------------- phases --
-enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1, PH_MOE_ROUTE = 2 };
-enum XSrc { X_NONE = 0, X_BF16 = 1, X_NORM = 2, X_EMBED_NORM = 3 };
+enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1 };
+enum XSrc { X_NONE = 0, X_BF16 = 1, X_NORM = 2, X_EMBED_NORM = 3, X_F32 = 4 };
 enum Epi {
   EPI_STORE_BF16 = 0,
   EPI_STORE_F32 = 1,
-  EPI_QKV = 2,       // RoPE q and k, q -> q buffer, k/v -> cache row at pos
-  EPI_RESID = 3,     // resid[n] += bf16(y)
-  EPI_SWIGLU = 4,    // h[n/2] = bf16(silu(bf16 gate) * bf16 up)
-  EPI_LOGITS = 5,    // logits[n] = y (fp32), running argmax
-  EPI_MOE_GU = 6,    // SwiGLU into the expert slot's h
-  EPI_MOE_DOWN = 7   // resid[n] += bf16(w1 bf16(y1) + w2 bf16(y2))
+  EPI_QKV = 2,       // RoPE q and k; q -> fp32 q buffer, k, v -> bf16 cache row at pos
+  EPI_RESID = 3,     // resid[n] += y
+  EPI_SWIGLU = 4,    // h[n/2] = silu(gate) * up (fp32)
+  EPI_LOGITS = 5     // logits[n] = y (fp32), running argmax
 };
 enum ErrCode {
   ERR_NONE = 0,
@@ -96,24 +98,35 @@ struct Phase {
   int epi;
   const uint8_t* W;        // packed weights
   const uint16_t* s8;      // int8 row scales
-  long long expert_stride; // MoE: bytes between experts' packed matrices
   int xsrc;
-  const void* xptr;        // bf16 vector, or fp32 residual for X_NORM
+  const void* xptr;        // bf16 or fp32 vector, or the fp32 residual for X_NORM
   const uint16_t* gain;    // RMSNorm gain
   float eps;
   void* out;               // epilogue target
-  int layer;
   int q_rows, kv_rows;     // EPI_QKV split
   // attention (also used by EPI_QKV)
-  const uint16_t* qbuf;
+  void* qbuf;              // q: fp32 (q_f32) or bf16 [Hq][hd]
   uint16_t* kc;            // cache base for this layer [Hkv][Tmax][hd]
   uint16_t* vc;
-  uint16_t* attn_out;
+  void* attn_out;          // fp32 (out_f32) or bf16 [Hq][hd]
+  int q_f32, out_f32;
   int Hq, Hkv, hd, Tmax;
   float* part;             // [Hq][nch_max][hd + 2] partials
   unsigned* tick;          // [Hkv] combine tickets
   int stream_cur;          // 1: the row at pos is in memory before launch (standalone)
 };
+
+// Split of a decode attention over positions 0..T-1 into nch chunks of CH
+// positions per kv head (CH a multiple of the slot size), aiming at about
+// `target` units in all.  Kernel and host use this one definition.
+__host__ __device__ inline void attn_split(int T, int Hkv, int target, int& CH, int& nch) {
+  int want = (target + Hkv - 1) / Hkv;
+  if (want < 1) want = 1;
+  const int maxch = (T + ATT_POS_PER_SLOT - 1) / ATT_POS_PER_SLOT;
+  nch = want < maxch ? want : maxch;
+  CH = ((T + nch - 1) / nch + ATT_POS_PER_SLOT - 1) / ATT_POS_PER_SLOT * ATT_POS_PER_SLOT;
+  nch = (T + CH - 1) / CH;
+}
 
 struct Params {
   const Phase* prog;   // device program (nullptr: use `single`)

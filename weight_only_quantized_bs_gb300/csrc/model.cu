@@ -30,7 +30,7 @@ struct gf_kv {
   int Tmax = 0;
   uint16_t *kc = nullptr, *vc = nullptr;
   float2* rope = nullptr;
-  uint16_t *qbuf = nullptr, *attn = nullptr, *h = nullptr;
+  float *qbuf = nullptr, *attn = nullptr, *h = nullptr;
   float* resid = nullptr;
   float* part = nullptr;
   float* amax_val = nullptr;
@@ -190,9 +190,9 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->kc, cache_elems * 2))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->vc, cache_elems * 2))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->rope, (size_t)Tmax * (hd / 2) * sizeof(float2)))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->qbuf, (size_t)Hq * hd * 2))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->attn, (size_t)Hq * hd * 2))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->h, (size_t)c.ffn * 2))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->qbuf, (size_t)Hq * hd * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->attn, (size_t)Hq * hd * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->h, (size_t)c.ffn * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->resid, (size_t)c.d * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->part, (size_t)Hq * nch_max * (hd + 2) * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_val, (size_t)G * 4))) break;
@@ -259,6 +259,8 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[1].kc = kcl;
     P[1].vc = vcl;
     P[1].attn_out = kv->attn;
+    P[1].q_f32 = 1;
+    P[1].out_f32 = 1;
     P[1].Hq = Hq;
     P[1].Hkv = Hkv;
     P[1].hd = hd;
@@ -269,7 +271,7 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[1].rot = (int)(cum_units % G);
     // o projection + residual
     gemv(P[2], m->o[l]);
-    P[2].xsrc = X_BF16;
+    P[2].xsrc = X_F32;
     P[2].xptr = kv->attn;
     P[2].epi = EPI_RESID;
     P[2].out = kv->resid;
@@ -283,7 +285,7 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[3].out = kv->h;
     // down + residual
     gemv(P[4], m->dn[l]);
-    P[4].xsrc = X_BF16;
+    P[4].xsrc = X_F32;
     P[4].xptr = kv->h;
     P[4].epi = EPI_RESID;
     P[4].out = kv->resid;
