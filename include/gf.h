@@ -117,7 +117,7 @@ int gf_gemv_w4g(const void* x, const void* qpacked, int N, int K, int G, void* y
  * range is split across CTAs and merged with a log-sum-exp combine; the
  * caller provides `ws` of at least gf_attn_workspace_bytes() bytes (scratch,
  * contents undefined after the call).  hd must be 64 or 128, Hq % Hkv == 0,
- * Hq / Hkv <= 8, 0 <= pos < Tmax. */
+ * Hq / Hkv <= 4, 0 <= pos < Tmax. */
 size_t gf_attn_workspace_bytes(int Hq, int Hkv, int hd);
 int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq, int Hkv, int hd,
                    int Tmax, int pos, void* out, void* ws, size_t ws_bytes, gf_stream stream);
@@ -130,7 +130,8 @@ int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq
  * counterpart of this call; it exists only for such callers.
  * Scratch: a static device array of GF_NOALLOC_ATTN_SCRATCH bytes in the
  * library, held by every GPU that loads the library until the process exits.
- * Shapes needing more (Hq * ceil(SMs / Hkv) * (hd + 2) * 4 + 256 bytes)
+ * Shapes needing more (Hq * ceil(SMs / Hkv) * (hd + 2) * 4 bytes, plus 4 per kv
+ * head rounded up to 256)
  * return GF_EINVAL with the size in gf_last_error().  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  Every call

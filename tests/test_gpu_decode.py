@@ -78,7 +78,7 @@ def test_decode_small_hd128(dtype):
     check(got, am, ref)
 
 
-def test_decode_gqa8_ragged():
-    cfg = models.config("tiny", n_heads=8, n_kv_heads=1, d=512, head_dim=64, ffn=736, vocab=1003)
+def test_decode_gqa4_ragged():
+    cfg = models.config("tiny", n_heads=8, n_kv_heads=2, d=512, head_dim=64, ffn=736, vocab=1003)
     got, am, ref = run_teacher_forced(cfg, "int4", seed=13, n_prompt=5, n_gen=40, tmax=64)
     check(got, am, ref)

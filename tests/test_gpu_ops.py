@@ -123,7 +123,7 @@ def _attn_case(Hq, Hkv, hd, T, Tmax, seed):
 
 
 @pytest.mark.parametrize("Hq,Hkv,hd,T,Tmax", [
-    (4, 2, 64, 1, 8), (4, 2, 64, 33, 40), (8, 1, 64, 100, 128), (32, 32, 128, 6, 2048),
+    (4, 2, 64, 1, 8), (4, 2, 64, 33, 40), (4, 1, 64, 100, 128), (8, 2, 128, 300, 512), (32, 32, 128, 6, 2048),
     (32, 32, 128, 206, 2048), (32, 8, 128, 128, 8192), (32, 8, 128, 1024, 8192), (32, 8, 128, 8192, 8192)])
 def test_decode_attn(Hq, Hkv, hd, T, Tmax):
     out, ref = _attn_case(Hq, Hkv, hd, T, Tmax, seed=T)

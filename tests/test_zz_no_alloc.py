@@ -51,7 +51,7 @@ def test_noalloc_rejects_shapes_beyond_the_scratch():
     L = gf.lib()
     dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")
     p = ctypes.c_void_p(dummy.data_ptr())
-    # 4096 query heads over 512 kv heads need 4096 * 130 * 4 bytes (> 2 MiB)
-    rc = L.gf_decode_attn_noalloc(p, p, p, 4096, 512, 128, 16, 0, p, None)
+    # 4096 query heads over 1024 kv heads need 4096 * 130 * 4 bytes (> 2 MiB)
+    rc = L.gf_decode_attn_noalloc(p, p, p, 4096, 1024, 128, 16, 0, p, None)
     assert rc == 1
     assert b"static scratch" in L.gf_last_error()

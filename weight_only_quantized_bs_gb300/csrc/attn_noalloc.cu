@@ -57,13 +57,14 @@ int gf_decode_attn_noalloc(const void* q, const void* kcache, const void* vcache
     set_error("gf_decode_attn_noalloc: cannot query the device");
     return GF_ECUDA;
   }
-  // same scratch shape as gf_decode_attn: partials, then 256 bytes of tickets
+  // same scratch shape as gf_decode_attn: partials, then one ticket per kv head
   const int nch_max = (sms + Hkv - 1) / Hkv;
   const size_t part_bytes = (size_t)Hq * nch_max * (hd + 2) * sizeof(float);
-  if (part_bytes + 256 > (size_t)GF_NOALLOC_ATTN_SCRATCH || Hkv > 64) {
+  const size_t need = part_bytes + ((size_t)Hkv * sizeof(unsigned) + 255) / 256 * 256;
+  if (need > (size_t)GF_NOALLOC_ATTN_SCRATCH) {
     set_error("gf_decode_attn_noalloc: needs %zu bytes of scratch for Hq=%d Hkv=%d hd=%d; the static scratch holds "
               "%d bytes (use gf_decode_attn with a workspace instead)",
-              part_bytes + 256, Hq, Hkv, hd, GF_NOALLOC_ATTN_SCRATCH);
+              need, Hq, Hkv, hd, GF_NOALLOC_ATTN_SCRATCH);
     return GF_EINVAL;
   }
   int dev = 0;

@@ -3,11 +3,12 @@
 // One CTA per SM runs a program of phases (a single GEMV or attention for the
 // standalone calls; every layer of a decode step for gf_decode_step).  In
 // each CTA one producer thread streams the CTA's weight half-tiles (16 rows x
-// one K-block) and KV-cache rows from HBM into a ring of 14 shared-memory
+// one K-block) and KV-cache rows from HBM into a ring of 16 shared-memory
 // slots with bulk asynchronous copies (cp.async.bulk, completion counted on
 // an mbarrier, L2 evict-first hint), running ahead across phase boundaries
 // because the weight stream does not depend on activations.  Each slot
-// belongs to one of eight consumer warps (round robin), which dequantises the
+// belongs to one of eight consumer warps (stream index mod 8, so a ring entry
+// always serves the same warp), which dequantises the
 // int8 / int4 codes of its 16 rows in registers against an fp32 copy of the
 // input vector held in shared memory and releases the slot; the K-block
 // partial sums of a half-tile meet in shared memory, where the last warp to
@@ -441,64 +442,50 @@ __device__ __forceinline__ uint32_t word_of(const uint4& c, int j) {
   return j == 0 ? c.x : j == 1 ? c.y : j == 2 ? c.z : c.w;
 }
 
-// int4: view i of a code word (rotated right by 8i) carries code k = 8j+2i in
-// bits 15..18 and k = 8j+2i+1 in bits 19..22.  OR-ing the exponent of 1.0f
-// turns them into 1 + q/256 and 1 + q/16 exactly (one LOP3 each); subtracting
-// 1 (exact) leaves q/256 and q/16, which multiply the fp32 input pair with one
-// packed FMA.  R rows are interleaved so that their accumulator chains
-// overlap.  Result per row: (sum_even q x / 256, sum_odd q x / 16) over the
-// lane's 32-wide group.
-template <int R>
-__device__ __forceinline__ void dotR_int4(const uint4* c, const float2* x2, float2* acc) {
+// The dequantising dot products work on one 32-bit word of a 16-byte chunk at
+// a time (j = 0..3, a run-time loop so that the body stays small), for all 16
+// rows of the slot at once so that their accumulator chains overlap.
+//
+// int4: view i of a word (rotated right by 8i) carries code k = 8j+2i in bits
+// 15..18 and k = 8j+2i+1 in bits 19..22.  OR-ing the exponent of 1.0f turns
+// them into 1 + q/256 and 1 + q/16 exactly (one LOP3 each); subtracting 1
+// (exact, packed) leaves q/256 and q/16, which multiply the fp32 input pair
+// with one packed FMA.  acc[r] = (sum_even q x / 256, sum_odd q x / 16).
+__device__ __forceinline__ void word_int4(const uint32_t* wr, const float2* x2, float2* acc) {
   const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int i = 0; i < 4; ++i) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const uint32_t wj = word_of(c[r], j);
-        const uint32_t v = i ? __funnelshift_r(wj, wj, 8 * i) : wj;
-        const float lo = __uint_as_float((v & 0x00078000u) | 0x3F800000u);
-        const float hi = __uint_as_float((v & 0x00780000u) | 0x3F800000u);
-        acc[r] = ffma2(__fadd2_rn(make_float2(lo, hi), m1), x2[4 * j + i], acc[r]);
-      }
+    for (int r = 0; r < HROWS; ++r) {
+      const uint32_t v = i ? __funnelshift_r(wr[r], wr[r], 8 * i) : wr[r];
+      const float lo = __uint_as_float((v & 0x00078000u) | 0x3F800000u);
+      const float hi = __uint_as_float((v & 0x00780000u) | 0x3F800000u);
+      acc[r] = ffma2(__fadd2_rn(make_float2(lo, hi), m1), x2[i], acc[r]);
     }
   }
 }
 // int8: view i carries code k = 4j+i in bits 15..22; XOR with 0x3FC00000 sets
 // the exponent of 1.0f and flips the sign bit, giving 1 + (q + 128)/256;
-// subtracting 1.5 (exact) leaves q/256.  Result per row: q x / 256 by parity
-// of k.
-template <int R>
-__device__ __forceinline__ void dotR_int8(const uint4* c, const float2* x2, float2* acc) {
+// subtracting 1.5 (exact) leaves q/256.  acc[r] = q x / 256 by parity of k.
+__device__ __forceinline__ void word_int8(const uint32_t* wr, const float2* x2, float2* acc) {
   const float2 off = make_float2(-1.5f, -1.5f);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int r = 0; r < HROWS; ++r) {
+    float f[4];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const uint32_t wj = word_of(c[r], j);
-      float f[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t v = i ? __funnelshift_r(wj, wj, 8 * i) : wj;
-        f[i] = __uint_as_float((v & 0x007F8000u) ^ 0x3FC00000u);
-      }
-      acc[r] = ffma2(__fadd2_rn(make_float2(f[0], f[1]), off), x2[2 * j], acc[r]);
-      acc[r] = ffma2(__fadd2_rn(make_float2(f[2], f[3]), off), x2[2 * j + 1], acc[r]);
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t v = i ? __funnelshift_r(wr[r], wr[r], 8 * i) : wr[r];
+      f[i] = __uint_as_float((v & 0x007F8000u) ^ 0x3FC00000u);
     }
+    acc[r] = ffma2(__fadd2_rn(make_float2(f[0], f[1]), off), x2[0], acc[r]);
+    acc[r] = ffma2(__fadd2_rn(make_float2(f[2], f[3]), off), x2[1], acc[r]);
   }
 }
-template <int R>
-__device__ __forceinline__ void dotR_bf16(const uint4* c, const float2* x2, float2* acc) {
+// bf16: a word holds two weights, k = 2j and 2j+1.
+__device__ __forceinline__ void word_bf16(const uint32_t* wr, const float2* x2, float2* acc) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const uint32_t wj = word_of(c[r], j);
-      acc[r] = ffma2(make_float2(__uint_as_float(wj << 16), __uint_as_float(wj & 0xFFFF0000u)), x2[j], acc[r]);
-    }
-  }
+  for (int r = 0; r < HROWS; ++r)
+    acc[r] = ffma2(make_float2(__uint_as_float(wr[r] << 16), __uint_as_float(wr[r] & 0xFFFF0000u)), x2[0], acc[r]);
 }
 
 // Sums each of 16 per-lane values over the 32 lanes; afterwards lane l holds
@@ -539,11 +526,11 @@ __device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, 
     case EPI_STORE_F32:
       reinterpret_cast<float*>(ph.out)[n] = y;
       break;
-    case EPI_RESID: {
-      float* res = reinterpret_cast<float*>(ph.out);
-      res[n] = __ldcg(res + n) + y;
+    case EPI_RESID:
+      // one writer per row and phase, phases ordered by grid barriers: the
+      // fire-and-forget add is deterministic and hides the load latency
+      atomicAdd(reinterpret_cast<float*>(ph.out) + n, y);
       break;
-    }
     case EPI_SWIGLU:
       if ((n & 1) == 0) reinterpret_cast<float*>(ph.out)[n >> 1] = y / (1.0f + expf(-y)) * yp;  // gate, up
       break;
@@ -581,8 +568,8 @@ __device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, 
   }
 }
 
-// One GEMV phase for this CTA.  Slot j of the phase (in producer order)
-// belongs to warp j % NCW.  A warp accumulates its K-blocks of a half-tile in
+// One GEMV phase for this CTA.  Slot X of the stream (in producer order)
+// belongs to warp X % NCW.  A warp accumulates its K-blocks of a half-tile in
 // registers (16 rows per lane), reduces them over the lanes, and deposits the
 // 16 row sums in the half-tile's combine buffer; the last contributing warp
 // adds the deposits in warp order and runs the epilogue.
@@ -600,7 +587,8 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
     const int Rt = min(TR, ph.N - t * TR);
     for (int h = 0; h * HROWS < Rt; ++h, ++cs.useq) {
       const int r0 = h * HROWS;
-      const int bfirst = (int)((uint32_t)(w - (int)(j % NCW) + NCW) % NCW);  // this warp's first K-block
+      const int own0 = (int)((cs.it + j) % NCW);                              // owner of K-block 0
+      const int bfirst = (w - own0 + NCW) % NCW;                               // this warp's first K-block
       const int ncontrib = nb < NCW ? nb : NCW;
       if (bfirst < nb) {
         float v[HROWS];
@@ -615,38 +603,49 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
           // stale bytes of the slot and are masked out
           const bool lane_ok = lane < Lb;
           const int g = b * KBLK + lane;
-          float4 xv[U];
+          const int sw = swz(g, U);
+          float2 acc[HROWS];
 #pragma unroll
-          for (int u = 0; u < U; ++u) xv[u] = xs4[g * U + (u ^ swz(g, U))];
-          const float2* x2 = reinterpret_cast<const float2*>(xv);
-          float xg = 0.f;
-          if (DT == DT_INT4) xg = S.xsum[g];
-#pragma unroll
-          for (int r8 = 0; r8 < HROWS; r8 += 4) {
-            uint4 code[4];
-            uint32_t sz[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              code[r] = *reinterpret_cast<const uint4*>(base + ((r8 + r) * Lb + lane) * 16);
-              if (DT == DT_INT4) sz[r] = *reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF + ((r8 + r) * Lb + lane) * 4);
+          for (int r = 0; r < HROWS; ++r) acc[r] = make_float2(0.f, 0.f);
+          const uint32_t* wbase = reinterpret_cast<const uint32_t*>(base) + lane * 4;
+#pragma unroll 1
+          for (int jw = 0; jw < 4; ++jw) {
+            // inputs of word jw: int4 x[8jw..8jw+7], int8 x[4jw..4jw+3], bf16 x[2jw, 2jw+1]
+            float2 x2[4];
+            if (DT == DT_INT4) {
+              const float4 xa = xs4[g * U + ((2 * jw) ^ sw)], xb = xs4[g * U + ((2 * jw + 1) ^ sw)];
+              x2[0] = make_float2(xa.x, xa.y);
+              x2[1] = make_float2(xa.z, xa.w);
+              x2[2] = make_float2(xb.x, xb.y);
+              x2[3] = make_float2(xb.z, xb.w);
+            } else if (DT == DT_INT8) {
+              const float4 xa = xs4[g * U + (jw ^ sw)];
+              x2[0] = make_float2(xa.x, xa.y);
+              x2[1] = make_float2(xa.z, xa.w);
+            } else {
+              const float4 xa = xs4[g * U + ((jw >> 1) ^ sw)];
+              x2[0] = (jw & 1) ? make_float2(xa.z, xa.w) : make_float2(xa.x, xa.y);
             }
-            float2 a[4];
+            uint32_t wr[HROWS];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) a[r] = make_float2(0.f, 0.f);
-            if (DT == DT_INT4) dotR_int4<4>(code, x2, a);
-            else if (DT == DT_INT8) dotR_int8<4>(code, x2, a);
-            else dotR_bf16<4>(code, x2, a);
+            for (int r = 0; r < HROWS; ++r) wr[r] = wbase[r * Lb * 4 + jw];
+            if (DT == DT_INT4) word_int4(wr, x2, acc);
+            else if (DT == DT_INT8) word_int8(wr, x2, acc);
+            else word_bf16(wr, x2, acc);
+          }
+          if (DT == DT_INT4) {
+            const float xg = S.xsum[g];
+            const uint32_t* szp = reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF) + lane;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              float contrib;
-              if (DT == DT_INT4) {
-                const float Sq = fmaf(256.0f, a[r].x, 16.0f * a[r].y);
-                contrib = fmaf(__uint_as_float(sz[r] << 16), Sq, __uint_as_float(sz[r] & 0xFFFF0000u) * xg);
-              } else {
-                contrib = a[r].x + a[r].y;
-              }
-              v[r8 + r] += lane_ok ? contrib : 0.0f;
+            for (int r = 0; r < HROWS; ++r) {
+              const uint32_t sz = szp[r * Lb];
+              const float Sq = fmaf(256.0f, acc[r].x, 16.0f * acc[r].y);
+              const float contrib = fmaf(__uint_as_float(sz << 16), Sq, __uint_as_float(sz & 0xFFFF0000u) * xg);
+              v[r] += lane_ok ? contrib : 0.0f;
             }
+          } else {
+#pragma unroll
+            for (int r = 0; r < HROWS; ++r) v[r] += lane_ok ? acc[r].x + acc[r].y : 0.0f;
           }
           slot_release(S, cs, it);
         }
@@ -667,7 +666,7 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
           float tot = 0.0f;
           if (lane < HROWS) {
             for (int ww = 0; ww < NCW; ++ww) {
-              const int bw = (int)((uint32_t)(ww - (int)(j % NCW) + NCW) % NCW);
+              const int bw = (ww - own0 + NCW) % NCW;
               if (bw < nb) tot += tb[ww * HROWS + lane];
             }
           }
@@ -686,8 +685,8 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
 }
 
 // ----------------------------------------------------------- attention ---
-// One unit = one kv head x one chunk of positions.  Slot k of the phase (16
-// positions of K and V) belongs to warp k % NCW; lane l owns dims
+// One unit = one kv head x one chunk of positions.  Each slot (16 positions
+// of K and V) belongs to the warp given by its stream index; lane l owns dims
 // l*DPL..l*DPL+DPL-1.  Each warp keeps an online softmax (m, l, o) per q head
 // of the group; the warps merge in shared memory; a head split over several
 // chunks merges its chunks' (m, l, o) in the CTA that finishes last
@@ -695,7 +694,6 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
 template <int HD>
 __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int u, int nch, int CH, int pos,
                           uint32_t& j) {
-  constexpr int DPL = HD / 32;
   const int gq = ph.Hq / ph.Hkv;
   const int kvh = u / nch, c = u % nch;
   const int T = pos + 1, Ts = ph.stream_cur ? T : T - 1;
@@ -705,17 +703,25 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   float* sc = S.xs + MAX_GQ * HD;         // [NCW][gq][HD + 2]
   const int nslots = pe > p0 ? (pe - p0 + ATT_POS_PER_SLOT - 1) / ATT_POS_PER_SLOT : 0;
   // positions not streamed (the row written by this step) go to the warp
-  // after the last slot's owner; its loads are issued first
+  // after the last slot's owner; its loads are issued first (lanes 0..15)
   const int pg = max(pe, p0);
-  const int gw = (int)((j + (uint32_t)nslots) % NCW);
-  uint32_t kpre[DPL / 2], vpre[DPL / 2];
+  const int gw = (int)((cs.it + j + (uint32_t)nslots) % NCW);
   const bool has_g = (w == gw) && pg < p1;
-  if (has_g) {
-    const size_t off = ((size_t)kvh * ph.Tmax + pg) * HD + lane * DPL;
+  uint32_t gk[HD / 32], gv[HD / 32];
 #pragma unroll
-    for (int d = 0; d < DPL / 2; ++d) {
-      kpre[d] = __ldcg(reinterpret_cast<const unsigned*>(ph.kc + off) + d);
-      vpre[d] = __ldcg(reinterpret_cast<const unsigned*>(ph.vc + off) + d);
+  for (int e = 0; e < HD / 32; ++e) gk[e] = gv[e] = 0u;
+  if (has_g && lane < 16) {
+    const size_t off = ((size_t)kvh * ph.Tmax + pg) * HD + lane * (HD / 16);
+    if constexpr (HD / 16 == 8) {
+      const uint4 kk = __ldcg(reinterpret_cast<const uint4*>(ph.kc + off));
+      const uint4 vv = __ldcg(reinterpret_cast<const uint4*>(ph.vc + off));
+      gk[0] = kk.x; gk[1] = kk.y; gk[2] = kk.z; gk[3] = kk.w;
+      gv[0] = vv.x; gv[1] = vv.y; gv[2] = vv.z; gv[3] = vv.w;
+    } else {
+      const uint2 kk = __ldcg(reinterpret_cast<const uint2*>(ph.kc + off));
+      const uint2 vv = __ldcg(reinterpret_cast<const uint2*>(ph.vc + off));
+      gk[0] = kk.x; gk[1] = kk.y;
+      gv[0] = vv.x; gv[1] = vv.y;
     }
   }
   const float scale = rsqrtf((float)HD);
@@ -727,70 +733,98 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   }
   if (!cta_sync(S, cs, P.err)) return false;
 
-  float m[MAX_GQ], l[MAX_GQ], o[MAX_GQ][DPL];
+  // Each warp takes two positions per step: lanes 0..15 one, 16..31 the
+  // other; lane l owns dims (l % 16) * DP2 .. + DP2 - 1 of its position.
+  constexpr int DP2 = HD / 16;
+  const int half = lane >> 4, hl = lane & 15;
+  float m[MAX_GQ], l[MAX_GQ], o[MAX_GQ][DP2];
 #pragma unroll
   for (int jj = 0; jj < MAX_GQ; ++jj) {
     m[jj] = -INFINITY;
     l[jj] = 0.f;
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) o[jj][d] = 0.f;
+    for (int d = 0; d < DP2; ++d) o[jj][d] = 0.f;
   }
-  auto consume = [&](const uint32_t* kk, const uint32_t* vv) {
-    float kf[DPL], vf[DPL];
+  // one position per half-warp: kw / vw hold this lane's DP2 dims of the
+  // position's K and V rows (bf16 pairs); `valid` false leaves the state as is
+  auto load_kv = [&](const uint16_t* klane, const uint16_t* vlane, uint32_t* kw, uint32_t* vw) {
+    if constexpr (DP2 == 8) {
+      const uint4 kk = *reinterpret_cast<const uint4*>(klane), vv = *reinterpret_cast<const uint4*>(vlane);
+      kw[0] = kk.x; kw[1] = kk.y; kw[2] = kk.z; kw[3] = kk.w;
+      vw[0] = vv.x; vw[1] = vv.y; vw[2] = vv.z; vw[3] = vv.w;
+    } else {
+      const uint2 kk = *reinterpret_cast<const uint2*>(klane), vv = *reinterpret_cast<const uint2*>(vlane);
+      kw[0] = kk.x; kw[1] = kk.y;
+      vw[0] = vv.x; vw[1] = vv.y;
+    }
+  };
+  auto consume2 = [&](const uint32_t* kw, const uint32_t* vw, bool valid) {
+    float kf[DP2], vf[DP2];
 #pragma unroll
-    for (int d = 0; d < DPL / 2; ++d) {
-      kf[2 * d] = __uint_as_float(kk[d] << 16);
-      kf[2 * d + 1] = __uint_as_float(kk[d] & 0xFFFF0000u);
-      vf[2 * d] = __uint_as_float(vv[d] << 16);
-      vf[2 * d + 1] = __uint_as_float(vv[d] & 0xFFFF0000u);
+    for (int e = 0; e < DP2 / 2; ++e) {
+      kf[2 * e] = __uint_as_float(kw[e] << 16);
+      kf[2 * e + 1] = __uint_as_float(kw[e] & 0xFFFF0000u);
+      vf[2 * e] = __uint_as_float(vw[e] << 16);
+      vf[2 * e + 1] = __uint_as_float(vw[e] & 0xFFFF0000u);
     }
 #pragma unroll
     for (int jj = 0; jj < MAX_GQ; ++jj) {
       if (jj < gq) {
         float dot = 0.f;
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) dot = fmaf(qs[jj * HD + lane * DPL + d], kf[d], dot);
+        for (int d = 0; d < DP2; ++d) dot = fmaf(qs[jj * HD + hl * DP2 + d], kf[d], dot);
 #pragma unroll
-        for (int of = 16; of; of >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, of);
-        const float mn = fmaxf(m[jj], dot);
-        const float corr = expf(m[jj] - mn), p = expf(dot - mn);
-        l[jj] = fmaf(l[jj], corr, p);
+        for (int of = 8; of; of >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, of);
+        if (valid) {
+          const float mn = fmaxf(m[jj], dot);
+          const float corr = expf(m[jj] - mn), p = expf(dot - mn);
+          l[jj] = fmaf(l[jj], corr, p);
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) o[jj][d] = fmaf(o[jj][d], corr, p * vf[d]);
-        m[jj] = mn;
+          for (int d = 0; d < DP2; ++d) o[jj][d] = fmaf(o[jj][d], corr, p * vf[d]);
+          m[jj] = mn;
+        }
       }
     }
   };
-  for (int k = (int)((uint32_t)(w - (int)(j % NCW) + NCW) % NCW); k < nslots; k += NCW) {
+  for (int k = (w - (int)((cs.it + j) % NCW) + NCW) % NCW; k < nslots; k += NCW) {
     const uint32_t it = cs.it + j + (uint32_t)k;
     const int np = min(ATT_POS_PER_SLOT, pe - (p0 + k * ATT_POS_PER_SLOT));
     const uint8_t* base;
     if (!slot_acquire(S, cs, it, P.err, base)) return false;
     const uint16_t* kb = reinterpret_cast<const uint16_t*>(base);
     const uint16_t* vb = kb + ATT_POS_PER_SLOT * HD;
-    for (int q = 0; q < np; ++q) {
-      uint32_t kk[DPL / 2], vv[DPL / 2];
+    for (int q = 0; q < np; q += 2) {
+      const int qq = q + half;
+      uint32_t kw[DP2 / 2], vw[DP2 / 2];
 #pragma unroll
-      for (int d = 0; d < DPL / 2; ++d) {
-        kk[d] = reinterpret_cast<const uint32_t*>(kb + q * HD + lane * DPL)[d];
-        vv[d] = reinterpret_cast<const uint32_t*>(vb + q * HD + lane * DPL)[d];
-      }
-      consume(kk, vv);
+      for (int e = 0; e < DP2 / 2; ++e) kw[e] = vw[e] = 0u;
+      if (qq < np) load_kv(kb + qq * HD + hl * DP2, vb + qq * HD + hl * DP2, kw, vw);
+      consume2(kw, vw, qq < np);
     }
     slot_release(S, cs, it);
   }
   j += (uint32_t)nslots;
-  if (has_g) consume(kpre, vpre);
-  // merge the warps of this CTA
+  if (has_g) consume2(gk, gv, half == 0);
+  // merge the two half-warps (xor 16), then the warps of this CTA
 #pragma unroll
   for (int jj = 0; jj < MAX_GQ; ++jj) {
     if (jj < gq) {
-      float* dst = sc + (w * gq + jj) * (HD + 2);
+      const float mo = __shfl_xor_sync(0xffffffffu, m[jj], 16);
+      const float lo = __shfl_xor_sync(0xffffffffu, l[jj], 16);
+      const float mn = fmaxf(m[jj], mo);
+      const float ea = l[jj] > 0.f ? expf(m[jj] - mn) : 0.f, eb = lo > 0.f ? expf(mo - mn) : 0.f;
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) dst[2 + lane * DPL + d] = o[jj][d];
-      if (lane == 0) {
-        dst[0] = m[jj];
-        dst[1] = l[jj];
+      for (int d = 0; d < DP2; ++d) o[jj][d] = o[jj][d] * ea + __shfl_xor_sync(0xffffffffu, o[jj][d], 16) * eb;
+      l[jj] = l[jj] * ea + lo * eb;
+      m[jj] = mn;
+      if (half == 0) {
+        float* dst = sc + (w * gq + jj) * (HD + 2);
+#pragma unroll
+        for (int d = 0; d < DP2; ++d) dst[2 + hl * DP2 + d] = o[jj][d];
+        if (hl == 0) {
+          dst[0] = m[jj];
+          dst[1] = l[jj];
+        }
       }
     }
   }
@@ -1078,7 +1112,8 @@ size_t gf_attn_workspace_bytes(int Hq, int Hkv, int hd) {
   if (Hq <= 0 || Hkv <= 0 || hd <= 0) return 0;
   const int sms = device_sms() > 0 ? device_sms() : 1;
   const int nch_max = (sms + Hkv - 1) / Hkv;
-  return (size_t)Hq * nch_max * (hd + 2) * sizeof(float) + 256;
+  // partials, then one combine ticket per kv head
+  return (size_t)Hq * nch_max * (hd + 2) * sizeof(float) + ((size_t)Hkv * sizeof(unsigned) + 255) / 256 * 256;
 }
 
 int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq, int Hkv, int hd, int Tmax, int pos,
@@ -1110,7 +1145,8 @@ int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq
   ph.hd = hd;
   ph.Tmax = Tmax;
   ph.stream_cur = 1;
-  const size_t part_bytes = need - 256;
+  const int nch_max = (sms + Hkv - 1) / Hkv;
+  const size_t part_bytes = (size_t)Hq * nch_max * (hd + 2) * sizeof(float);
   ph.part = (float*)ws;
   ph.tick = (unsigned*)((uint8_t*)ws + part_bytes);
   GF_CUDA(cudaMemsetAsync(ph.tick, 0, Hkv * sizeof(unsigned), (cudaStream_t)stream));

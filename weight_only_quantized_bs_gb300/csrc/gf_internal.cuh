@@ -30,13 +30,11 @@ __host__ __device__ inline long long full_tile_bytes(int dt, int C) {
 }
 __host__ __device__ inline long long packed_bytes(int dt, int N, int K) {
   int C = K / per_chunk(dt);
-  int ntiles = (N + TR - 1) / TR;
   long long total = (long long)(N / TR) * full_tile_bytes(dt, C);
   if (N % TR) {
     int Rt = N % TR;
     for (int c0 = 0; c0 < C; c0 += KBLK) total += block_bytes(dt, Rt, C - c0 < KBLK ? C - c0 : KBLK);
   }
-  (void)ntiles;
   return total;
 }
 // Byte offset of K-block b of the tile holding row-tile t (rows Rt), and of
@@ -51,18 +49,26 @@ constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp
 constexpr int HROWS = 16;                    // rows of a slot: half a tile
 constexpr int SLOT_BYTES = 10240;            // codes of 16 rows x 32 chunks + int4 scale words
 constexpr int SLOT_SZ_OFF = 8192;            // int4 scale words inside a slot
-constexpr int NSLOT = 14;
-constexpr int NTB = 32;                      // tile-half combine buffers
+// Slot X of the CTA's stream (counted over the whole program) belongs to
+// consumer warp X % NCW and uses ring entry X % NSLOT.  NSLOT is a multiple
+// of NCW, so every ring entry always belongs to the same warp: the previous
+// use of the entry a warp waits on is that warp's own, already consumed slot,
+// and the mbarrier phase parity it waits for is never ambiguous.
+constexpr int NSLOT = 16;
+constexpr int NTB = 16;                      // tile-half combine buffers
 constexpr int OFF_RING = 0;
 constexpr int OFF_X = OFF_RING + NSLOT * SLOT_BYTES;     // fp32 x, swizzled
 constexpr int OFF_XSUM = OFF_X + KMAX * 4;               // fp32 sum of x per 32-wide group
 constexpr int OFF_TB = OFF_XSUM + (KMAX / 32) * 4 + 256;  // [NTB][NCW][HROWS] partial row sums
 constexpr int OFF_TBC = OFF_TB + NTB * NCW * HROWS * 4;  // [NTB] arrival counters
 constexpr int OFF_BAR = OFF_TBC + NTB * 4;               // mbarriers
-constexpr int OFF_MISC = OFF_BAR + 256;
+constexpr int OFF_MISC = OFF_BAR + 320;
 constexpr int SMEM_BYTES = OFF_MISC + 512;
+static_assert(NSLOT % NCW == 0, "ring entries must map to a fixed warp");
+static_assert((2 * NSLOT + 1) * 8 <= 320, "mbarrier area");
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr int ATT_POS_PER_SLOT = 16;
-constexpr int MAX_GQ = 8;                    // q heads per kv head
+constexpr int MAX_GQ = 4;                    // q heads per kv head (GQA group)
 constexpr int MAX_M = 8;                     // rows of a verify pass
 
 // --------------------------------------------------------------- phases --
@@ -117,12 +123,15 @@ struct Phase {
 };
 
 // Split of a decode attention over positions 0..T-1 into nch chunks of CH
-// positions per kv head (CH a multiple of the slot size), aiming at about
-// `target` units in all.  Kernel and host use this one definition.
+// positions per kv head (CH a multiple of the slot size, chunks of at least
+// ATT_MIN_CHUNK positions so that short contexts stay in one CTA and skip the
+// cross-CTA merge), aiming at about `target` units in all.  Kernel and host
+// use this one definition.
+constexpr int ATT_MIN_CHUNK = 256;           // positions per chunk, at least
 __host__ __device__ inline void attn_split(int T, int Hkv, int target, int& CH, int& nch) {
   int want = (target + Hkv - 1) / Hkv;
   if (want < 1) want = 1;
-  const int maxch = (T + ATT_POS_PER_SLOT - 1) / ATT_POS_PER_SLOT;
+  const int maxch = (T + ATT_MIN_CHUNK - 1) / ATT_MIN_CHUNK;
   nch = want < maxch ? want : maxch;
   CH = ((T + nch - 1) / nch + ATT_POS_PER_SLOT - 1) / ATT_POS_PER_SLOT * ATT_POS_PER_SLOT;
   nch = (T + CH - 1) / CH;
