@@ -44,7 +44,7 @@ __host__ __device__ inline long long block_offset(int dt, int C, int t, int Rt, 
 }
 
 // ------------------------------------------------------- engine sizes ----
-constexpr int NCW = 8;                       // consumer warps per CTA
+constexpr int NCW = 7;                       // consumer warps per CTA
 constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp
 constexpr int HROWS = 16;                    // rows of a slot: half a tile
 constexpr int SLOT_BYTES = 10240;            // codes of 16 rows x 32 chunks + int4 scale words
@@ -54,7 +54,7 @@ constexpr int SLOT_SZ_OFF = 8192;            // int4 scale words inside a slot
 // of NCW, so every ring entry always belongs to the same warp: the previous
 // use of the entry a warp waits on is that warp's own, already consumed slot,
 // and the mbarrier phase parity it waits for is never ambiguous.
-constexpr int NSLOT = 16;
+constexpr int NSLOT = 14;
 constexpr int NTB = 16;                      // tile-half combine buffers
 constexpr int OFF_RING = 0;
 constexpr int OFF_X = OFF_RING + NSLOT * SLOT_BYTES;     // fp32 x, swizzled
