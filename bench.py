@@ -106,6 +106,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def measured_traffic(workload, dtype):
+    """DRAM bytes per k_engine launch from a committed ncu capture
+    (profiles/traffic.json), or None when absent, for another workload, or
+    taken on a different engine source than the one built now."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    src = os.path.join(ROOT, "weight_only_quantized_bs_gb300", "csrc", "engine.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    r = rec.get("%s/%s" % (workload, dtype))
+    if not r or r.get("engine_sha") != sha:
+        return None
+    return r["bytes_per_launch"]
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -304,7 +322,9 @@ def run_ours(args):
                          int(head["weight_bytes"] / 1e6)},
         "achieved_gbs": round(head["gbs"], 1),
         "roofline": {"bound": "hbm", "achieved": round(head["gbs"], 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(head["gbs"] / hbm_peak, 4), "traffic": None,
+                     "frac": round(head["gbs"] / hbm_peak, 4),
+                     "traffic": measured_traffic(args.workload, args.dtype),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind,
                      "kernel": "k_engine (one launch per token)"},
         "copy_ceiling_gbs": round(copy_gbs, 1),
