@@ -82,3 +82,17 @@ def test_decode_gqa4_ragged():
     cfg = models.config("tiny", n_heads=8, n_kv_heads=2, d=512, head_dim=64, ffn=736, vocab=1003)
     got, am, ref = run_teacher_forced(cfg, "int4", seed=13, n_prompt=5, n_gen=40, tmax=64)
     check(got, am, ref)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "int8", "int4"])
+def test_decode_moe_tiny(dtype):
+    cfg = models.config("tiny-moe")
+    got, am, ref = run_teacher_forced(cfg, dtype, seed=14, n_prompt=5, n_gen=30, tmax=64)
+    check(got, am, ref)
+
+
+def test_decode_moe_mixtral_like():
+    """Mixtral structure (8 experts, top-2, GQA 32/8 -> 4, head 128) at small width."""
+    cfg = models.config("mixtral-8x7b", d=1024, n_layers=2, n_heads=8, n_kv_heads=2, ffn=1536, vocab=3000)
+    got, am, ref = run_teacher_forced(cfg, "int8", seed=15, n_prompt=5, n_gen=10, tmax=32)
+    check(got, am, ref)

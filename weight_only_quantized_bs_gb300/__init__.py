@@ -210,7 +210,9 @@ def _ptr_array(tensors):
 class Model:
     """Library-owned quantised weights of a decoder.  `layers` yields, per
     layer, a dict of bf16 device tensors wqkv, wo, wgu (gate/up rows
-    interleaved), wd, g_attn, g_ffn; `glob` holds embed, g_final, lm_head."""
+    interleaved), wd, g_attn, g_ffn -- for a mixture of experts wgu and wd are
+    lists (one per expert) and `router` [n_experts][d] is added; `glob` holds
+    embed, g_final, lm_head."""
 
     def __init__(self, cfg, wdtype, glob, layers):
         self.cfg = cfg
@@ -219,15 +221,18 @@ class Model:
                     cfg["vocab"], cfg.get("n_experts", 0), cfg["eps"], cfg["theta"])
         keep = []
         arrays = {}
-        for name in ("wqkv", "wo", "wgu", "wd", "g_attn", "g_ffn"):
-            ts = [L[name] for L in layers]
+        moe = cfg.get("n_experts", 0) > 0
+        for name in ("wqkv", "wo", "wgu", "wd", "g_attn", "g_ffn") + (("router",) if moe else ()):
+            if moe and name in ("wgu", "wd"):
+                ts = [t for L in layers for t in L[name]]   # layer-major, one per expert
+            else:
+                ts = [L[name] for L in layers]
             keep.append(ts)
             arrays[name] = _ptr_array(ts)
+        cp = lambda a: ctypes.cast(a, ctypes.c_void_p)  # noqa: E731
         w = _Weights(glob["embed"].data_ptr(), glob["g_final"].data_ptr(), glob["lm_head"].data_ptr(),
-                     ctypes.cast(arrays["wqkv"], ctypes.c_void_p), ctypes.cast(arrays["wo"], ctypes.c_void_p),
-                     ctypes.cast(arrays["wgu"], ctypes.c_void_p), ctypes.cast(arrays["wd"], ctypes.c_void_p),
-                     ctypes.cast(arrays["g_attn"], ctypes.c_void_p), ctypes.cast(arrays["g_ffn"], ctypes.c_void_p),
-                     None)
+                     cp(arrays["wqkv"]), cp(arrays["wo"]), cp(arrays["wgu"]), cp(arrays["wd"]),
+                     cp(arrays["g_attn"]), cp(arrays["g_ffn"]), cp(arrays["router"]) if moe else None)
         h = ctypes.c_void_p()
         _check(lib().gf_model_create(ctypes.byref(c), self.wdtype, ctypes.byref(w), ctypes.byref(h)),
                "gf_model_create")

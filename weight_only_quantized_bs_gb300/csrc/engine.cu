@@ -145,8 +145,8 @@ struct Smem {
   uint64_t* full;   // [NSLOT]
   uint64_t* empty;  // [NSLOT]
   uint64_t* cbar;   // consumer-warps barrier
-  float* red;       // [64] reduction scratch
-  int* bcast;       // [64] broadcast ints
+  float* red;       // [64] reduction scratch; [32..39] router logits, [40..41] expert weights
+  int* bcast;       // [64] broadcast ints; [32..33] chosen experts, [34] phase they were chosen in
 };
 
 __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
@@ -187,6 +187,28 @@ __device__ __forceinline__ bool prod_slot(const Smem& S, Prod& pr, int* err, uin
   return true;
 }
 
+// The producer needs the two experts of a MOE_GU phase before it can stream
+// their weights: consumer thread 0 publishes them in shared memory, tagged
+// with the phase index.  Bounded wait.
+__device__ bool wait_experts(const Smem& S, int* err, int pi) {
+  volatile int* seq = S.bcast + 34;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 0;; ++it) {
+    if (*seq == pi + 1) {
+      __threadfence_block();
+      return true;
+    }
+    __nanosleep(64);
+    if ((it & 31) == 31) {
+      if (ld_relaxed(err)) return false;
+      if (gtimer() - t0 > WAIT_NS) {
+        atomicCAS(err, 0, ERR_WAIT_ROUTER);
+        return false;
+      }
+    }
+  }
+}
+
 // Slot order of a GEMV phase (producer and consumers walk it identically):
 // for each of the CTA's tiles t, for each half h of the tile's rows, the
 // K-blocks b in order.
@@ -202,14 +224,28 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
     const Phase& ph = phase_at(P, pi);
     if (ph.kind == PH_GEMV) {
       const int dt = ph.dtype, C = ph.K / per_chunk(dt);
-      const int ntiles = (ph.N + TR - 1) / TR, nb = (C + KBLK - 1) / KBLK;
+      // a phase covers nseg matrices of Ns rows each (two experts for MOE_GU)
+      const int nseg = ph.moe == MOE_GU ? 2 : 1, Ns = ph.N / nseg;
+      const int tps = (Ns + TR - 1) / TR, ntiles = nseg * tps, nb = (C + KBLK - 1) / KBLK;
+      const uint8_t* wseg[2] = {ph.W, ph.W};
+      if (ph.moe != MOE_NONE) {
+        if (ph.moe == MOE_GU && !(ok = wait_experts(S, err, pi))) break;
+        volatile int* sel = S.bcast + 32;
+        if (ph.moe == MOE_GU) {
+          wseg[0] = ph.W + (size_t)sel[0] * ph.expert_stride;
+          wseg[1] = ph.W + (size_t)sel[1] * ph.expert_stride;
+        } else {
+          wseg[0] = ph.W + (size_t)sel[ph.moe - MOE_DOWN0] * ph.expert_stride;
+        }
+      }
       for (int t = first_unit(cta, ph.rot, G); t < ntiles && ok; t += G) {
-        const int Rt = min(TR, ph.N - t * TR);
+        const int seg = t / tps, lt = t % tps;
+        const int Rt = min(TR, Ns - lt * TR);
         for (int h = 0; h * HROWS < Rt && ok; ++h) {
           const int r0 = h * HROWS, rh = min(HROWS, Rt - r0);
           for (int b = 0; b < nb; ++b) {
             const int Lb = min(KBLK, C - b * KBLK);
-            const uint8_t* blk = ph.W + block_offset(dt, C, t, Rt, b);
+            const uint8_t* blk = wseg[seg] + block_offset(dt, C, lt, Rt, b);
             const uint32_t cb = (uint32_t)(rh * Lb * 16);
             const uint32_t sb = dt == DT_INT4 ? (uint32_t)((rh * Lb * 4 + 15) / 16 * 16) : 0u;
             uint8_t* dst;
@@ -517,8 +553,8 @@ __device__ __forceinline__ void amax_merge(ArgMax& a, float v, int i) {
 
 // Epilogue of one output row n (value y); lanes 0..15 call it together, each
 // with its own row of the half-tile; yp is the value of row n ^ 1.
-__device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, int n, float y, float yp, int pos,
-                                              ArgMax& am) {
+__device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, const Smem& S, int seg, int n, float y,
+                                              float yp, int pos, ArgMax& am) {
   switch (ph.epi) {
     case EPI_STORE_BF16:
       reinterpret_cast<uint16_t*>(ph.out)[n] = f2bf(y);
@@ -563,6 +599,12 @@ __device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, 
       P.logits[n] = y;
       amax_merge(am, y, n);
       break;
+    case EPI_MOE_SWIGLU:  // rows of a segment: gate j, up j interleaved; F = rows / 2
+      if ((n & 1) == 0) reinterpret_cast<float*>(ph.out)[(size_t)seg * (ph.N / 4) + (n >> 1)] = y / (1.0f + expf(-y)) * yp;
+      break;
+    case EPI_MOE_RESID:
+      atomicAdd(reinterpret_cast<float*>(ph.out) + n, S.red[40 + ph.moe - MOE_DOWN0] * y);
+      break;
     default:
       break;
   }
@@ -579,12 +621,18 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
   constexpr int U = E / 4;
   const int G = P.nctas;
   const int C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
-  const int ntiles = (ph.N + TR - 1) / TR;
+  const int nseg = ph.moe == MOE_GU ? 2 : 1, Ns = ph.N / nseg;
+  const int tps = (Ns + TR - 1) / TR, ntiles = nseg * tps;
   const int lane = cs.lane, w = cs.warp;
   const float4* xs4 = reinterpret_cast<const float4*>(S.xs);
   uint32_t j = 0;  // slot index within the phase
   for (int t = first_unit(cta, ph.rot, G); t < ntiles; t += G) {
-    const int Rt = min(TR, ph.N - t * TR);
+    const int seg = t / tps, lt = t % tps;
+    const int Rt = min(TR, Ns - lt * TR);
+    // int8 row scales of the segment's matrix (the chosen expert's, for MoE)
+    const uint16_t* s8 = ph.s8;
+    if (DT == DT_INT8 && ph.moe != MOE_NONE)
+      s8 += (size_t)S.bcast[32 + (ph.moe == MOE_GU ? seg : ph.moe - MOE_DOWN0)] * Ns;
     for (int h = 0; h * HROWS < Rt; ++h, ++cs.useq) {
       const int r0 = h * HROWS;
       const int own0 = (int)((cs.it + j) % NCW);                              // owner of K-block 0
@@ -671,10 +719,10 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
             }
           }
           if (lane == 0) S.tbc[buf] = 0;
-          const int r = r0 + lane, n = t * TR + r;
-          if (DT == DT_INT8 && lane < HROWS && r < Rt) tot *= 256.0f * bf2f(ph.s8[n]);
+          const int r = r0 + lane, n = lt * TR + r;
+          if (DT == DT_INT8 && lane < HROWS && r < Rt) tot *= 256.0f * bf2f(s8[n]);
           const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
-          if (lane < HROWS && r < Rt) gemv_epilogue(ph, P, n, tot, yp, pos, am);
+          if (lane < HROWS && r < Rt) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, am);
         }
       }
       j += (uint32_t)nb;
@@ -883,6 +931,47 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   return true;
 }
 
+// ------------------------------------------------------- MoE router -----
+// Top-2 router of a mixture-of-experts layer ("Efficiently implementing the
+// Mixtral 8x7B model with gpt-fast"; gpt-fast README, "Mixtral 8x7B"):
+// logits r_e = x . Wr[e] over the staged (normalised) input, the two largest
+// (lower index first on ties), weights = softmax over those two.  Every CTA
+// computes the same logits in the same order, so all agree on the experts.
+__device__ bool route_experts(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int pi) {
+  const int K = ph.K, U = per_chunk(ph.dtype) / 4, K4 = K / 4;
+  const float4* xs4 = reinterpret_cast<const float4*>(S.xs);
+  for (int e = cs.warp; e < ph.n_experts; e += NCW) {
+    const uint2* wr = reinterpret_cast<const uint2*>(ph.router + (size_t)e * K);
+    float acc = 0.0f;
+    for (int k4 = cs.lane; k4 < K4; k4 += 32) {
+      const int g = k4 / U, u = k4 % U;
+      const float4 x = xs4[g * U + (u ^ swz(g, U))];
+      const float4 wv = bf4(wr[k4]);
+      acc = fmaf(x.x, wv.x, fmaf(x.y, wv.y, fmaf(x.z, wv.z, fmaf(x.w, wv.w, acc))));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (cs.lane == 0) S.red[32 + e] = acc;
+  }
+  if (!cta_sync(S, cs, P.err)) return false;
+  if (cs.ctid == 0) {
+    int e1 = 0;
+    for (int e = 1; e < ph.n_experts; ++e)
+      if (S.red[32 + e] > S.red[32 + e1]) e1 = e;
+    int e2 = e1 == 0 ? 1 : 0;
+    for (int e = 0; e < ph.n_experts; ++e)
+      if (e != e1 && S.red[32 + e] > S.red[32 + e2]) e2 = e;
+    const float b = expf(S.red[32 + e2] - S.red[32 + e1]);  // r2 <= r1
+    S.red[40] = 1.0f / (1.0f + b);
+    S.red[41] = b / (1.0f + b);
+    S.bcast[32] = e1;
+    S.bcast[33] = e2;
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(S.bcast + 34) = pi + 1;  // releases the producer
+  }
+  return cta_sync(S, cs, P.err);
+}
+
 // ------------------------------------------------------ argmax finish ----
 __device__ bool argmax_finish(const Params& P, const Smem& S, Cons& cs, int cta, ArgMax am) {
   // warp reduce, then CTA, then across CTAs through the last-arriving CTA
@@ -930,6 +1019,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < NTB) S.tbc[tid] = 0;
+  if (tid == 0) S.bcast[34] = 0;
   __syncthreads();
   const int pos = P.d_pos ? *P.d_pos : P.pos_const;
   // Reject a position or token that would index outside the cache, the RoPE
@@ -975,6 +1065,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     if (tr) tr[1] = gtimer();
     if (ph.kind == PH_GEMV) {
       if (!stage_x(ph, P, S, cs, cta)) return;
+      if (ph.moe == MOE_GU && !route_experts(ph, P, S, cs, pi)) return;
       if (tr) tr[2] = gtimer();
       bool ok;
       if (ph.dtype == DT_INT4) ok = gemv_phase<DT_INT4>(ph, P, S, cs, cta, pos, am);

@@ -80,8 +80,14 @@ enum Epi {
   EPI_QKV = 2,       // RoPE q and k; q -> fp32 q buffer, k, v -> bf16 cache row at pos
   EPI_RESID = 3,     // resid[n] += y
   EPI_SWIGLU = 4,    // h[n/2] = silu(gate) * up (fp32)
-  EPI_LOGITS = 5     // logits[n] = y (fp32), running argmax
+  EPI_LOGITS = 5,    // logits[n] = y (fp32), running argmax
+  EPI_MOE_SWIGLU = 6,  // h[slot * F + n/2] = silu(gate) * up for the slot's expert
+  EPI_MOE_RESID = 7    // resid[n] += w[slot] * y
 };
+// Mixture-of-experts role of a GEMV phase: MOE_GU runs the router and then the
+// gate/up rows of the two chosen experts (2 * N_e rows); MOE_DOWN0 / 1 run the
+// down projection of the first / second chosen expert.
+enum MoeMode { MOE_NONE = 0, MOE_GU = 1, MOE_DOWN0 = 2, MOE_DOWN1 = 3 };
 enum ErrCode {
   ERR_NONE = 0,
   ERR_WAIT_FULL = 1,
@@ -91,7 +97,8 @@ enum ErrCode {
   ERR_DRAIN = 5,
   ERR_BAD_PROGRAM = 6,
   ERR_BAD_POS = 7,    // *d_pos outside [0, Tmax)
-  ERR_BAD_TOKEN = 8   // token id outside [0, vocab)
+  ERR_BAD_TOKEN = 8,  // token id outside [0, vocab)
+  ERR_WAIT_ROUTER = 9 // the producer gave up waiting for the expert choice
 };
 
 struct Phase {
@@ -120,6 +127,11 @@ struct Phase {
   float* part;             // [Hq][nch_max][hd + 2] partials
   unsigned* tick;          // [Hkv] combine tickets
   int stream_cur;          // 1: the row at pos is in memory before launch (standalone)
+  // mixture of experts
+  int moe;                 // MoeMode
+  int n_experts;
+  long long expert_stride; // bytes between consecutive experts' packed matrices
+  const uint16_t* router;  // [n_experts][K] bf16 (MOE_GU)
 };
 
 // Split of a decode attention over positions 0..T-1 into nch chunks of CH

@@ -16,8 +16,9 @@ struct gf_model {
     uint16_t* s8 = nullptr;
     int N = 0, K = 0;
   };
-  std::vector<Mat> qkv, o, gu, dn;  // per layer
-  std::vector<uint16_t*> g_attn, g_ffn;
+  std::vector<Mat> qkv, o, gu, dn;  // per layer (MoE: gu / dn hold all experts back to back)
+  std::vector<uint16_t*> g_attn, g_ffn, router;
+  long long gu_stride = 0, dn_stride = 0;  // MoE: bytes between experts
   Mat lm;
   uint16_t* embed = nullptr;
   uint16_t* g_final = nullptr;
@@ -80,6 +81,30 @@ static int make_mat(gf_model* m, const void* src, int N, int K, gf_model::Mat& o
   return gf_repack_bf16(src, N, K, out.W, nullptr);
 }
 
+// E experts of one layer quantised into one buffer, expert e at e * stride
+// (and int8 scales at e * N).
+static int make_experts(gf_model* m, const void* const* srcs, int E, int N, int K, gf_model::Mat& out,
+                        long long& stride) {
+  out.N = N;
+  out.K = K;
+  const int dt = m->wdtype;
+  stride = packed_bytes(dt, N, K);
+  int rc = dev_alloc(m->allocs, (void**)&out.W, (size_t)(stride * E));
+  if (rc) return rc;
+  if (dt == DT_INT8 && (rc = dev_alloc(m->allocs, (void**)&out.s8, (size_t)N * E * 2))) return rc;
+  for (int e = 0; e < E && !rc; ++e) {
+    if (!srcs[e]) {
+      set_error("gf_model_create: null expert weight");
+      return GF_EINVAL;
+    }
+    uint8_t* dst = out.W + (size_t)e * stride;
+    if (dt == DT_INT8) rc = gf_quantize_w8(srcs[e], N, K, dst, out.s8 + (size_t)e * N, nullptr);
+    else if (dt == DT_INT4) rc = gf_quantize_w4g(srcs[e], N, K, 32, dst, nullptr);
+    else rc = gf_repack_bf16(srcs[e], N, K, dst, nullptr);
+  }
+  return rc;
+}
+
 static int copy_vec(gf_model* m, const void* src, size_t elems, uint16_t** out) {
   int rc = dev_alloc(m->allocs, (void**)out, elems * 2);
   if (rc) return rc;
@@ -95,8 +120,8 @@ static int check_cfg(const gf_model_config* c) {
     set_error("gf_model_create: unsupported configuration");
     return GF_EINVAL;
   }
-  if (c->n_experts) {
-    set_error("gf_model_create: mixture-of-experts models are not supported by this build");
+  if (c->n_experts == 1 || c->n_experts < 0 || c->n_experts > 8) {
+    set_error("gf_model_create: n_experts must be 0 (dense) or 2..8");
     return GF_EUNSUPPORTED;
   }
   return GF_OK;
@@ -112,7 +137,7 @@ int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w,
   int rc = check_cfg(cfg);
   if (rc) return rc;
   if (!w || !out || wdtype < 0 || wdtype > 2 || !w->embed || !w->g_final || !w->lm_head || !w->wqkv || !w->wo ||
-      !w->wgu || !w->wd || !w->g_attn || !w->g_ffn) {
+      !w->wgu || !w->wd || !w->g_attn || !w->g_ffn || (cfg->n_experts && !w->router)) {
     set_error("gf_model_create: null weights or bad dtype");
     return GF_EINVAL;
   }
@@ -127,16 +152,33 @@ int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w,
   m->dn.resize(c.n_layers);
   m->g_attn.resize(c.n_layers);
   m->g_ffn.resize(c.n_layers);
+  m->router.resize(c.n_layers);
+  const int E = c.n_experts;
   for (int l = 0; l < c.n_layers && !rc; ++l) {
-    if (!w->wqkv[l] || !w->wo[l] || !w->wgu[l] || !w->wd[l] || !w->g_attn[l] || !w->g_ffn[l]) {
+    if (!w->wqkv[l] || !w->wo[l] || !w->g_attn[l] || !w->g_ffn[l] || (E && !w->router[l])) {
       set_error("gf_model_create: null weight pointer in layer %d", l);
       rc = GF_EINVAL;
       break;
     }
     if ((rc = make_mat(m, w->wqkv[l], qkvN, c.d, m->qkv[l]))) break;
     if ((rc = make_mat(m, w->wo[l], c.d, c.n_heads * hd, m->o[l]))) break;
-    if ((rc = make_mat(m, w->wgu[l], 2 * c.ffn, c.d, m->gu[l]))) break;
-    if ((rc = make_mat(m, w->wd[l], c.d, c.ffn, m->dn[l]))) break;
+    if (E) {
+      const long long before = m->weight_bytes;
+      if ((rc = make_experts(m, w->wgu + (size_t)l * E, E, 2 * c.ffn, c.d, m->gu[l], m->gu_stride))) break;
+      if ((rc = make_experts(m, w->wd + (size_t)l * E, E, c.d, c.ffn, m->dn[l], m->dn_stride))) break;
+      if ((rc = copy_vec(m, w->router[l], (size_t)E * c.d, &m->router[l]))) break;
+      // a token streams two experts and the router
+      m->weight_bytes = before + 2 * (m->gu_stride + m->dn_stride) + (long long)E * c.d * 2;
+      if (wdtype == DT_INT8) m->weight_bytes += 2LL * (2 * c.ffn + c.d) * 2;
+    } else {
+      if (!w->wgu[l] || !w->wd[l]) {
+        set_error("gf_model_create: null weight pointer in layer %d", l);
+        rc = GF_EINVAL;
+        break;
+      }
+      if ((rc = make_mat(m, w->wgu[l], 2 * c.ffn, c.d, m->gu[l]))) break;
+      if ((rc = make_mat(m, w->wd[l], c.d, c.ffn, m->dn[l]))) break;
+    }
     if ((rc = copy_vec(m, w->g_attn[l], c.d, &m->g_attn[l]))) break;
     if ((rc = copy_vec(m, w->g_ffn[l], c.d, &m->g_ffn[l]))) break;
     m->weight_bytes += 2LL * c.d * 2;
@@ -182,7 +224,9 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
   int rc = GF_OK;
   const size_t cache_elems = (size_t)L * Hkv * Tmax * hd;
   const int nch_max = (G + Hkv - 1) / Hkv;
-  const int nph = 5 * L + 1;
+  const int E = c.n_experts;
+  const int ppl = E ? 6 : 5;  // phases per layer
+  const int nph = ppl * L + 1;
   const int nbars = nph;
   const size_t nticks = (size_t)L * Hkv;
   kv->counter_bytes = (nbars + nticks + 1) * sizeof(unsigned);
@@ -192,7 +236,7 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->rope, (size_t)Tmax * (hd / 2) * sizeof(float2)))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->qbuf, (size_t)Hq * hd * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->attn, (size_t)Hq * hd * 4))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->h, (size_t)c.ffn * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->h, (size_t)c.ffn * 4 * (c.n_experts ? 2 : 1)))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->resid, (size_t)c.d * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->part, (size_t)Hq * nch_max * (hd + 2) * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_val, (size_t)G * 4))) break;
@@ -236,7 +280,7 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     cum_units += (mat.N + TR - 1) / TR;
   };
   for (int l = 0; l < L; ++l) {
-    Phase* P = &ph[5 * l];
+    Phase* P = &ph[ppl * l];
     uint16_t* kcl = kv->kc + (size_t)l * Hkv * Tmax * hd;
     uint16_t* vcl = kv->vc + (size_t)l * Hkv * Tmax * hd;
     // q/k/v with RoPE and the KV append
@@ -275,20 +319,49 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[2].xptr = kv->attn;
     P[2].epi = EPI_RESID;
     P[2].out = kv->resid;
-    // gate/up + SwiGLU
-    gemv(P[3], m->gu[l]);
-    P[3].xsrc = X_NORM;
-    P[3].xptr = kv->resid;
-    P[3].gain = m->g_ffn[l];
-    P[3].eps = c.eps;
-    P[3].epi = EPI_SWIGLU;
-    P[3].out = kv->h;
-    // down + residual
-    gemv(P[4], m->dn[l]);
-    P[4].xsrc = X_F32;
-    P[4].xptr = kv->h;
-    P[4].epi = EPI_RESID;
-    P[4].out = kv->resid;
+    if (!E) {
+      // gate/up + SwiGLU
+      gemv(P[3], m->gu[l]);
+      P[3].xsrc = X_NORM;
+      P[3].xptr = kv->resid;
+      P[3].gain = m->g_ffn[l];
+      P[3].eps = c.eps;
+      P[3].epi = EPI_SWIGLU;
+      P[3].out = kv->h;
+      // down + residual
+      gemv(P[4], m->dn[l]);
+      P[4].xsrc = X_F32;
+      P[4].xptr = kv->h;
+      P[4].epi = EPI_RESID;
+      P[4].out = kv->resid;
+    } else {
+      // router + gate/up of the two chosen experts (2 x 2 ffn rows)
+      gf_model::Mat two = m->gu[l];
+      two.N = 2 * m->gu[l].N;
+      gemv(P[3], two);
+      P[3].moe = MOE_GU;
+      P[3].n_experts = E;
+      P[3].expert_stride = m->gu_stride;
+      P[3].router = m->router[l];
+      P[3].xsrc = X_NORM;
+      P[3].xptr = kv->resid;
+      P[3].gain = m->g_ffn[l];
+      P[3].eps = c.eps;
+      P[3].epi = EPI_MOE_SWIGLU;
+      P[3].out = kv->h;
+      // down projection of each chosen expert, weighted into the residual
+      for (int k = 0; k < 2; ++k) {
+        Phase& D = P[4 + k];
+        gemv(D, m->dn[l]);
+        D.moe = k == 0 ? MOE_DOWN0 : MOE_DOWN1;
+        D.n_experts = E;
+        D.expert_stride = m->dn_stride;
+        D.xsrc = X_F32;
+        D.xptr = kv->h + (size_t)k * c.ffn;
+        D.epi = EPI_MOE_RESID;
+        D.out = kv->resid;
+      }
+    }
   }
   Phase& lm = ph[nph - 1];
   gemv(lm, m->lm);

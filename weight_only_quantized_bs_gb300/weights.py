@@ -11,18 +11,28 @@ def to_dev(a, device="cuda"):
     return t.to(device, non_blocking=False).view(torch.bfloat16)
 
 
+def _interleave(wg, wu):
+    wgu = np.empty((2 * wg.shape[0], wg.shape[1]), dtype=np.uint16)
+    wgu[0::2] = wg
+    wgu[1::2] = wu
+    return wgu
+
+
 def fuse_layer(w, device="cuda"):
-    wgu = np.empty((2 * w["wg"].shape[0], w["wg"].shape[1]), dtype=np.uint16)
-    wgu[0::2] = w["wg"]
-    wgu[1::2] = w["wu"]
-    return {
+    out = {
         "wqkv": to_dev(np.concatenate([w["wq"], w["wk"], w["wv"]], axis=0), device),
         "wo": to_dev(w["wo"], device),
-        "wgu": to_dev(wgu, device),
-        "wd": to_dev(w["wd"], device),
         "g_attn": to_dev(w["g_attn"], device),
         "g_ffn": to_dev(w["g_ffn"], device),
     }
+    if "experts" in w:
+        out["wgu"] = [to_dev(_interleave(e["wg"], e["wu"]), device) for e in w["experts"]]
+        out["wd"] = [to_dev(e["wd"], device) for e in w["experts"]]
+        out["router"] = to_dev(w["router"], device)
+    else:
+        out["wgu"] = to_dev(_interleave(w["wg"], w["wu"]), device)
+        out["wd"] = to_dev(w["wd"], device)
+    return out
 
 
 def device_globals(g, device="cuda"):
