@@ -146,7 +146,9 @@ struct Smem {
   uint64_t* empty;  // [NSLOT]
   uint64_t* cbar;   // consumer-warps barrier
   float* red;       // [64] reduction scratch; [32..39] router logits, [40..41] expert weights
-  int* bcast;       // [64] broadcast ints; [32..33] chosen experts, [34] phase they were chosen in
+  int* bcast;       // [64] broadcast ints; [32..33] chosen experts, [34] phase they were chosen in,
+                    // [48..55] verify: union of the rows' experts, [56] its size
+  float* moew;      // [MAX_M][8] verify: weight of expert e for row m (0 if not chosen)
 };
 
 __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
@@ -161,6 +163,7 @@ __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
   s.cbar = s.empty + NSLOT;
   s.red = reinterpret_cast<float*>(base + OFF_MISC);
   s.bcast = reinterpret_cast<int*>(base + OFF_MISC + 256);
+  s.moew = reinterpret_cast<float*>(base + OFF_MISC + 512);
   return s;
 }
 
@@ -209,6 +212,131 @@ __device__ bool wait_experts(const Smem& S, int* err, int pi) {
   }
 }
 
+// ------------------------------------------------ attention units -------
+// Units of an attention phase: for each query row m (one in a decode step,
+// M in a verify pass) the kv heads times the chunks of that row's positions
+// 0..pos+m.  Positions below `Ts` come through the ring; the rest (rows
+// written during this launch) are read from global memory.
+struct AttnUnit {
+  int m, kvh, c, nch, T, Ts, p0, p1;
+};
+__device__ int attn_units(const Phase& ph, const Params& P, int pos, int u, AttnUnit* out) {
+  const bool ver = verifying(P);
+  const int M = ver ? P.M : 1;
+  int base = 0;
+  for (int m = 0; m < M; ++m) {
+    const int T = pos + m + 1;
+    int CH, nch;
+    attn_split(T, ph.Hkv, P.unit_target, CH, nch);
+    const int n = ph.Hkv * nch;
+    if (u >= base && u < base + n && out) {
+      const int v = u - base;
+      out->m = m;
+      out->kvh = v / nch;
+      out->c = v % nch;
+      out->nch = nch;
+      out->T = T;
+      out->Ts = ver ? pos : (ph.stream_cur ? T : T - 1);
+      out->p0 = out->c * CH;
+      out->p1 = min(out->p0 + CH, T);
+      return 0;
+    }
+    base += n;
+  }
+  return base;
+}
+
+// Segments of a GEMV phase: the matrices it covers (several experts for MoE).
+__device__ __forceinline__ int gemv_segments(const Phase& ph, const Params& P, const Smem& S, int& Ns,
+                                             const uint8_t** wseg, int* eseg) {
+  volatile int* bc = S.bcast;
+  if (ph.moe == MOE_NONE) {
+    Ns = ph.N;
+    wseg[0] = ph.W;
+    eseg[0] = 0;
+    return 1;
+  }
+  if (verifying(P)) {  // verify: the union of the rows' experts
+    const int n = bc[56];
+    Ns = ph.N;
+    for (int k = 0; k < n; ++k) {
+      eseg[k] = bc[48 + k];
+      wseg[k] = ph.W + (size_t)eseg[k] * ph.expert_stride;
+    }
+    return n;
+  }
+  if (ph.moe == MOE_GU) {
+    Ns = ph.N / 2;
+    for (int k = 0; k < 2; ++k) {
+      eseg[k] = bc[32 + k];
+      wseg[k] = ph.W + (size_t)eseg[k] * ph.expert_stride;
+    }
+    return 2;
+  }
+  Ns = ph.N;
+  eseg[0] = bc[32 + ph.moe - MOE_DOWN0];
+  wseg[0] = ph.W + (size_t)eseg[0] * ph.expert_stride;
+  return 1;
+}
+
+// Slot order of a multi-row (verify) GEMV phase: the CTA's tiles in groups of
+// up to VTG tiles of one segment; per group, K-block by K-block, the group's
+// tiles and their halves.  Consumers walk the same order.
+struct TileGroups {
+  int first, G, ntiles, tps;
+};
+__device__ __forceinline__ int group_end(const TileGroups& tg, int i0) {
+  const int t0 = tg.first + i0 * tg.G, seg = t0 / tg.tps;
+  int i1 = i0 + 1;
+  while (i1 - i0 < VTG) {
+    const int t = tg.first + i1 * tg.G;
+    if (t >= tg.ntiles || t / tg.tps != seg) break;
+    ++i1;
+  }
+  return i1;
+}
+
+__device__ bool wait_experts(const Smem& S, int* err, int pi);
+
+__device__ bool produce_gemv_m(const Phase& ph, const Params& P, const Smem& S, Prod& pr, int cta, int pi) {
+  int* err = P.err;
+  if (ph.moe == MOE_GU && !wait_experts(S, err, pi)) return false;
+  const int dt = ph.dtype, C = ph.K / per_chunk(dt), nb = (C + KBLK - 1) / KBLK;
+  int Ns;
+  const uint8_t* wseg[8];
+  int eseg[8];
+  const int nseg = gemv_segments(ph, P, S, Ns, wseg, eseg);
+  TileGroups tg;
+  tg.tps = (Ns + TR - 1) / TR;
+  tg.ntiles = nseg * tg.tps;
+  tg.G = P.nctas;
+  tg.first = first_unit(cta, ph.rot, P.nctas);
+  for (int i0 = 0; tg.first + i0 * tg.G < tg.ntiles;) {
+    const int i1 = group_end(tg, i0);
+    for (int b = 0; b < nb; ++b) {
+      const int Lb = min(KBLK, C - b * KBLK);
+      for (int i = i0; i < i1; ++i) {
+        const int t = tg.first + i * tg.G, seg = t / tg.tps, lt = t % tg.tps;
+        const int Rt = min(TR, Ns - lt * TR);
+        for (int h = 0; h * HROWS < Rt; ++h) {
+          const int r0 = h * HROWS, rh = min(HROWS, Rt - r0);
+          const uint8_t* blk = wseg[seg] + block_offset(dt, C, lt, Rt, b);
+          const uint32_t cb = (uint32_t)(rh * Lb * 16);
+          const uint32_t sb = dt == DT_INT4 ? (uint32_t)((rh * Lb * 4 + 15) / 16 * 16) : 0u;
+          uint8_t* dst;
+          uint64_t* fb;
+          if (!prod_slot(S, pr, err, dst, fb)) return false;
+          mbar_expect_tx(fb, cb + sb);
+          bulk_g2s(dst, blk + (size_t)r0 * Lb * 16, cb, fb, pr.pol);
+          if (sb) bulk_g2s(dst + SLOT_SZ_OFF, blk + (size_t)Rt * Lb * 16 + (size_t)r0 * Lb * 4, sb, fb, pr.pol);
+        }
+      }
+    }
+    i0 = i1;
+  }
+  return true;
+}
+
 // Slot order of a GEMV phase (producer and consumers walk it identically):
 // for each of the CTA's tiles t, for each half h of the tile's rows, the
 // K-blocks b in order.
@@ -222,7 +350,9 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
   bool ok = true;
   for (int pi = 0; pi < P.nphases && ok; ++pi) {
     const Phase& ph = phase_at(P, pi);
-    if (ph.kind == PH_GEMV) {
+    if (ph.kind == PH_GEMV && verifying(P)) {
+      ok = produce_gemv_m(ph, P, S, pr, cta, pi);
+    } else if (ph.kind == PH_GEMV) {
       const int dt = ph.dtype, C = ph.K / per_chunk(dt);
       // a phase covers nseg matrices of Ns rows each (two experts for MOE_GU)
       const int nseg = ph.moe == MOE_GU ? 2 : 1, Ns = ph.N / nseg;
@@ -258,14 +388,13 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
         }
       }
     } else if (ph.kind == PH_ATTN) {
-      const int T = pos + 1, Ts = ph.stream_cur ? T : T - 1;
-      int CH, nch;
-      attn_split(T, ph.Hkv, P.unit_target, CH, nch);
-      const int nunits = ph.Hkv * nch;
       const uint32_t rowb = (uint32_t)ph.hd * 2;
+      const int nunits = attn_units(ph, P, pos, -1, nullptr);
       for (int u = first_unit(cta, ph.rot, G); u < nunits && ok; u += G) {
-        const int hh = u / nch, c = u % nch;
-        const int p0 = c * CH, p1 = min(p0 + CH, T), pe = min(p1, Ts);
+        AttnUnit au;
+        attn_units(ph, P, pos, u, &au);
+        const int hh = au.kvh;
+        const int p0 = au.p0, p1 = au.p1, pe = min(p1, au.Ts);
         for (int p = p0; p < pe; p += ATT_POS_PER_SLOT) {
           const int np = min(ATT_POS_PER_SLOT, pe - p);
           uint8_t* dst;
@@ -740,41 +869,42 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
 // chunks merges its chunks' (m, l, o) in the CTA that finishes last
 // (log-sum-exp combine).
 template <int HD>
-__device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int u, int nch, int CH, int pos,
+__device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, const AttnUnit& au, int pos,
                           uint32_t& j) {
   const int gq = ph.Hq / ph.Hkv;
-  const int kvh = u / nch, c = u % nch;
-  const int T = pos + 1, Ts = ph.stream_cur ? T : T - 1;
-  const int p0 = c * CH, p1 = min(p0 + CH, T), pe = min(p1, Ts);
+  const int kvh = au.kvh, c = au.c, nch = au.nch;
+  const int p0 = au.p0, p1 = au.p1, pe = min(p1, au.Ts);
   const int lane = cs.lane, w = cs.warp;
+  const size_t qrow = (size_t)au.m * ph.Hq * HD;  // this unit's query / output row
   float* qs = S.xs;                       // [gq][HD], pre-scaled by 1/sqrt(HD)
   float* sc = S.xs + MAX_GQ * HD;         // [NCW][gq][HD + 2]
   const int nslots = pe > p0 ? (pe - p0 + ATT_POS_PER_SLOT - 1) / ATT_POS_PER_SLOT : 0;
-  // positions not streamed (the row written by this step) go to the warp
-  // after the last slot's owner; its loads are issued first (lanes 0..15)
+  // positions not streamed (rows written during this launch) go to the warp
+  // after the last slot's owner; the first two are loaded up front
   const int pg = max(pe, p0);
   const int gw = (int)((cs.it + j + (uint32_t)nslots) % NCW);
   const bool has_g = (w == gw) && pg < p1;
   uint32_t gk[HD / 32], gv[HD / 32];
 #pragma unroll
   for (int e = 0; e < HD / 32; ++e) gk[e] = gv[e] = 0u;
-  if (has_g && lane < 16) {
-    const size_t off = ((size_t)kvh * ph.Tmax + pg) * HD + lane * (HD / 16);
+  auto load_global = [&](int p, uint32_t* kw, uint32_t* vw) {
+    const size_t off = ((size_t)kvh * ph.Tmax + p) * HD + (lane & 15) * (HD / 16);
     if constexpr (HD / 16 == 8) {
       const uint4 kk = __ldcg(reinterpret_cast<const uint4*>(ph.kc + off));
       const uint4 vv = __ldcg(reinterpret_cast<const uint4*>(ph.vc + off));
-      gk[0] = kk.x; gk[1] = kk.y; gk[2] = kk.z; gk[3] = kk.w;
-      gv[0] = vv.x; gv[1] = vv.y; gv[2] = vv.z; gv[3] = vv.w;
+      kw[0] = kk.x; kw[1] = kk.y; kw[2] = kk.z; kw[3] = kk.w;
+      vw[0] = vv.x; vw[1] = vv.y; vw[2] = vv.z; vw[3] = vv.w;
     } else {
       const uint2 kk = __ldcg(reinterpret_cast<const uint2*>(ph.kc + off));
       const uint2 vv = __ldcg(reinterpret_cast<const uint2*>(ph.vc + off));
-      gk[0] = kk.x; gk[1] = kk.y;
-      gv[0] = vv.x; gv[1] = vv.y;
+      kw[0] = kk.x; kw[1] = kk.y;
+      vw[0] = vv.x; vw[1] = vv.y;
     }
-  }
+  };
+  if (has_g && pg + (lane >> 4) < p1) load_global(pg + (lane >> 4), gk, gv);
   const float scale = rsqrtf((float)HD);
   for (int i = cs.ctid; i < gq * HD; i += NCW * 32) {
-    const size_t qi = (size_t)kvh * gq * HD + i;
+    const size_t qi = qrow + (size_t)kvh * gq * HD + i;
     const float qv = ph.q_f32 ? __ldcg(reinterpret_cast<const float*>(ph.qbuf) + qi)
                               : bf2f(__ldcg(reinterpret_cast<const uint16_t*>(ph.qbuf) + qi));
     qs[i] = qv * scale;
@@ -852,7 +982,16 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
     slot_release(S, cs, it);
   }
   j += (uint32_t)nslots;
-  if (has_g) consume2(gk, gv, half == 0);
+  if (has_g) {
+    consume2(gk, gv, pg + half < p1);
+    for (int p = pg + 2; p < p1; p += 2) {
+      uint32_t kw[DP2 / 2], vw[DP2 / 2];
+#pragma unroll
+      for (int e = 0; e < DP2 / 2; ++e) kw[e] = vw[e] = 0u;
+      if (p + half < p1) load_global(p + half, kw, vw);
+      consume2(kw, vw, p + half < p1);
+    }
+  }
   // merge the two half-warps (xor 16), then the warps of this CTA
 #pragma unroll
   for (int jj = 0; jj < MAX_GQ; ++jj) {
@@ -891,10 +1030,10 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
     }
     const int hq = kvh * gq + jj;
     if (nch == 1) {  // the whole head was here
-      if (ph.out_f32) reinterpret_cast<float*>(ph.attn_out)[(size_t)hq * HD + d] = O / L;
-      else reinterpret_cast<uint16_t*>(ph.attn_out)[(size_t)hq * HD + d] = f2bf(O / L);
+      if (ph.out_f32) reinterpret_cast<float*>(ph.attn_out)[qrow + (size_t)hq * HD + d] = O / L;
+      else reinterpret_cast<uint16_t*>(ph.attn_out)[qrow + (size_t)hq * HD + d] = f2bf(O / L);
     } else {
-      float* part = ph.part + ((size_t)hq * nch + c) * stride;
+      float* part = ph.part + (((size_t)au.m * ph.Hq + hq) * nch + c) * stride;
       part[2 + d] = O;
       if (d == 0) {
         part[0] = M;
@@ -905,8 +1044,9 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   if (nch == 1) return true;
   __threadfence();
   if (!cta_sync(S, cs, P.err)) return false;
+  unsigned* tick = ph.tick + (size_t)au.m * ph.Hkv + kvh;
   if (cs.ctid == 0) {
-    const unsigned old = atomicAdd(ph.tick + kvh, 1u);
+    const unsigned old = atomicAdd(tick, 1u);
     S.bcast[0] = (old == (unsigned)(nch - 1));
   }
   if (!cta_sync(S, cs, P.err)) return false;
@@ -914,7 +1054,7 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
     __threadfence();
     for (int i = cs.ctid; i < gq * HD; i += NCW * 32) {
       const int jj = i / HD, d = i % HD, hq = kvh * gq + jj;
-      const float* pb = ph.part + (size_t)hq * nch * stride;
+      const float* pb = ph.part + ((size_t)au.m * ph.Hq + hq) * nch * stride;
       float M = -INFINITY;
       for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(pb + cc * stride));
       float L = 0.f, O = 0.f;
@@ -923,10 +1063,408 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
         L = fmaf(__ldcg(pb + cc * stride + 1), e, L);
         O = fmaf(__ldcg(pb + cc * stride + 2 + d), e, O);
       }
-      if (ph.out_f32) reinterpret_cast<float*>(ph.attn_out)[(size_t)hq * HD + d] = O / L;
-      else reinterpret_cast<uint16_t*>(ph.attn_out)[(size_t)hq * HD + d] = f2bf(O / L);
+      if (ph.out_f32) reinterpret_cast<float*>(ph.attn_out)[qrow + (size_t)hq * HD + d] = O / L;
+      else reinterpret_cast<uint16_t*>(ph.attn_out)[qrow + (size_t)hq * HD + d] = f2bf(O / L);
     }
-    if (cs.ctid == 0) ph.tick[kvh] = 0u;
+    if (cs.ctid == 0) *tick = 0u;
+  }
+  return true;
+}
+
+// ========================================================= verify pass ====
+// A speculative-verification pass (gpt-fast README, "Speculative sampling")
+// feeds M rows (the last accepted token and the drafts) at positions
+// pos..pos+M-1 through every layer with ONE stream of the weights.  GEMV
+// phases then work K-block by K-block over groups of up to VTG tiles: the
+// CTA stages the K-block's inputs of all M rows (fp32, swizzled per chunk),
+// each slot's owner warp dequantises its codes once and multiplies them with
+// the M rows, reduces over its lanes and adds the row sums into a shared
+// accumulator (each (row, m) has one writer per K-block, K-blocks in order:
+// deterministic); the group's epilogues then run per (row, m).
+struct VS {
+  float* xk;    // [MAX_M][KBLK chunks][E] inputs of the current K-block
+  float* xgk;   // [MAX_M][KBLK] their sums per 32-wide group (int4)
+  float* acc;   // [VTG * TR][MAX_M] row sums of the tile group
+  float* rfac;  // [MAX_M] RMSNorm factors
+};
+__device__ __forceinline__ VS vsmem(const Smem& S) {
+  VS v;
+  v.xk = S.xs;
+  v.xgk = v.xk + MAX_M * KBLK * 32;
+  v.acc = v.xgk + MAX_M * KBLK;
+  v.rfac = v.acc + VTG * TR * MAX_M;
+  return v;
+}
+
+// Row m of the phase's input, element k: the source a decode step would read.
+__device__ __forceinline__ float4 vin4(const Phase& ph, const Params& P, const VS& V, int m, int e, int k4) {
+  if (ph.xsrc == X_F32) {
+    const float* x = reinterpret_cast<const float*>(ph.xptr) + (size_t)m * ph.x_mstride + (size_t)e * ph.x_sstride;
+    return __ldcg(reinterpret_cast<const float4*>(x) + k4);
+  }
+  float4 a;
+  if (ph.xsrc == X_EMBED_NORM) a = bf4(*reinterpret_cast<const uint2*>(P.embed + (size_t)P.tokens[m] * ph.K + 4 * k4));
+  else a = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ph.xptr) + (size_t)m * ph.K) + k4);
+  const float4 g = bf4(reinterpret_cast<const uint2*>(ph.gain)[k4]);
+  const float r = V.rfac[m];
+  return make_float4(a.x * r * g.x, a.y * r * g.y, a.z * r * g.z, a.w * r * g.w);
+}
+
+// RMSNorm factors of the M rows (and, for the first layer, the residual rows
+// written from the embedding by CTA 0).
+__device__ bool verify_norm(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
+  const VS V = vsmem(S);
+  const int K4 = ph.K / 4;
+  for (int m = cs.warp; m < P.M; m += NCW) {
+    float ss = 0.f;
+    for (int k4 = cs.lane; k4 < K4; k4 += 32) {
+      float4 a;
+      if (ph.xsrc == X_EMBED_NORM) {
+        a = bf4(*reinterpret_cast<const uint2*>(P.embed + (size_t)P.tokens[m] * ph.K + 4 * k4));
+        if (cta == 0) reinterpret_cast<float4*>(P.resid + (size_t)m * ph.K)[k4] = a;
+      } else {
+        a = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ph.xptr) + (size_t)m * ph.K) + k4);
+      }
+      ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (cs.lane == 0) V.rfac[m] = 1.0f / sqrtf(ss / (float)ph.K + ph.eps);
+  }
+  return cta_sync(S, cs, P.err);
+}
+
+// Router of a verify pass: logits for every (row, expert), top-2 per row,
+// weights into moew (0 for experts a row did not choose), and the union of
+// the chosen experts in index order for the producer.
+__device__ bool verify_route(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int pi) {
+  const VS V = vsmem(S);
+  const int K4 = ph.K / 4, E = ph.n_experts;
+  float* rl = S.moew;  // logits first, weights after
+  for (int q = cs.warp; q < P.M * E; q += NCW) {
+    const int m = q / E, e = q % E;
+    const uint2* wr = reinterpret_cast<const uint2*>(ph.router + (size_t)e * ph.K);
+    float acc = 0.f;
+    for (int k4 = cs.lane; k4 < K4; k4 += 32) {
+      const float4 x = vin4(ph, P, V, m, 0, k4);
+      const float4 wv = bf4(wr[k4]);
+      acc = fmaf(x.x, wv.x, fmaf(x.y, wv.y, fmaf(x.z, wv.z, fmaf(x.w, wv.w, acc))));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (cs.lane == 0) rl[m * 8 + e] = acc;
+  }
+  if (!cta_sync(S, cs, P.err)) return false;
+  if (cs.ctid == 0) {
+    unsigned used = 0u;
+    for (int m = 0; m < P.M; ++m) {
+      float* r = rl + m * 8;
+      int e1 = 0;
+      for (int e = 1; e < E; ++e)
+        if (r[e] > r[e1]) e1 = e;
+      int e2 = e1 == 0 ? 1 : 0;
+      for (int e = 0; e < E; ++e)
+        if (e != e1 && r[e] > r[e2]) e2 = e;
+      const float b = expf(r[e2] - r[e1]);
+      const float w1 = 1.0f / (1.0f + b), w2 = b / (1.0f + b);
+      for (int e = 0; e < 8; ++e) r[e] = e == e1 ? w1 : e == e2 ? w2 : 0.0f;
+      used |= (1u << e1) | (1u << e2);
+    }
+    int n = 0;
+    for (int e = 0; e < E; ++e)
+      if (used & (1u << e)) S.bcast[48 + n++] = e;
+    S.bcast[56] = n;
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(S.bcast + 34) = pi + 1;  // releases the producer
+  }
+  return cta_sync(S, cs, P.err);
+}
+
+// Epilogue of row n (value y, partner row n ^ 1 value yp) for input row m.
+__device__ __forceinline__ void gemv_epilogue_m(const Phase& ph, const Params& P, const Smem& S, int e, int n, int m,
+                                                float y, float yp, int pos, ArgMax* am) {
+  switch (ph.epi) {
+    case EPI_STORE_F32:
+      reinterpret_cast<float*>(ph.out)[(size_t)m * ph.out_mstride + n] = y;
+      break;
+    case EPI_RESID:
+      atomicAdd(reinterpret_cast<float*>(ph.out) + (size_t)m * ph.out_mstride + n, y);
+      break;
+    case EPI_SWIGLU:
+      if ((n & 1) == 0) reinterpret_cast<float*>(ph.out)[(size_t)m * ph.out_mstride + (n >> 1)] = y / (1.0f + expf(-y)) * yp;
+      break;
+    case EPI_MOE_SWIGLU:  // h of (row m, expert e)
+      if ((n & 1) == 0)
+        reinterpret_cast<float*>(ph.out)[((size_t)m * 8 + e) * ph.out_mstride + (n >> 1)] = y / (1.0f + expf(-y)) * yp;
+      break;
+    case EPI_MOE_RESID: {
+      const float wgt = S.moew[m * 8 + e];
+      if (wgt != 0.0f) atomicAdd(reinterpret_cast<float*>(ph.out) + (size_t)m * ph.out_mstride + n, wgt * y);
+      break;
+    }
+    case EPI_QKV: {
+      const int hd = ph.hd, p = pos + m;
+      if (n < ph.q_rows + ph.kv_rows) {
+        if ((n & 1) == 0) {
+          const bool isq = n < ph.q_rows;
+          const int nn = isq ? n : n - ph.q_rows;
+          const int d = nn % hd;
+          const float2 cs = P.rope[(size_t)p * (hd / 2) + d / 2];
+          const float o0 = y * cs.x - yp * cs.y, o1 = y * cs.y + yp * cs.x;
+          if (isq) {
+            float* q = reinterpret_cast<float*>(ph.qbuf) + (size_t)m * ph.q_rows + n;
+            q[0] = o0;
+            q[1] = o1;
+          } else {
+            uint16_t* k = ph.kc + ((size_t)(nn / hd) * ph.Tmax + p) * hd + d;
+            k[0] = f2bf(o0);
+            k[1] = f2bf(o1);
+          }
+        }
+      } else {
+        const int nn = n - ph.q_rows - ph.kv_rows;
+        ph.vc[((size_t)(nn / hd) * ph.Tmax + p) * hd + nn % hd] = f2bf(y);
+      }
+      break;
+    }
+    case EPI_LOGITS:
+      P.logits[(size_t)m * P.vocab + n] = y;
+      amax_merge(am[m], y, n);
+      break;
+    default:
+      break;
+  }
+}
+
+template <int DT>
+__device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta, int pos, int pi,
+                             ArgMax* am) {
+  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
+  constexpr int U = E / 4;
+  constexpr int WP = E / 8;  // input pairs per 32-bit word of codes
+  const VS V = vsmem(S);
+  const int M = P.M;
+  const int C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
+  const int lane = cs.lane, w = cs.warp;
+  if ((ph.xsrc == X_NORM || ph.xsrc == X_EMBED_NORM) && !verify_norm(ph, P, S, cs, cta)) return false;
+  if (ph.moe == MOE_GU && !verify_route(ph, P, S, cs, pi)) return false;
+  int Ns;
+  const uint8_t* wseg[8];
+  int eseg[8];
+  const int nseg = gemv_segments(ph, P, S, Ns, wseg, eseg);
+  TileGroups tg;
+  tg.tps = (Ns + TR - 1) / TR;
+  tg.ntiles = nseg * tg.tps;
+  tg.G = P.nctas;
+  tg.first = first_unit(cta, ph.rot, P.nctas);
+  for (int i = cs.ctid; i < VTG * TR * MAX_M; i += NCW * 32) V.acc[i] = 0.f;
+  const float4* xk4 = reinterpret_cast<const float4*>(V.xk);
+  uint32_t j = 0;
+  for (int i0 = 0; tg.first + i0 * tg.G < tg.ntiles;) {
+    const int i1 = group_end(tg, i0);
+    const int seg = (tg.first + i0 * tg.G) / tg.tps, e = eseg[seg];
+    for (int b = 0; b < nb; ++b) {
+      const int Lb = min(KBLK, C - b * KBLK);
+      // stage the K-block's inputs of the M rows
+      const int per_m = KBLK * U;  // float4 per row
+      for (int q0 = 0; q0 < MAX_M * per_m; q0 += NCW * 32) {
+        const int q = q0 + cs.ctid, m = q / per_m, f4 = q % per_m, l = f4 / U, u = f4 % U;
+        const bool ok = m < M && l < Lb;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok) a = vin4(ph, P, V, m, e, (b * KBLK + l) * U + u);
+        if (ok) reinterpret_cast<float4*>(V.xk)[m * per_m + l * U + (u ^ swz(l, U))] = a;
+        if (DT == DT_INT4) {
+          float sg = a.x + a.y + a.z + a.w;
+          sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+          sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+          sg += __shfl_xor_sync(0xffffffffu, sg, 4);
+          if (ok && (lane & 7) == 0) V.xgk[m * KBLK + l] = sg;
+        }
+      }
+      if (!cta_sync(S, cs, P.err)) return false;
+      for (int i = i0; i < i1; ++i) {
+        const int t = tg.first + i * tg.G, lt = t % tg.tps;
+        const int Rt = min(TR, Ns - lt * TR);
+        for (int h = 0; h * HROWS < Rt; ++h, ++j) {
+          const uint32_t it = cs.it + j;
+          if ((int)(it % NCW) != w) continue;
+          const uint8_t* base;
+          if (!slot_acquire(S, cs, it, P.err, base)) return false;
+          const bool lane_ok = lane < Lb;
+          const int sw = swz(lane, U);
+          const uint32_t* wbase = reinterpret_cast<const uint32_t*>(base) + lane * 4;
+#pragma unroll 1
+          for (int rb = 0; rb < HROWS; rb += 4) {
+            float2 a[4][MAX_M];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+              for (int m = 0; m < MAX_M; ++m) a[r][m] = make_float2(0.f, 0.f);
+#pragma unroll 1
+            for (int jw = 0; jw < 4; ++jw) {
+              float2 xp[MAX_M][WP];
+#pragma unroll
+              for (int m = 0; m < MAX_M; ++m) {
+                if (m < M) {
+                  const float4* xm = xk4 + m * (KBLK * U) + lane * U;
+                  if (DT == DT_INT4) {
+                    const float4 xa = xm[(2 * jw) ^ sw], xb = xm[(2 * jw + 1) ^ sw];
+                    xp[m][0] = make_float2(xa.x, xa.y);
+                    xp[m][1 % WP] = make_float2(xa.z, xa.w);
+                    xp[m][2 % WP] = make_float2(xb.x, xb.y);
+                    xp[m][3 % WP] = make_float2(xb.z, xb.w);
+                  } else if (DT == DT_INT8) {
+                    const float4 xa = xm[jw ^ sw];
+                    xp[m][0] = make_float2(xa.x, xa.y);
+                    xp[m][1 % WP] = make_float2(xa.z, xa.w);
+                  } else {
+                    const float4 xa = xm[(jw >> 1) ^ sw];
+                    xp[m][0] = (jw & 1) ? make_float2(xa.z, xa.w) : make_float2(xa.x, xa.y);
+                  }
+                } else {
+#pragma unroll
+                  for (int i2 = 0; i2 < WP; ++i2) xp[m][i2] = make_float2(0.f, 0.f);
+                }
+              }
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                const uint32_t wv = wbase[(rb + r) * Lb * 4 + jw];
+                float2 qv[WP];
+                if (DT == DT_INT4) {
+#pragma unroll
+                  for (int i2 = 0; i2 < 4; ++i2) {
+                    const uint32_t v = i2 ? __funnelshift_r(wv, wv, 8 * i2) : wv;
+                    qv[i2 % WP] = __fadd2_rn(make_float2(__uint_as_float((v & 0x00078000u) | 0x3F800000u),
+                                                         __uint_as_float((v & 0x00780000u) | 0x3F800000u)),
+                                             make_float2(-1.0f, -1.0f));
+                  }
+                } else if (DT == DT_INT8) {
+                  float f[4];
+#pragma unroll
+                  for (int i2 = 0; i2 < 4; ++i2) {
+                    const uint32_t v = i2 ? __funnelshift_r(wv, wv, 8 * i2) : wv;
+                    f[i2] = __uint_as_float((v & 0x007F8000u) ^ 0x3FC00000u);
+                  }
+                  qv[0] = __fadd2_rn(make_float2(f[0], f[1]), make_float2(-1.5f, -1.5f));
+                  qv[1 % WP] = __fadd2_rn(make_float2(f[2], f[3]), make_float2(-1.5f, -1.5f));
+                } else {
+                  qv[0] = make_float2(__uint_as_float(wv << 16), __uint_as_float(wv & 0xFFFF0000u));
+                }
+#pragma unroll
+                for (int m = 0; m < MAX_M; ++m)
+#pragma unroll
+                  for (int i2 = 0; i2 < WP; ++i2) a[r][m] = ffma2(qv[i2], xp[m][i2], a[r][m]);
+              }
+            }
+            // per (row, m) contributions, then a reduce-scatter over the lanes:
+            // lane l ends with the total of row l >> 3 of the batch, input row l & 7
+            float v[32];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              uint32_t sz = 0u;
+              if (DT == DT_INT4) sz = reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF)[(rb + r) * Lb + lane];
+#pragma unroll
+              for (int m = 0; m < MAX_M; ++m) {
+                float c;
+                if (DT == DT_INT4) {
+                  const float Sq = fmaf(256.0f, a[r][m].x, 16.0f * a[r][m].y);
+                  c = fmaf(__uint_as_float(sz << 16), Sq, __uint_as_float(sz & 0xFFFF0000u) * V.xgk[m * KBLK + lane]);
+                } else {
+                  c = a[r][m].x + a[r][m].y;
+                }
+                v[r * 8 + m] = (lane_ok && m < M) ? c : 0.0f;
+              }
+            }
+#pragma unroll
+            for (int sft = 16, n = 32; sft >= 1; sft >>= 1, n >>= 1) {
+              const bool hi = lane & sft;
+#pragma unroll
+              for (int k = 0; k < n / 2; ++k) {
+                const float keep = hi ? v[k + n / 2] : v[k];
+                const float send = hi ? v[k] : v[k + n / 2];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+              }
+            }
+            const int rr = h * HROWS + rb + (lane >> 3), m = lane & 7;
+            if (m < M) V.acc[((i - i0) * TR + rr) * MAX_M + m] += v[0];
+          }
+          slot_release(S, cs, it);
+        }
+      }
+      if (!cta_sync(S, cs, P.err)) return false;
+    }
+    // epilogues of the group: one thread per (row pair, m)
+    const uint16_t* s8 = ph.s8;
+    if (DT == DT_INT8 && ph.moe != MOE_NONE) s8 += (size_t)e * Ns;
+    for (int q = cs.ctid; q < (i1 - i0) * (TR / 2) * M; q += NCW * 32) {
+      const int m = q % M, pr = q / M, gi = pr / (TR / 2), r = (pr % (TR / 2)) * 2;
+      const int t = tg.first + (i0 + gi) * tg.G, lt = t % tg.tps;
+      const int Rt = min(TR, Ns - lt * TR);
+      for (int k = 0; k < 2; ++k) {
+        if (r + k >= Rt) break;
+        const int n = lt * TR + r + k;
+        float y = V.acc[(gi * TR + r + k) * MAX_M + m];
+        float yp = (r + (k ^ 1) < Rt) ? V.acc[(gi * TR + r + (k ^ 1)) * MAX_M + m] : 0.f;
+        if (DT == DT_INT8) {
+          y *= 256.0f * bf2f(s8[n]);
+          if (r + (k ^ 1) < Rt) yp *= 256.0f * bf2f(s8[n ^ 1]);
+        }
+        gemv_epilogue_m(ph, P, S, e, n, m, y, yp, pos, am);
+      }
+    }
+    if (!cta_sync(S, cs, P.err)) return false;
+    for (int q = cs.ctid; q < VTG * TR * MAX_M; q += NCW * 32) V.acc[q] = 0.f;
+    if (!cta_sync(S, cs, P.err)) return false;
+    i0 = i1;
+  }
+  cs.it += j;
+  return true;
+}
+
+// Argmax of every row of a verify pass, then the greedy acceptance: with a_m
+// the argmax of row m and d_i = tokens[i] the drafts, n = the largest n with
+// a_{i-1} == d_i for all i <= n; next token a_n; the position advances by n+1.
+__device__ bool verify_finish(const Params& P, const Smem& S, Cons& cs, int cta, ArgMax* am) {
+  for (int m = 0; m < P.M; ++m) {
+    ArgMax a = am[m];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float v = __shfl_xor_sync(0xffffffffu, a.v, o);
+      const int i = __shfl_xor_sync(0xffffffffu, a.i, o);
+      amax_merge(a, v, i);
+    }
+    if (cs.lane == 0) {
+      S.red[cs.warp * 8 + m] = a.v;  // red has 64 floats: warps x rows <= 7 x 8
+      S.bcast[cs.warp * 8 + m] = a.i;
+    }
+  }
+  if (!cta_sync(S, cs, P.err)) return false;
+  if (cs.ctid == 0) {
+    for (int m = 0; m < P.M; ++m) {
+      ArgMax b = {S.red[m], S.bcast[m]};
+      for (int w = 1; w < NCW; ++w) amax_merge(b, S.red[w * 8 + m], S.bcast[w * 8 + m]);
+      P.amax_val[cta * MAX_M + m] = b.v;
+      P.amax_idx[cta * MAX_M + m] = b.i;
+    }
+    __threadfence();
+    const unsigned old = atomicAdd(P.amax_tick, 1u);
+    if (old == (unsigned)(P.nctas - 1)) {
+      __threadfence();
+      int a[MAX_M];
+      for (int m = 0; m < P.M; ++m) {
+        ArgMax g = {-INFINITY, 0x7fffffff};
+        for (int k = 0; k < P.nctas; ++k)
+          amax_merge(g, __ldcg(P.amax_val + k * MAX_M + m), __ldcg(P.amax_idx + k * MAX_M + m));
+        a[m] = g.i;
+      }
+      int n = 0;
+      while (n < P.M - 1 && a[n] == P.tokens[n + 1]) ++n;
+      *P.n_accepted = n;
+      *P.next_token = a[n];
+      *P.amax_tick = 0u;
+      int* pos = const_cast<int*>(P.d_pos);
+      *pos = *pos + n + 1;
+    }
   }
   return true;
 }
@@ -1033,6 +1571,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     if (tid == 0) atomicCAS(P.err, 0, ERR_BAD_TOKEN);
     return;
   }
+  if (verifying(P)) {
+    bool bad = P.M < 1 || P.M > MAX_M || pos + P.M > P.tmax;
+    for (int m = 0; m < P.M; ++m) bad |= P.tokens[m] < 0 || P.tokens[m] >= P.vocab;
+    if (bad) {
+      if (tid == 0) atomicCAS(P.err, 0, ERR_BAD_TOKEN);
+      return;
+    }
+  }
 
   if (warp == NCW) {
     if (lane == 0) producer(P, S, cta, pos);
@@ -1049,6 +1595,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   cs.starved = 0;
   const int G = P.nctas;
   ArgMax am = {-INFINITY, 0x7fffffff};
+  ArgMax amv[MAX_M];
+#pragma unroll
+  for (int m = 0; m < MAX_M; ++m) amv[m] = am;
   bool any_logits = false;
 
   for (int pi = 0; pi < P.nphases; ++pi) {
@@ -1063,7 +1612,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
       if (!cta_sync(S, cs, P.err)) return;
     }
     if (tr) tr[1] = gtimer();
-    if (ph.kind == PH_GEMV) {
+    if (ph.kind == PH_GEMV && verifying(P)) {
+      if (tr) tr[2] = gtimer();
+      bool ok;
+      if (ph.dtype == DT_INT4) ok = gemv_phase_m<DT_INT4>(ph, P, S, cs, cta, pos, pi, amv);
+      else if (ph.dtype == DT_INT8) ok = gemv_phase_m<DT_INT8>(ph, P, S, cs, cta, pos, pi, amv);
+      else ok = gemv_phase_m<DT_BF16>(ph, P, S, cs, cta, pos, pi, amv);
+      if (!ok) return;
+      if (ph.epi == EPI_LOGITS) any_logits = true;
+    } else if (ph.kind == PH_GEMV) {
       if (!stage_x(ph, P, S, cs, cta)) return;
       if (ph.moe == MOE_GU && !route_experts(ph, P, S, cs, pi)) return;
       if (tr) tr[2] = gtimer();
@@ -1075,14 +1632,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
       if (ph.epi == EPI_LOGITS) any_logits = true;
     } else if (ph.kind == PH_ATTN) {
       if (tr) tr[2] = tr[1];
-      const int T = pos + 1;
-      int CH, nch;
-      attn_split(T, ph.Hkv, P.unit_target, CH, nch);
-      const int nunits = ph.Hkv * nch;
+      const int nunits = attn_units(ph, P, pos, -1, nullptr);
       uint32_t j = 0;
       for (int u = first_unit(cta, ph.rot, G); u < nunits; u += G) {
-        const bool ok = ph.hd == 128 ? attn_unit<128>(ph, P, S, cs, u, nch, CH, pos, j)
-                                     : attn_unit<64>(ph, P, S, cs, u, nch, CH, pos, j);
+        AttnUnit au;
+        attn_units(ph, P, pos, u, &au);
+        const bool ok = ph.hd == 128 ? attn_unit<128>(ph, P, S, cs, au, pos, j)
+                                     : attn_unit<64>(ph, P, S, cs, au, pos, j);
         if (!ok) return;
       }
       cs.it += j;
@@ -1097,7 +1653,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     if (ph.signal_bar >= 0 && tid == 0) grid_arrive(P.bars + ph.signal_bar);
     if (tr) tr[4] = gtimer();
   }
-  if (any_logits) argmax_finish(P, S, cs, cta, am);
+  if (any_logits) {
+    if (verifying(P)) verify_finish(P, S, cs, cta, amv);
+    else argmax_finish(P, S, cs, cta, am);
+  }
 }
 
 int launch_engine(const Params& p, int grid, bool cooperative, cudaStream_t s) {

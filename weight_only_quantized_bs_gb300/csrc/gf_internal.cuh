@@ -63,13 +63,14 @@ constexpr int OFF_TB = OFF_XSUM + (KMAX / 32) * 4 + 256;  // [NTB][NCW][HROWS] p
 constexpr int OFF_TBC = OFF_TB + NTB * NCW * HROWS * 4;  // [NTB] arrival counters
 constexpr int OFF_BAR = OFF_TBC + NTB * 4;               // mbarriers
 constexpr int OFF_MISC = OFF_BAR + 320;
-constexpr int SMEM_BYTES = OFF_MISC + 512;
+constexpr int SMEM_BYTES = OFF_MISC + 1024;  // red[64] f32, bcast[64] i32, moew[64] f32, spare
 static_assert(NSLOT % NCW == 0, "ring entries must map to a fixed warp");
 static_assert((2 * NSLOT + 1) * 8 <= 320, "mbarrier area");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr int ATT_POS_PER_SLOT = 16;
 constexpr int MAX_GQ = 4;                    // q heads per kv head (GQA group)
 constexpr int MAX_M = 8;                     // rows of a verify pass
+constexpr int VTG = 4;                       // tiles per group of a multi-row GEMV phase
 
 // --------------------------------------------------------------- phases --
 enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1 };
@@ -87,7 +88,10 @@ enum Epi {
 // Mixture-of-experts role of a GEMV phase: MOE_GU runs the router and then the
 // gate/up rows of the two chosen experts (2 * N_e rows); MOE_DOWN0 / 1 run the
 // down projection of the first / second chosen expert.
-enum MoeMode { MOE_NONE = 0, MOE_GU = 1, MOE_DOWN0 = 2, MOE_DOWN1 = 3 };
+enum MoeMode { MOE_NONE = 0, MOE_GU = 1, MOE_DOWN0 = 2, MOE_DOWN1 = 3, MOE_DOWNU = 4 };
+// In a verify pass (several rows) MOE_GU streams the union of the experts the
+// rows chose (each expert once, in index order) and MOE_DOWNU the down
+// projections of that union.
 enum ErrCode {
   ERR_NONE = 0,
   ERR_WAIT_FULL = 1,
@@ -132,6 +136,10 @@ struct Phase {
   int n_experts;
   long long expert_stride; // bytes between consecutive experts' packed matrices
   const uint16_t* router;  // [n_experts][K] bf16 (MOE_GU)
+  // multi-row (verify) input addressing: row m, expert segment e of X_F32
+  int x_mstride;           // floats between rows
+  long long x_sstride;     // floats between experts (MOE_DOWNU)
+  long long out_mstride;   // elements between rows of the epilogue target
 };
 
 // Split of a decode attention over positions 0..T-1 into nch chunks of CH
@@ -172,12 +180,22 @@ struct Params {
   int vocab;
   int tmax;            // positions must lie in [0, tmax) (0: not checked)
   unsigned long long* trace;  // [nphases][nctas][TRACE_W] timestamps and counters (nullptr: off)
+  // speculative verification (tokens != nullptr): rows m = 0..M-1 are
+  // tokens[m] at pos + m, 1 <= M <= MAX_M
+  int M;               // rows of the pass (1 for a decode step)
+  const int* tokens;   // [M] token ids (verify)
+  int* n_accepted;     // verify outputs
+  int* next_token;
+  float* hbuf_moe;     // verify MoE: [MAX_M][8][ffn] SwiGLU outputs per row and expert
 };
 // Trace record of one CTA in one phase (ns of %globaltimer, then counters):
 // 0 phase entered, 1 grid barrier passed, 2 input staged, 3 units done,
 // 4 phase closed, 5 producer finished issuing the phase, 6 consumer slot
 // waits that found the slot empty, 7 producer waits that found no free slot.
 constexpr int TRACE_W = 8;
+
+// A launch is a verification pass when it carries its rows' tokens.
+__host__ __device__ __forceinline__ bool verifying(const Params& P) { return P.tokens != nullptr; }
 
 // ------------------------------------------------------------ host side --
 void set_error(const char* fmt, ...);

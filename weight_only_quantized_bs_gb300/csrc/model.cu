@@ -32,8 +32,12 @@ struct gf_kv {
   uint16_t *kc = nullptr, *vc = nullptr;
   float2* rope = nullptr;
   float *qbuf = nullptr, *attn = nullptr, *h = nullptr;
-  float* resid = nullptr;
+  float* resid = nullptr;      // [MAX_M][d] (row 0: decode)
   float* part = nullptr;
+  float* hmoe = nullptr;       // verify MoE: [MAX_M][8][ffn]
+  float* vlogits = nullptr;    // verify: [MAX_M][vocab] when the caller passes no logits
+  gf::Phase* vprog = nullptr;  // verify program
+  int nvphases = 0;
   float* amax_val = nullptr;
   int* amax_idx = nullptr;
   unsigned* counters = nullptr;  // bars, then attention tickets, then the argmax ticket
@@ -228,21 +232,24 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
   const int ppl = E ? 6 : 5;  // phases per layer
   const int nph = ppl * L + 1;
   const int nbars = nph;
-  const size_t nticks = (size_t)L * Hkv;
+  const size_t nticks = (size_t)L * MAX_M * Hkv;
   kv->counter_bytes = (nbars + nticks + 1) * sizeof(unsigned);
   do {
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->kc, cache_elems * 2))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->vc, cache_elems * 2))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->rope, (size_t)Tmax * (hd / 2) * sizeof(float2)))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->qbuf, (size_t)Hq * hd * 4))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->attn, (size_t)Hq * hd * 4))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->h, (size_t)c.ffn * 4 * (c.n_experts ? 2 : 1)))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->resid, (size_t)c.d * 4))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->part, (size_t)Hq * nch_max * (hd + 2) * 4))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_val, (size_t)G * 4))) break;
-    if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_idx, (size_t)G * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->qbuf, (size_t)MAX_M * Hq * hd * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->attn, (size_t)MAX_M * Hq * hd * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->h, (size_t)MAX_M * c.ffn * 4 * (c.n_experts ? 2 : 1)))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->resid, (size_t)MAX_M * c.d * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->part, (size_t)MAX_M * Hq * nch_max * (hd + 2) * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_val, (size_t)G * MAX_M * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_idx, (size_t)G * MAX_M * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->vlogits, (size_t)MAX_M * c.vocab * 4))) break;
+    if (c.n_experts && (rc = dev_alloc(kv->allocs, (void**)&kv->hmoe, (size_t)MAX_M * 8 * c.ffn * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->counters, kv->counter_bytes))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->prog, (size_t)nph * sizeof(Phase)))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->vprog, (size_t)(5 * L + 1) * sizeof(Phase)))) break;
   } while (0);
   if (rc) {
     free_all(kv->allocs);
@@ -310,7 +317,7 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[1].hd = hd;
     P[1].Tmax = Tmax;
     P[1].part = kv->part;
-    P[1].tick = kv->ticks + (size_t)l * Hkv;
+    P[1].tick = kv->ticks + (size_t)l * MAX_M * Hkv;
     P[1].stream_cur = 0;
     P[1].rot = (int)(cum_units % G);
     // o projection + residual
@@ -376,6 +383,49 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
   }
   kv->nphases = nph;
   if (e == cudaSuccess) e = cudaMemcpy(kv->prog, ph.data(), ph.size() * sizeof(Phase), cudaMemcpyHostToDevice);
+
+  // The verify program: the same layers over up to MAX_M rows, each GEMV
+  // phase reading its rows' inputs at a row stride; a MoE layer streams the
+  // union of the rows' experts (gate/up, then down) once.
+  const int nvph = 5 * L + 1;
+  std::vector<Phase> vp(nvph);
+  memset(vp.data(), 0, vp.size() * sizeof(Phase));
+  cum_units = 0;
+  for (int l = 0; l < L; ++l) {
+    Phase* P = &vp[5 * l];
+    const Phase* D = &ph[ppl * l];
+    P[0] = D[0];  // q/k/v: rows m at pos + m
+    P[0].out_mstride = 0;
+    P[1] = D[1];  // attention of each row
+    P[2] = D[2];  // o
+    P[2].x_mstride = Hq * hd;
+    P[2].out_mstride = c.d;
+    if (!E) {
+      P[3] = D[3];
+      P[3].out_mstride = c.ffn;
+      P[4] = D[4];
+      P[4].x_mstride = c.ffn;
+      P[4].out_mstride = c.d;
+    } else {
+      P[3] = D[3];  // router + gate/up of the union of experts
+      P[3].N = m->gu[l].N;
+      P[3].out = kv->hmoe;
+      P[3].out_mstride = c.ffn;
+      P[4] = D[4];  // down projections of the union, weighted per row
+      P[4].moe = MOE_DOWNU;
+      P[4].xptr = kv->hmoe;
+      P[4].x_mstride = 8 * c.ffn;
+      P[4].x_sstride = c.ffn;
+      P[4].out_mstride = c.d;
+    }
+  }
+  vp[nvph - 1] = ph[nph - 1];
+  for (int i = 0; i < nvph; ++i) {
+    vp[i].wait_bar = i == 0 ? -1 : i - 1;
+    vp[i].signal_bar = i == nvph - 1 ? -1 : i;
+  }
+  kv->nvphases = nvph;
+  if (e == cudaSuccess) e = cudaMemcpy(kv->vprog, vp.data(), vp.size() * sizeof(Phase), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     rc = cuda_fail(e, "gf_kv_create");
     free_all(kv->allocs);
@@ -470,6 +520,7 @@ static int decode_launch(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t
   p.vocab = m->cfg.vocab;
   p.tmax = kv->Tmax;
   p.trace = d_trace;
+  p.M = 1;
   if (!p.err) {
     set_error("gf_decode_step: cannot resolve the device error word");
     return GF_ECUDA;
@@ -479,10 +530,44 @@ static int decode_launch(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t
 
 int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t* d_pos, int32_t* d_n_accepted,
                 int32_t* d_next_token, float* d_logits, gf_stream stream) {
-  (void)m; (void)kv; (void)d_tokens; (void)k; (void)d_pos; (void)d_n_accepted; (void)d_next_token;
-  (void)d_logits; (void)stream;
-  set_error("gf_verify_k: not available in this build");
-  return GF_EUNSUPPORTED;
+  if (!m || !kv || kv->m != m || !d_tokens || !d_pos || !d_n_accepted || !d_next_token || k < 0 || k + 1 > MAX_M) {
+    set_error("gf_verify_k: bad arguments (k must be 0..%d)", MAX_M - 1);
+    return GF_EINVAL;
+  }
+  if (d_logits && !aligned16(d_logits)) {
+    set_error("gf_verify_k: logits must be 16-byte aligned");
+    return GF_EALIGN;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  GF_CUDA(cudaMemsetAsync(kv->counters, 0, kv->counter_bytes, s));
+  Params p;
+  memset(&p, 0, sizeof p);
+  p.prog = kv->vprog;
+  p.nphases = kv->nvphases;
+  p.d_pos = d_pos;
+  p.nctas = kv->sms;
+  p.unit_target = kv->sms;
+  p.bars = kv->bars;
+  p.err = device_err_ptr();
+  p.rope = kv->rope;
+  p.resid = kv->resid;
+  p.embed = m->embed;
+  p.logits = d_logits ? d_logits : kv->vlogits;
+  p.amax_val = kv->amax_val;
+  p.amax_idx = kv->amax_idx;
+  p.amax_tick = kv->amax_tick;
+  p.vocab = m->cfg.vocab;
+  p.tmax = kv->Tmax;
+  p.M = k + 1;
+  p.tokens = d_tokens;
+  p.n_accepted = d_n_accepted;
+  p.next_token = d_next_token;
+  p.hbuf_moe = kv->hmoe;
+  if (!p.err) {
+    set_error("gf_verify_k: cannot resolve the device error word");
+    return GF_ECUDA;
+  }
+  return launch_engine(p, kv->sms, true, s);
 }
 
 }  // extern "C"
