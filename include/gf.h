@@ -65,9 +65,9 @@ long long gf_packed_bytes(int wdtype, int N, int K);
  * another.  A block holds its Rt x Lb chunks row-major (chunk (r, l) at byte
  * 16 (r Lb + l)); for int4 it is followed by Rt x Lb 32-bit words s | z << 16
  * (the bf16 scale and zero of chunk (r, l)'s group) padded with zeros to a
- * multiple of 16 bytes.  Inside an int8 / int4 chunk, 32-bit word j is the
- * natural little-endian word (int8 code 4j+i in bits 8i..8i+7; int4 code
- * 8j+i in bits 4i..4i+3) rotated left by 15 bits.  bf16 chunks are natural.
+ * multiple of 16 bytes.  Chunks hold their weights in k order: bf16 values,
+ * int8 codes one byte each (two's complement), int4 codes two per byte (code
+ * 2i in the low nibble of byte i, code 2i+1 in the high nibble).
  */
 
 /* int8 weight-only quantisation (gpt-fast README, "Int8 weight-only

@@ -131,10 +131,10 @@ void orc_quant_w4g(const uint16_t* W, long N, long K, int G, uint8_t* q, uint16_
  *   block      = Rt*Lb code chunks, chunk (r, l) at byte 16*(r*Lb + l); for
  *                int4 followed by Rt*Lb 4-byte words (s | z << 16) at
  *                4*(r*Lb + l), zero-padded to a multiple of 16 bytes
- *   chunk body = bf16: 8 values, k ascending.  int8 / int4: four 32-bit
- *                little-endian words; word j is rotl32(n_j, 15) where n_j has
- *                int8 code k=4j+i in bits 8i..8i+7 (two's complement) or int4
- *                code k=8j+i in bits 4i..4i+3. */
+ *   chunk body = bf16: 8 values, k ascending.  int8: 16 codes, k ascending,
+ *                one byte each (two's complement).  int4: byte i holds code
+ *                k=2i in bits 0..3 and code k=2i+1 in bits 4..7 (as 32-bit
+ *                little-endian words: word j has code 8j+i in bits 4i..4i+3). */
 enum { ORC_BF16 = 0, ORC_INT8 = 1, ORC_INT4 = 2 };
 
 static int per_chunk(int dt) { return dt == ORC_BF16 ? 8 : dt == ORC_INT8 ? 16 : 32; }
@@ -153,9 +153,6 @@ long orc_packed_bytes(int dt, long N, long K, int TR) {
   }
   return total;
 }
-
-static uint32_t rotl32(uint32_t v, int r) { return (v << r) | (v >> (32 - r)); }
-static uint32_t rotr32(uint32_t v, int r) { return (v >> r) | (v << (32 - r)); }
 
 static void put32(uint8_t* p, uint32_t v) {
   p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); p[2] = (uint8_t)(v >> 16); p[3] = (uint8_t)(v >> 24);
@@ -185,18 +182,10 @@ void orc_pack(int dt, long N, long K, int TR, const void* src, const uint16_t* s
             for (int i = 0; i < 8; ++i) { ch[2 * i] = (uint8_t)w[i]; ch[2 * i + 1] = (uint8_t)(w[i] >> 8); }
           } else if (dt == ORC_INT8) {
             const int8_t* c = (const int8_t*)src + n * K + k0;
-            for (int j = 0; j < 4; ++j) {
-              uint32_t nat = 0;
-              for (int i = 0; i < 4; ++i) nat |= (uint32_t)(uint8_t)c[4 * j + i] << (8 * i);
-              put32(ch + 4 * j, rotl32(nat, 15));
-            }
+            for (int i = 0; i < 16; ++i) ch[i] = (uint8_t)c[i];
           } else {
             const uint8_t* c = (const uint8_t*)src + n * K + k0;
-            for (int j = 0; j < 4; ++j) {
-              uint32_t nat = 0;
-              for (int i = 0; i < 8; ++i) nat |= (uint32_t)(c[8 * j + i] & 15u) << (4 * i);
-              put32(ch + 4 * j, rotl32(nat, 15));
-            }
+            for (int i = 0; i < 16; ++i) ch[i] = (uint8_t)((c[2 * i] & 15u) | ((c[2 * i + 1] & 15u) << 4));
             long g = k0 / 32;
             put32(blk + Rt * Lb * 16 + 4 * (r * Lb + l),
                   (uint32_t)s[n * ng + g] | ((uint32_t)z[n * ng + g] << 16));
@@ -227,15 +216,12 @@ void orc_unpack(int dt, long N, long K, int TR, const uint8_t* in, void* dst, ui
             for (int i = 0; i < 8; ++i) w[i] = (uint16_t)(ch[2 * i] | (ch[2 * i + 1] << 8));
           } else if (dt == ORC_INT8) {
             int8_t* c = (int8_t*)dst + n * K + k0;
-            for (int j = 0; j < 4; ++j) {
-              uint32_t nat = rotr32(get32(ch + 4 * j), 15);
-              for (int i = 0; i < 4; ++i) c[4 * j + i] = (int8_t)(uint8_t)(nat >> (8 * i));
-            }
+            for (int i = 0; i < 16; ++i) c[i] = (int8_t)ch[i];
           } else {
             uint8_t* c = (uint8_t*)dst + n * K + k0;
-            for (int j = 0; j < 4; ++j) {
-              uint32_t nat = rotr32(get32(ch + 4 * j), 15);
-              for (int i = 0; i < 8; ++i) c[8 * j + i] = (uint8_t)((nat >> (4 * i)) & 15u);
+            for (int i = 0; i < 16; ++i) {
+              c[2 * i] = (uint8_t)(ch[i] & 15u);
+              c[2 * i + 1] = (uint8_t)(ch[i] >> 4);
             }
             uint32_t v = get32(blk + Rt * Lb * 16 + 4 * (r * Lb + l));
             s[n * ng + k0 / 32] = (uint16_t)v;

@@ -147,13 +147,31 @@ def test_layout_hand_words():
         assert list(packed.view("<u4")) == words
 
 
-def _views_decode_int4(word):
-    """Decode one packed int4 word the way the GEMV reads it: view i is the
-    word rotated right by 8i; its bits 15..18 hold code 2i, 19..22 code 2i+1."""
+def _subnormal_decode_int4(word):
+    """Decode one packed int4 word the way the GEMV reads it: code i sits in
+    bits p..p+3 of the word (i < 6, p = 4i) or of the word shifted right by 8
+    bits (i = 6, 7: p = 16, 20); masking those bits and reading the result as
+    an IEEE binary32 gives the exact value code * 2^(p - 149) (a subnormal,
+    or for bit 23 set the smallest normal binade, which continues it)."""
+    out = []
+    for i in range(8):
+        v, p = (word, 4 * i) if i < 6 else (word >> 8, 4 * i - 8)
+        f = np.array([v & (15 << p)], dtype=np.uint32).view(np.float32)[0]
+        q = float(f) * 2.0 ** (149 - p)
+        assert q == int(q)
+        out.append(int(q))
+    return out
+
+
+def _subnormal_decode_int8(word):
+    """int8 as the GEMV reads it: byte i (two's complement) XOR 0x80 is the
+    offset code q + 128 in bits p..p+7 of the word (i < 3, p = 8i) or of the
+    word shifted right by 8 (i = 3, p = 16), read as binary32."""
     out = []
     for i in range(4):
-        v = ((word >> (8 * i)) | (word << (32 - 8 * i))) & 0xFFFFFFFF if i else word
-        out += [(v >> 15) & 15, (v >> 19) & 15]
+        v, p = (word, 8 * i) if i < 3 else (word >> 8, 16)
+        f = np.array([(v ^ 0x80808080) & (255 << p)], dtype=np.uint32).view(np.float32)[0]
+        out.append(int(float(f) * 2.0 ** (149 - p)) - 128)
     return out
 
 
@@ -169,10 +187,14 @@ def test_layout_views_recover_codes():
         for c in range(2):
             got = []
             for j in range(4):
-                got += _views_decode_int4(int(words[(r * 2 + c) * 4 + j]))
+                got += _subnormal_decode_int4(int(words[(r * 2 + c) * 4 + j]))
             assert got == list(codes[r, 32 * c:32 * c + 32])
     sz = words[24:30]
     assert list(sz & 0xFFFF) == list(s.reshape(-1)) and list(sz >> 16) == list(z.reshape(-1))
+    codes8 = rng.integers(-127, 128, size=(2, 32)).astype(np.int8)
+    words8 = oracle.pack(oracle.INT8, 2, 32, 32, codes8).view("<u4")
+    got8 = [c for w in words8 for c in _subnormal_decode_int8(int(w))]
+    assert got8 == list(codes8.reshape(-1))
 
 
 @pytest.mark.parametrize("dt,N,K", [(0, 45, 8 * 40), (1, 70, 16 * 37), (2, 33, 32 * 45),

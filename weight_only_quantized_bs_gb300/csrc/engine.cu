@@ -468,6 +468,38 @@ __device__ __forceinline__ void slot_release(const Smem& S, const Cons& cs, uint
   if (cs.lane == 0) mbar_arrive(&S.empty[it % NSLOT]);
 }
 
+// Dequantisation through subnormals.  A code c held in bits p..p+3 (int4)
+// or p..p+7 (int8, offset to c + 128) of a 32-bit word whose other bits are
+// clear reads, as an IEEE binary32, exactly c * 2^(p - 149): a subnormal, or
+// with bit 23 set a number of the smallest normal binade, whose spacing is
+// the same, so the value stays linear in c.  That holds for every p up to 20
+// (int4) or 16 (int8); the codes of a word's top byte are taken from the word
+// shifted right by 8.  The staged input carries the inverse power (each x is
+// multiplied by 2^(85 - p) for the position p its code is read from), so a
+// fused multiply-add adds c * x * 2^-64 with one rounding, as with ordinary
+// fp32 operands: one AND per code, one packed FMA per two codes, no bias to
+// remove.  Products and partial sums are normal numbers for any input above
+// about 2^-60 in magnitude; the 2^-64 is undone in the epilogue (exact).
+// FMAs must keep subnormal operands (no flush-to-zero), which is the default.
+constexpr float DQ_UP = 18446744073709551616.0f;  // 2^64
+constexpr float DQ_DOWN = 1.0f / DQ_UP;           // 2^-64
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }  // normal range
+// multipliers of the staged inputs, per component of float4 number u of a chunk
+__device__ __forceinline__ float4 dq_mult(int dt, int u) {
+  if (dt == DT_INT4)
+    return (u & 1) ? make_float4(pow2f(69), pow2f(65), pow2f(69), pow2f(65))
+                   : make_float4(pow2f(85), pow2f(81), pow2f(77), pow2f(73));
+  if (dt == DT_INT8) return make_float4(pow2f(85), pow2f(77), pow2f(69), pow2f(69));
+  return make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+}
+__device__ __forceinline__ float4 dq_inv(int dt, int u) {
+  if (dt == DT_INT4)
+    return (u & 1) ? make_float4(pow2f(-69), pow2f(-65), pow2f(-69), pow2f(-65))
+                   : make_float4(pow2f(-85), pow2f(-81), pow2f(-77), pow2f(-73));
+  if (dt == DT_INT8) return make_float4(pow2f(-85), pow2f(-77), pow2f(-69), pow2f(-69));
+  return make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+}
 // ------------------------------------------------------ input staging ----
 __device__ __forceinline__ int swz(int g, int U) { return ((g * U) >> 3) & (U - 1); }
 
@@ -477,17 +509,22 @@ __device__ __forceinline__ float4 bf4(uint2 h) {
 }
 
 // Stores float4 number k4 of x (swizzled per chunk so that the 32 lanes of a
-// warp read their chunks without bank conflicts) and, for int4, the sum of
-// each 32-wide group (8 consecutive threads hold one group).
+// warp read their chunks without bank conflicts), multiplied by the powers of
+// two that the subnormal dequantisation of int4 / int8 codes expects, and the
+// chunk sums the epilogues need: for int4 the sum of x over each 32-wide group
+// (8 consecutive threads hold one group), for int8 128 times the sum over each
+// 16-wide chunk (4 threads), both times 2^-64.
 __device__ __forceinline__ void stage_store(const Smem& S, const Cons& cs, int dt, int U, int k4, bool ok, float4 a) {
   const int g = k4 / U, u = k4 % U;
-  if (ok) reinterpret_cast<float4*>(S.xs)[g * U + (u ^ swz(g, U))] = a;
-  if (dt == DT_INT4) {
+  const float4 m = dq_mult(dt, u);
+  if (ok)
+    reinterpret_cast<float4*>(S.xs)[g * U + (u ^ swz(g, U))] = make_float4(a.x * m.x, a.y * m.y, a.z * m.z, a.w * m.w);
+  if (dt != DT_BF16) {
     float sg = a.x + a.y + a.z + a.w;
     sg += __shfl_xor_sync(0xffffffffu, sg, 1);
     sg += __shfl_xor_sync(0xffffffffu, sg, 2);
-    sg += __shfl_xor_sync(0xffffffffu, sg, 4);
-    if (ok && (cs.lane & 7) == 0) S.xsum[g] = sg;
+    if (dt == DT_INT4) sg += __shfl_xor_sync(0xffffffffu, sg, 4);
+    if (ok && (cs.lane & (U - 1)) == 0) S.xsum[g] = sg * (dt == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
   }
 }
 
@@ -603,54 +640,41 @@ __device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& c
 // ------------------------------------------------------ GEMV compute -----
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-__device__ __forceinline__ uint32_t word_of(const uint4& c, int j) {
-  return j == 0 ? c.x : j == 1 ? c.y : j == 2 ? c.z : c.w;
-}
+__device__ __forceinline__ float2 bits2(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
 
-// The dequantising dot products work on one 32-bit word of a 16-byte chunk at
-// a time (j = 0..3, a run-time loop so that the body stays small), for all 16
-// rows of the slot at once so that their accumulator chains overlap.
-//
-// int4: view i of a word (rotated right by 8i) carries code k = 8j+2i in bits
-// 15..18 and k = 8j+2i+1 in bits 19..22.  OR-ing the exponent of 1.0f turns
-// them into 1 + q/256 and 1 + q/16 exactly (one LOP3 each); subtracting 1
-// (exact, packed) leaves q/256 and q/16, which multiply the fp32 input pair
-// with one packed FMA.  acc[r] = (sum_even q x / 256, sum_odd q x / 16).
-__device__ __forceinline__ void word_int4(const uint32_t* wr, const float2* x2, float2* acc) {
-  const float2 m1 = make_float2(-1.0f, -1.0f);
+// One 16-byte chunk of one row against the chunk's staged inputs x (natural
+// k order, as pairs), accumulated into acc.
+// int4: word j holds codes 8j..8j+7 in nibbles 0..7.
+__device__ __forceinline__ float2 chunk_int4(const uint4 q, const float2* x, float2 acc) {
+  const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int r = 0; r < HROWS; ++r) {
-      const uint32_t v = i ? __funnelshift_r(wr[r], wr[r], 8 * i) : wr[r];
-      const float lo = __uint_as_float((v & 0x00078000u) | 0x3F800000u);
-      const float hi = __uint_as_float((v & 0x00780000u) | 0x3F800000u);
-      acc[r] = ffma2(__fadd2_rn(make_float2(lo, hi), m1), x2[i], acc[r]);
-    }
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = wv[j], h = w >> 8;
+    acc = ffma2(bits2(w & 0x0000000Fu, w & 0x000000F0u), x[4 * j + 0], acc);
+    acc = ffma2(bits2(w & 0x00000F00u, w & 0x0000F000u), x[4 * j + 1], acc);
+    acc = ffma2(bits2(w & 0x000F0000u, w & 0x00F00000u), x[4 * j + 2], acc);
+    acc = ffma2(bits2(h & 0x000F0000u, h & 0x00F00000u), x[4 * j + 3], acc);
   }
+  return acc;
 }
-// int8: view i carries code k = 4j+i in bits 15..22; XOR with 0x3FC00000 sets
-// the exponent of 1.0f and flips the sign bit, giving 1 + (q + 128)/256;
-// subtracting 1.5 (exact) leaves q/256.  acc[r] = q x / 256 by parity of k.
-__device__ __forceinline__ void word_int8(const uint32_t* wr, const float2* x2, float2* acc) {
-  const float2 off = make_float2(-1.5f, -1.5f);
+// int8: word j holds codes 4j..4j+3, one byte each (two's complement; the XOR
+// with 0x80 makes the offset code c + 128).
+__device__ __forceinline__ float2 chunk_int8(const uint4 q, const float2* x, float2 acc) {
+  const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int r = 0; r < HROWS; ++r) {
-    float f[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t v = i ? __funnelshift_r(wr[r], wr[r], 8 * i) : wr[r];
-      f[i] = __uint_as_float((v & 0x007F8000u) ^ 0x3FC00000u);
-    }
-    acc[r] = ffma2(__fadd2_rn(make_float2(f[0], f[1]), off), x2[0], acc[r]);
-    acc[r] = ffma2(__fadd2_rn(make_float2(f[2], f[3]), off), x2[1], acc[r]);
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = wv[j] ^ 0x80808080u, h = w >> 8;
+    acc = ffma2(bits2(w & 0x000000FFu, w & 0x0000FF00u), x[2 * j + 0], acc);
+    acc = ffma2(bits2(w & 0x00FF0000u, h & 0x00FF0000u), x[2 * j + 1], acc);
   }
+  return acc;
 }
-// bf16: a word holds two weights, k = 2j and 2j+1.
-__device__ __forceinline__ void word_bf16(const uint32_t* wr, const float2* x2, float2* acc) {
+// bf16: word j holds weights 2j (low half) and 2j+1 (high half).
+__device__ __forceinline__ float2 chunk_bf16(const uint4 q, const float2* x, float2 acc) {
+  const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int r = 0; r < HROWS; ++r)
-    acc[r] = ffma2(make_float2(__uint_as_float(wr[r] << 16), __uint_as_float(wr[r] & 0xFFFF0000u)), x2[0], acc[r]);
+  for (int j = 0; j < 4; ++j) acc = ffma2(bits2(wv[j] << 16, wv[j] & 0xFFFF0000u), x[j], acc);
+  return acc;
 }
 
 // Sums each of 16 per-lane values over the 32 lanes; afterwards lane l holds
@@ -768,63 +792,57 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
       const int bfirst = (w - own0 + NCW) % NCW;                               // this warp's first K-block
       const int ncontrib = nb < NCW ? nb : NCW;
       if (bfirst < nb) {
+        // int4: v[r] collects s * (codes . x) + z * (sum of x) per group, x 2^-64;
+        // int8 / bf16: acc[r] collects the row's dot product over the blocks
         float v[HROWS];
+        float2 acc[HROWS];
 #pragma unroll
-        for (int r = 0; r < HROWS; ++r) v[r] = 0.0f;
+        for (int r = 0; r < HROWS; ++r) {
+          v[r] = 0.0f;
+          acc[r] = make_float2(0.f, 0.f);
+        }
+        float bias = 0.0f;  // int8: 128 * sum x * 2^-64 over this lane's chunks
         for (int b = bfirst; b < nb; b += NCW) {
           const uint32_t it = cs.it + j + (uint32_t)b;
           const uint8_t* base;
           if (!slot_acquire(S, cs, it, P.err, base)) return false;
           const int Lb = min(KBLK, C - b * KBLK);
-          // lanes past the block width (and rows past the tile) read in-bounds
-          // stale bytes of the slot and are masked out
-          const bool lane_ok = lane < Lb;
-          const int g = b * KBLK + lane;
-          const int sw = swz(g, U);
-          float2 acc[HROWS];
+          // lane l takes chunk l of every row of the slot; rows past the tile
+          // read in-bounds stale bytes of the slot and are discarded later
+          if (lane < Lb) {
+            const int g = b * KBLK + lane;
+            const int sw = swz(g, U);
+            float2 xr[E / 2];
 #pragma unroll
-          for (int r = 0; r < HROWS; ++r) acc[r] = make_float2(0.f, 0.f);
-          const uint32_t* wbase = reinterpret_cast<const uint32_t*>(base) + lane * 4;
-#pragma unroll 1
-          for (int jw = 0; jw < 4; ++jw) {
-            // inputs of word jw: int4 x[8jw..8jw+7], int8 x[4jw..4jw+3], bf16 x[2jw, 2jw+1]
-            float2 x2[4];
+            for (int u = 0; u < U; ++u) {
+              const float4 t = xs4[g * U + (u ^ sw)];
+              xr[2 * u] = make_float2(t.x, t.y);
+              xr[2 * u + 1] = make_float2(t.z, t.w);
+            }
+            const uint4* wq = reinterpret_cast<const uint4*>(base) + lane;
             if (DT == DT_INT4) {
-              const float4 xa = xs4[g * U + ((2 * jw) ^ sw)], xb = xs4[g * U + ((2 * jw + 1) ^ sw)];
-              x2[0] = make_float2(xa.x, xa.y);
-              x2[1] = make_float2(xa.z, xa.w);
-              x2[2] = make_float2(xb.x, xb.y);
-              x2[3] = make_float2(xb.z, xb.w);
+              const float xg = S.xsum[g];
+              const uint32_t* szp = reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF) + lane;
+#pragma unroll
+              for (int r = 0; r < HROWS; ++r) {
+                const float2 a = chunk_int4(wq[r * Lb], xr, make_float2(0.f, 0.f));
+                const uint32_t sz = szp[r * Lb];
+                v[r] = fmaf(__uint_as_float(sz << 16), a.x + a.y, fmaf(__uint_as_float(sz & 0xFFFF0000u), xg, v[r]));
+              }
             } else if (DT == DT_INT8) {
-              const float4 xa = xs4[g * U + (jw ^ sw)];
-              x2[0] = make_float2(xa.x, xa.y);
-              x2[1] = make_float2(xa.z, xa.w);
+              bias += S.xsum[g];
+#pragma unroll
+              for (int r = 0; r < HROWS; ++r) acc[r] = chunk_int8(wq[r * Lb], xr, acc[r]);
             } else {
-              const float4 xa = xs4[g * U + ((jw >> 1) ^ sw)];
-              x2[0] = (jw & 1) ? make_float2(xa.z, xa.w) : make_float2(xa.x, xa.y);
+#pragma unroll
+              for (int r = 0; r < HROWS; ++r) acc[r] = chunk_bf16(wq[r * Lb], xr, acc[r]);
             }
-            uint32_t wr[HROWS];
-#pragma unroll
-            for (int r = 0; r < HROWS; ++r) wr[r] = wbase[r * Lb * 4 + jw];
-            if (DT == DT_INT4) word_int4(wr, x2, acc);
-            else if (DT == DT_INT8) word_int8(wr, x2, acc);
-            else word_bf16(wr, x2, acc);
-          }
-          if (DT == DT_INT4) {
-            const float xg = S.xsum[g];
-            const uint32_t* szp = reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF) + lane;
-#pragma unroll
-            for (int r = 0; r < HROWS; ++r) {
-              const uint32_t sz = szp[r * Lb];
-              const float Sq = fmaf(256.0f, acc[r].x, 16.0f * acc[r].y);
-              const float contrib = fmaf(__uint_as_float(sz << 16), Sq, __uint_as_float(sz & 0xFFFF0000u) * xg);
-              v[r] += lane_ok ? contrib : 0.0f;
-            }
-          } else {
-#pragma unroll
-            for (int r = 0; r < HROWS; ++r) v[r] += lane_ok ? acc[r].x + acc[r].y : 0.0f;
           }
           slot_release(S, cs, it);
+        }
+        if (DT != DT_INT4) {
+#pragma unroll
+          for (int r = 0; r < HROWS; ++r) v[r] = (acc[r].x + acc[r].y) - bias;
         }
         // deposit this warp's 16 row sums, then the last contributor combines
         const float y = warp_rows16(v, lane);
@@ -849,7 +867,8 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
           }
           if (lane == 0) S.tbc[buf] = 0;
           const int r = r0 + lane, n = lt * TR + r;
-          if (DT == DT_INT8 && lane < HROWS && r < Rt) tot *= 256.0f * bf2f(s8[n]);
+          if (DT == DT_INT4) tot *= DQ_UP;
+          if (DT == DT_INT8 && lane < HROWS && r < Rt) tot *= DQ_UP * bf2f(s8[n]);
           const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
           if (lane < HROWS && r < Rt) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, am);
         }
@@ -1083,7 +1102,7 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
 // deterministic); the group's epilogues then run per (row, m).
 struct VS {
   float* xk;    // [MAX_M][KBLK chunks][E] inputs of the current K-block
-  float* xgk;   // [MAX_M][KBLK] their sums per 32-wide group (int4)
+  float* xgk;   // [MAX_M][KBLK] chunk sums of the inputs, as S.xsum
   float* acc;   // [VTG * TR][MAX_M] row sums of the tile group
   float* rfac;  // [MAX_M] RMSNorm factors
 };
@@ -1272,13 +1291,16 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
         const bool ok = m < M && l < Lb;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
         if (ok) a = vin4(ph, P, V, m, e, (b * KBLK + l) * U + u);
-        if (ok) reinterpret_cast<float4*>(V.xk)[m * per_m + l * U + (u ^ swz(l, U))] = a;
-        if (DT == DT_INT4) {
+        const float4 mu = dq_mult(DT, u);
+        if (ok)
+          reinterpret_cast<float4*>(V.xk)[m * per_m + l * U + (u ^ swz(l, U))] =
+              make_float4(a.x * mu.x, a.y * mu.y, a.z * mu.z, a.w * mu.w);
+        if (DT != DT_BF16) {  // chunk sums as in stage_store
           float sg = a.x + a.y + a.z + a.w;
           sg += __shfl_xor_sync(0xffffffffu, sg, 1);
           sg += __shfl_xor_sync(0xffffffffu, sg, 2);
-          sg += __shfl_xor_sync(0xffffffffu, sg, 4);
-          if (ok && (lane & 7) == 0) V.xgk[m * KBLK + l] = sg;
+          if (DT == DT_INT4) sg += __shfl_xor_sync(0xffffffffu, sg, 4);
+          if (ok && (lane & (U - 1)) == 0) V.xgk[m * KBLK + l] = sg * (DT == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
         }
       }
       if (!cta_sync(S, cs, P.err)) return false;
@@ -1330,25 +1352,18 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
               for (int r = 0; r < 4; ++r) {
                 const uint32_t wv = wbase[(rb + r) * Lb * 4 + jw];
                 float2 qv[WP];
-                if (DT == DT_INT4) {
-#pragma unroll
-                  for (int i2 = 0; i2 < 4; ++i2) {
-                    const uint32_t v = i2 ? __funnelshift_r(wv, wv, 8 * i2) : wv;
-                    qv[i2 % WP] = __fadd2_rn(make_float2(__uint_as_float((v & 0x00078000u) | 0x3F800000u),
-                                                         __uint_as_float((v & 0x00780000u) | 0x3F800000u)),
-                                             make_float2(-1.0f, -1.0f));
-                  }
-                } else if (DT == DT_INT8) {
-                  float f[4];
-#pragma unroll
-                  for (int i2 = 0; i2 < 4; ++i2) {
-                    const uint32_t v = i2 ? __funnelshift_r(wv, wv, 8 * i2) : wv;
-                    f[i2] = __uint_as_float((v & 0x007F8000u) ^ 0x3FC00000u);
-                  }
-                  qv[0] = __fadd2_rn(make_float2(f[0], f[1]), make_float2(-1.5f, -1.5f));
-                  qv[1 % WP] = __fadd2_rn(make_float2(f[2], f[3]), make_float2(-1.5f, -1.5f));
+                if (DT == DT_INT4) {  // the subnormal reading of chunk_int4
+                  const uint32_t hv = wv >> 8;
+                  qv[0] = bits2(wv & 0x0000000Fu, wv & 0x000000F0u);
+                  qv[1 % WP] = bits2(wv & 0x00000F00u, wv & 0x0000F000u);
+                  qv[2 % WP] = bits2(wv & 0x000F0000u, wv & 0x00F00000u);
+                  qv[3 % WP] = bits2(hv & 0x000F0000u, hv & 0x00F00000u);
+                } else if (DT == DT_INT8) {  // as chunk_int8
+                  const uint32_t w8 = wv ^ 0x80808080u, hv = w8 >> 8;
+                  qv[0] = bits2(w8 & 0x000000FFu, w8 & 0x0000FF00u);
+                  qv[1 % WP] = bits2(w8 & 0x00FF0000u, hv & 0x00FF0000u);
                 } else {
-                  qv[0] = make_float2(__uint_as_float(wv << 16), __uint_as_float(wv & 0xFFFF0000u));
+                  qv[0] = bits2(wv << 16, wv & 0xFFFF0000u);
                 }
 #pragma unroll
                 for (int m = 0; m < MAX_M; ++m)
@@ -1367,8 +1382,10 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
               for (int m = 0; m < MAX_M; ++m) {
                 float c;
                 if (DT == DT_INT4) {
-                  const float Sq = fmaf(256.0f, a[r][m].x, 16.0f * a[r][m].y);
-                  c = fmaf(__uint_as_float(sz << 16), Sq, __uint_as_float(sz & 0xFFFF0000u) * V.xgk[m * KBLK + lane]);
+                  c = fmaf(__uint_as_float(sz << 16), a[r][m].x + a[r][m].y,
+                           __uint_as_float(sz & 0xFFFF0000u) * V.xgk[m * KBLK + lane]);
+                } else if (DT == DT_INT8) {
+                  c = (a[r][m].x + a[r][m].y) - V.xgk[m * KBLK + lane];
                 } else {
                   c = a[r][m].x + a[r][m].y;
                 }
@@ -1405,9 +1422,12 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
         const int n = lt * TR + r + k;
         float y = V.acc[(gi * TR + r + k) * MAX_M + m];
         float yp = (r + (k ^ 1) < Rt) ? V.acc[(gi * TR + r + (k ^ 1)) * MAX_M + m] : 0.f;
-        if (DT == DT_INT8) {
-          y *= 256.0f * bf2f(s8[n]);
-          if (r + (k ^ 1) < Rt) yp *= 256.0f * bf2f(s8[n ^ 1]);
+        if (DT == DT_INT4) {
+          y *= DQ_UP;
+          yp *= DQ_UP;
+        } else if (DT == DT_INT8) {
+          y *= DQ_UP * bf2f(s8[n]);
+          if (r + (k ^ 1) < Rt) yp *= DQ_UP * bf2f(s8[n ^ 1]);
         }
         gemv_epilogue_m(ph, P, S, e, n, m, y, yp, pos, am);
       }
@@ -1483,7 +1503,8 @@ __device__ bool route_experts(const Phase& ph, const Params& P, const Smem& S, C
     float acc = 0.0f;
     for (int k4 = cs.lane; k4 < K4; k4 += 32) {
       const int g = k4 / U, u = k4 % U;
-      const float4 x = xs4[g * U + (u ^ swz(g, U))];
+      const float4 xm = xs4[g * U + (u ^ swz(g, U))], iv = dq_inv(ph.dtype, u);
+      const float4 x = make_float4(xm.x * iv.x, xm.y * iv.y, xm.z * iv.z, xm.w * iv.w);
       const float4 wv = bf4(wr[k4]);
       acc = fmaf(x.x, wv.x, fmaf(x.y, wv.y, fmaf(x.z, wv.z, fmaf(x.w, wv.w, acc))));
     }

@@ -58,8 +58,8 @@ constexpr int NSLOT = 14;
 constexpr int NTB = 16;                      // tile-half combine buffers
 constexpr int OFF_RING = 0;
 constexpr int OFF_X = OFF_RING + NSLOT * SLOT_BYTES;     // fp32 x, swizzled
-constexpr int OFF_XSUM = OFF_X + KMAX * 4;               // fp32 sum of x per 32-wide group
-constexpr int OFF_TB = OFF_XSUM + (KMAX / 32) * 4 + 256;  // [NTB][NCW][HROWS] partial row sums
+constexpr int OFF_XSUM = OFF_X + KMAX * 4;               // fp32 sums of x per chunk (int8) / group (int4)
+constexpr int OFF_TB = OFF_XSUM + (KMAX / 16) * 4 + 256;  // [NTB][NCW][HROWS] partial row sums
 constexpr int OFF_TBC = OFF_TB + NTB * NCW * HROWS * 4;  // [NTB] arrival counters
 constexpr int OFF_BAR = OFF_TBC + NTB * 4;               // mbarriers
 constexpr int OFF_MISC = OFF_BAR + 320;

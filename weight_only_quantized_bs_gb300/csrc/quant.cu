@@ -18,8 +18,6 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
 }
-__device__ __forceinline__ uint32_t rotl15(uint32_t v) { return __funnelshift_l(v, v, 15); }
-__device__ __forceinline__ uint32_t rotr15(uint32_t v) { return __funnelshift_r(v, v, 15); }
 
 struct ChunkAddr {
   long long code, sz;
@@ -59,7 +57,7 @@ __global__ void __launch_bounds__(256) k_quant_w8(const uint16_t* __restrict__ W
       uint32_t words[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint32_t nat = 0;
+        uint32_t word = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int k = 4 * j + i;
@@ -69,9 +67,9 @@ __global__ void __launch_bounds__(256) k_quant_w8(const uint16_t* __restrict__ W
             code = (int)rintf(bf2f(wb) / sv);
             code = max(-127, min(127, code));
           }
-          nat |= (uint32_t)(uint8_t)(int8_t)code << (8 * i);
+          word |= (uint32_t)(uint8_t)(int8_t)code << (8 * i);
         }
-        words[j] = rotl15(nat);
+        words[j] = word;
       }
       ChunkAddr a = chunk_addr(DT_INT8, N, C, n, c);
       *reinterpret_cast<uint4*>(P + a.code) = make_uint4(words[0], words[1], words[2], words[3]);
@@ -112,7 +110,7 @@ __global__ void __launch_bounds__(256) k_quant_w4g(const uint16_t* __restrict__ 
       uint32_t words[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint32_t nat = 0;
+        uint32_t word = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           int code = 0;
@@ -120,9 +118,9 @@ __global__ void __launch_bounds__(256) k_quant_w4g(const uint16_t* __restrict__ 
             code = (int)rintf((w[8 * j + i] - mn) / sv);
             code = max(0, min(15, code));
           }
-          nat |= (uint32_t)code << (4 * i);
+          word |= (uint32_t)code << (4 * i);
         }
-        words[j] = rotl15(nat);
+        words[j] = word;
       }
       ChunkAddr a = chunk_addr(DT_INT4, N, C, n, c);
       *reinterpret_cast<uint4*>(P + a.code) = make_uint4(words[0], words[1], words[2], words[3]);
@@ -155,14 +153,11 @@ __global__ void __launch_bounds__(256) k_unpack(int dt, const uint8_t* __restric
       if (dt == DT_BF16) {
         *reinterpret_cast<uint4*>((uint16_t*)Q + (size_t)n * K + c * 8) = v;
       } else if (dt == DT_INT8) {
-        uint32_t o[4];
-        for (int j = 0; j < 4; ++j) o[j] = rotr15(wv[j]);
-        *reinterpret_cast<uint4*>((uint8_t*)Q + (size_t)n * K + c * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>((uint8_t*)Q + (size_t)n * K + c * 16) = v;
       } else {
         uint8_t* q = (uint8_t*)Q + (size_t)n * K + c * 32;
         for (int j = 0; j < 4; ++j) {
-          const uint32_t nat = rotr15(wv[j]);
-          for (int i = 0; i < 8; ++i) q[8 * j + i] = (uint8_t)((nat >> (4 * i)) & 15u);
+          for (int i = 0; i < 8; ++i) q[8 * j + i] = (uint8_t)((wv[j] >> (4 * i)) & 15u);
         }
         const uint32_t sz = *reinterpret_cast<const uint32_t*>(P + a.sz);
         S[(size_t)n * C + c] = (uint16_t)sz;
