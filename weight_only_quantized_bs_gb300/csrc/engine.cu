@@ -31,6 +31,12 @@ __device__ int g_err_word;
 
 // ------------------------------------------------------------- PTX glue --
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+// asynchronous 16-byte global -> shared copy (completion: cp_async_wait_all)
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
@@ -90,11 +96,24 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
+// try_wait that may suspend the thread for up to 20 us; the hardware wakes it
+// as soon as the phase completes, so the hint adds no latency but keeps a
+// waiting warp from spinning on issue slots the compute warps need.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __noinline__ bool mbar_wait_slow(uint64_t* b, uint32_t parity, int* err, int code) {
   const uint64_t t0 = gtimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_test(b, parity)) return true;
-    if ((it & 31) == 0) {
+    if (mbar_test_sleep(b, parity)) return true;
+    if ((it & 3) == 0) {
       if (ld_relaxed(err)) return false;
       if (gtimer() - t0 > WAIT_NS) {
         atomicCAS(err, 0, code);
@@ -142,6 +161,7 @@ struct Smem {
   float* xsum;      // sum of x over each 32-wide group (int4 zero offsets)
   float* tb;        // [NTB][NCW][HROWS] partial row sums of half-tiles
   int* tbc;         // [NTB] arrival counters
+  int* tbg;         // [NTB] half-tile allowed to use the buffer next
   uint64_t* full;   // [NSLOT]
   uint64_t* empty;  // [NSLOT]
   uint64_t* cbar;   // consumer-warps barrier
@@ -149,6 +169,7 @@ struct Smem {
   int* bcast;       // [64] broadcast ints; [32..33] chosen experts, [34] phase they were chosen in,
                     // [48..55] verify: union of the rows' experts, [56] its size
   float* moew;      // [MAX_M][8] verify: weight of expert e for row m (0 if not chosen)
+  Phase* phb;       // [2] the consumers' copies of the current and next phase descriptor
 };
 
 __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
@@ -158,12 +179,14 @@ __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
   s.xsum = reinterpret_cast<float*>(base + OFF_XSUM);
   s.tb = reinterpret_cast<float*>(base + OFF_TB);
   s.tbc = reinterpret_cast<int*>(base + OFF_TBC);
+  s.tbg = s.tbc + NTB;
   s.full = reinterpret_cast<uint64_t*>(base + OFF_BAR);
   s.empty = s.full + NSLOT;
   s.cbar = s.empty + NSLOT;
   s.red = reinterpret_cast<float*>(base + OFF_MISC);
   s.bcast = reinterpret_cast<int*>(base + OFF_MISC + 256);
   s.moew = reinterpret_cast<float*>(base + OFF_MISC + 512);
+  s.phb = reinterpret_cast<Phase*>(base + OFF_PHB);
   return s;
 }
 
@@ -421,7 +444,7 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
   for (uint32_t k = 0; k < n; ++k) {
     const uint32_t i = pr.it - 1 - k, slot = i % NSLOT, use = i / NSLOT;
     const uint64_t t0 = gtimer();
-    while (!mbar_test(&S.full[slot], use & 1u)) {
+    while (!mbar_test_sleep(&S.full[slot], use & 1u)) {
       if (gtimer() - t0 > WAIT_NS) {
         atomicCAS(err, 0, ERR_DRAIN);
         break;
@@ -437,6 +460,7 @@ struct Cons {
   uint32_t useq;     // half-tiles seen so far (combine-buffer index)
   int warp, lane, ctid;
   uint32_t starved;  // slot waits that found the slot still in flight (warp 0)
+  float rnorm;       // RMSNorm factor of the staged input (1 if none)
 };
 
 // all consumer warps meet; false if the wait gave up
@@ -529,112 +553,77 @@ __device__ __forceinline__ void stage_store(const Smem& S, const Cons& cs, int d
 }
 
 // Stages the phase's input vector into shared memory as fp32.  Thread t
-// handles float4 number t + 256 j; every load of a batch is issued before any
-// is used, so a phase pays about one L2 round trip per batch.
+// handles float4 numbers t + 224 i; all of its loads are issued before any is
+// used, so staging costs about one L2 round trip.  For an RMSNorm input only
+// the gain is applied here: the factor 1/rms needs the whole vector, and as
+// the GEMV is linear it is applied to the outputs in the epilogue instead
+// (cs.rnorm, 1 for other inputs), which keeps the reduction off the path.
 __device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
-  const int K = ph.K, dt = ph.dtype, E = per_chunk(dt), U = E / 4;
-  const int K4 = K / 4, NT = NCW * 32;
-  const int nit = (K4 + NT - 1) / NT;
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (ph.xsrc == X_BF16) {
-    const uint2* xb = reinterpret_cast<const uint2*>(ph.xptr);
-    for (int j0 = 0; j0 < nit; j0 += 8) {
-      uint2 h[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int k4 = cs.ctid + (j0 + t) * NT;
-        h[t] = make_uint2(0u, 0u);
-        if (j0 + t < nit && k4 < K4) h[t] = __ldcg(xb + k4);
-      }
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-        if (j0 + t < nit) stage_store(S, cs, dt, U, cs.ctid + (j0 + t) * NT, cs.ctid + (j0 + t) * NT < K4, bf4(h[t]));
-    }
-    return cta_sync(S, cs, P.err);
-  }
-  if (ph.xsrc == X_F32) {
-    const float4* xf = reinterpret_cast<const float4*>(ph.xptr);
-    for (int j0 = 0; j0 < nit; j0 += 8) {
-      float4 a[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int k4 = cs.ctid + (j0 + t) * NT;
-        a[t] = zero;
-        if (j0 + t < nit && k4 < K4) a[t] = __ldcg(xf + k4);
-      }
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-        if (j0 + t < nit) stage_store(S, cs, dt, U, cs.ctid + (j0 + t) * NT, cs.ctid + (j0 + t) * NT < K4, a[t]);
-    }
-    return cta_sync(S, cs, P.err);
-  }
-  // RMSNorm of the fp32 residual (or of the embedding row for the first layer)
-  const float* res = ph.xsrc == X_NORM ? reinterpret_cast<const float*>(ph.xptr) : nullptr;
+  constexpr int NT = NCW * 32, MAXIT = (KMAX / 4 + NT - 1) / NT;
+  const int K = ph.K, dt = ph.dtype, U = per_chunk(dt) / 4, K4 = K / 4;
+  const bool norm = ph.xsrc == X_NORM || ph.xsrc == X_EMBED_NORM;
   const uint16_t* emb = ph.xsrc == X_EMBED_NORM ? P.embed + (size_t)(*P.token) * K : nullptr;
-  const uint2* gain = reinterpret_cast<const uint2*>(ph.gain);
-  float4 keep[4];
-  uint2 gk[4];
+  float4 a[MAXIT];
+  uint2 gk[MAXIT];
+  // one load loop per source, each load writing its own register, so that
+  // nothing waits for a load before the next is issued
+#pragma unroll
+  for (int t = 0; t < MAXIT; ++t) {
+    const int k4 = cs.ctid + t * NT;
+    gk[t] = make_uint2(0x3F803F80u, 0x3F803F80u);  // bf16 ones
+    if (norm && k4 < K4) gk[t] = reinterpret_cast<const uint2*>(ph.gain)[k4];
+  }
+  if (ph.xsrc == X_F32 || ph.xsrc == X_NORM) {
+    const float4* src = reinterpret_cast<const float4*>(ph.xptr);
+#pragma unroll
+    for (int t = 0; t < MAXIT; ++t) {
+      const int k4 = cs.ctid + t * NT;
+      a[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k4 < K4) a[t] = __ldcg(src + k4);
+    }
+  } else {
+    const uint2* src = emb ? reinterpret_cast<const uint2*>(emb) : reinterpret_cast<const uint2*>(ph.xptr);
+    uint2 h[MAXIT];
+#pragma unroll
+    for (int t = 0; t < MAXIT; ++t) {
+      const int k4 = cs.ctid + t * NT;
+      h[t] = make_uint2(0u, 0u);
+      if (k4 < K4) h[t] = __ldcg(src + k4);
+    }
+#pragma unroll
+    for (int t = 0; t < MAXIT; ++t) a[t] = bf4(h[t]);
+  }
+  // keep every load above the shared-memory stores below (the compiler
+  // cannot tell that they do not alias), so that all are in flight at once
+  asm volatile("" ::: "memory");
   float ss = 0.0f;
-  for (int j0 = 0; j0 < nit; j0 += 4) {
-    float4 a[4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int k4 = cs.ctid + (j0 + t) * NT;
-      a[t] = zero;
-      if (j0 + t < nit && k4 < K4) {
-        if (res) {
-          a[t] = __ldcg(reinterpret_cast<const float4*>(res) + k4);
-        } else {
-          a[t] = bf4(*reinterpret_cast<const uint2*>(emb + 4 * k4));
-          if (cta == 0) reinterpret_cast<float4*>(P.resid)[k4] = a[t];
-        }
-        if (j0 == 0) gk[t] = gain[k4];
+  for (int t = 0; t < MAXIT; ++t) {
+    const int k4 = cs.ctid + t * NT;
+    if (t * NT < K4) {  // warp-uniform: the chunk sums shuffle within the warp
+      if (norm) {
+        ss += a[t].x * a[t].x + a[t].y * a[t].y + a[t].z * a[t].z + a[t].w * a[t].w;
+        if (emb && cta == 0 && k4 < K4) reinterpret_cast<float4*>(P.resid)[k4] = a[t];
+        const float4 g = bf4(gk[t]);
+        a[t] = make_float4(a[t].x * g.x, a[t].y * g.y, a[t].z * g.z, a[t].w * g.w);
       }
-    }
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      ss += a[t].x * a[t].x + a[t].y * a[t].y + a[t].z * a[t].z + a[t].w * a[t].w;
-      if (j0 == 0) keep[t] = a[t];
+      stage_store(S, cs, dt, U, k4, k4 < K4, a[t]);
     }
   }
+  if (norm) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (cs.lane == 0) S.red[cs.warp] = ss;
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (cs.lane == 0) S.red[cs.warp] = ss;
+  }
   if (!cta_sync(S, cs, P.err)) return false;
-  float tot = 0.0f;
+  cs.rnorm = 1.0f;
+  if (norm) {
+    float tot = 0.0f;
 #pragma unroll
-  for (int w = 0; w < NCW; ++w) tot += S.red[w];
-  const float r = 1.0f / sqrtf(tot / (float)K + ph.eps);
-  for (int j0 = 0; j0 < nit; j0 += 4) {
-    float4 a[4];
-    uint2 gg[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int k4 = cs.ctid + (j0 + t) * NT;
-      a[t] = zero;
-      gg[t] = make_uint2(0u, 0u);
-      if (j0 + t < nit && k4 < K4) {
-        if (j0 == 0) {
-          a[t] = keep[t];
-          gg[t] = gk[t];
-        } else {
-          a[t] = res ? __ldcg(reinterpret_cast<const float4*>(res) + k4)
-                     : bf4(*reinterpret_cast<const uint2*>(emb + 4 * k4));
-          gg[t] = gain[k4];
-        }
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      if (j0 + t < nit) {
-        const int k4 = cs.ctid + (j0 + t) * NT;
-        const float4 g = bf4(gg[t]);
-        const float4 v = make_float4(a[t].x * r * g.x, a[t].y * r * g.y, a[t].z * r * g.z, a[t].w * r * g.w);
-        stage_store(S, cs, dt, U, k4, k4 < K4, v);
-      }
-    }
+    for (int w = 0; w < NCW; ++w) tot += S.red[w];
+    cs.rnorm = 1.0f / sqrtf(tot / (float)K + ph.eps);
   }
-  return cta_sync(S, cs, P.err);
+  return true;
 }
 
 // ------------------------------------------------------ GEMV compute -----
@@ -642,39 +631,28 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return _
 
 __device__ __forceinline__ float2 bits2(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
 
-// One 16-byte chunk of one row against the chunk's staged inputs x (natural
+// One 32-bit word of codes of one row against its staged inputs x (natural
 // k order, as pairs), accumulated into acc.
-// int4: word j holds codes 8j..8j+7 in nibbles 0..7.
-__device__ __forceinline__ float2 chunk_int4(const uint4 q, const float2* x, float2 acc) {
-  const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t w = wv[j], h = w >> 8;
-    acc = ffma2(bits2(w & 0x0000000Fu, w & 0x000000F0u), x[4 * j + 0], acc);
-    acc = ffma2(bits2(w & 0x00000F00u, w & 0x0000F000u), x[4 * j + 1], acc);
-    acc = ffma2(bits2(w & 0x000F0000u, w & 0x00F00000u), x[4 * j + 2], acc);
-    acc = ffma2(bits2(h & 0x000F0000u, h & 0x00F00000u), x[4 * j + 3], acc);
-  }
+// int4: the word holds 8 consecutive codes in nibbles 0..7.
+__device__ __forceinline__ float2 word_int4(const uint32_t w, const float2* x, float2 acc) {
+  const uint32_t h = w >> 8;
+  acc = ffma2(bits2(w & 0x0000000Fu, w & 0x000000F0u), x[0], acc);
+  acc = ffma2(bits2(w & 0x00000F00u, w & 0x0000F000u), x[1], acc);
+  acc = ffma2(bits2(w & 0x000F0000u, w & 0x00F00000u), x[2], acc);
+  acc = ffma2(bits2(h & 0x000F0000u, h & 0x00F00000u), x[3], acc);
   return acc;
 }
-// int8: word j holds codes 4j..4j+3, one byte each (two's complement; the XOR
-// with 0x80 makes the offset code c + 128).
-__device__ __forceinline__ float2 chunk_int8(const uint4 q, const float2* x, float2 acc) {
-  const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t w = wv[j] ^ 0x80808080u, h = w >> 8;
-    acc = ffma2(bits2(w & 0x000000FFu, w & 0x0000FF00u), x[2 * j + 0], acc);
-    acc = ffma2(bits2(w & 0x00FF0000u, h & 0x00FF0000u), x[2 * j + 1], acc);
-  }
+// int8: 4 consecutive codes, one byte each (two's complement; the XOR with
+// 0x80 makes the offset code c + 128).
+__device__ __forceinline__ float2 word_int8(const uint32_t wq, const float2* x, float2 acc) {
+  const uint32_t w = wq ^ 0x80808080u, h = w >> 8;
+  acc = ffma2(bits2(w & 0x000000FFu, w & 0x0000FF00u), x[0], acc);
+  acc = ffma2(bits2(w & 0x00FF0000u, h & 0x00FF0000u), x[1], acc);
   return acc;
 }
-// bf16: word j holds weights 2j (low half) and 2j+1 (high half).
-__device__ __forceinline__ float2 chunk_bf16(const uint4 q, const float2* x, float2 acc) {
-  const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc = ffma2(bits2(wv[j] << 16, wv[j] & 0xFFFF0000u), x[j], acc);
-  return acc;
+// bf16: 2 consecutive weights (low half first).
+__device__ __forceinline__ float2 word_bf16(const uint32_t w, const float2* x, float2 acc) {
+  return ffma2(bits2(w << 16, w & 0xFFFF0000u), x[0], acc);
 }
 
 // Sums each of 16 per-lane values over the 32 lanes; afterwards lane l holds
@@ -707,7 +685,7 @@ __device__ __forceinline__ void amax_merge(ArgMax& a, float v, int i) {
 // Epilogue of one output row n (value y); lanes 0..15 call it together, each
 // with its own row of the half-tile; yp is the value of row n ^ 1.
 __device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, const Smem& S, int seg, int n, float y,
-                                              float yp, int pos, ArgMax& am) {
+                                              float yp, int pos, float2 rp, ArgMax& am) {
   switch (ph.epi) {
     case EPI_STORE_BF16:
       reinterpret_cast<uint16_t*>(ph.out)[n] = f2bf(y);
@@ -730,8 +708,7 @@ __device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, 
           const bool isq = n < ph.q_rows;
           const int nn = isq ? n : n - ph.q_rows;
           const int d = nn % hd;
-          const float2 cs = P.rope[(size_t)pos * (hd / 2) + d / 2];
-          const float o0 = y * cs.x - yp * cs.y, o1 = y * cs.y + yp * cs.x;
+          const float o0 = y * rp.x - yp * rp.y, o1 = y * rp.y + yp * rp.x;  // (cos, sin) of the pair
           if (isq) {
             float* q = reinterpret_cast<float*>(ph.qbuf) + n;
             q[0] = o0;
@@ -763,6 +740,86 @@ __device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, 
   }
 }
 
+// The work of one lane on one slot: its chunk (number g of the row) of
+// every row of the slot.  LBC is the slot's width in chunks when known at
+// compile time (full K-blocks: row offsets become immediates), else 0.
+template <int DT, int LBC>
+__device__ __forceinline__ void slot_rows(const uint8_t* base, int Lb, int lane, int g, const float4* xs4, const Smem& S,
+                                          float* v, float2* acc, float& bias) {
+  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
+  constexpr int U = E / 4;
+  const int L = LBC ? LBC : Lb;
+  // The four words of the chunk go by in a run-time loop (a small loop body
+  // stays in the instruction cache); in step jw lane l reads word
+  // (jw + l / 8) % 4, so that the 32 lanes' 4-byte loads hit 32 banks.
+  const int sw = swz(g, U);
+  const uint32_t* wrow = reinterpret_cast<const uint32_t*>(base) + lane * 4;
+  float2 a[HROWS];  // int4: this chunk's sums; int8 / bf16: running sums
+#pragma unroll
+  for (int r = 0; r < HROWS; ++r) a[r] = DT == DT_INT4 ? make_float2(0.f, 0.f) : acc[r];
+#pragma unroll 1
+  for (int jw = 0; jw < 4; ++jw) {
+    const int ws = (jw + (lane >> 3)) & 3;
+    float2 xr[4];
+    if (DT == DT_INT4) {
+      const float4 xa = xs4[g * U + ((2 * ws) ^ sw)], xb = xs4[g * U + ((2 * ws + 1) ^ sw)];
+      xr[0] = make_float2(xa.x, xa.y);
+      xr[1] = make_float2(xa.z, xa.w);
+      xr[2] = make_float2(xb.x, xb.y);
+      xr[3] = make_float2(xb.z, xb.w);
+    } else if (DT == DT_INT8) {
+      const float4 xa = xs4[g * U + (ws ^ sw)];
+      xr[0] = make_float2(xa.x, xa.y);
+      xr[1] = make_float2(xa.z, xa.w);
+    } else {
+      const float4 xa = xs4[g * U + ((ws >> 1) ^ sw)];
+      xr[0] = (ws & 1) ? make_float2(xa.z, xa.w) : make_float2(xa.x, xa.y);
+    }
+#pragma unroll
+    for (int r = 0; r < HROWS; ++r) {
+      const uint32_t wv = wrow[r * L * 4 + ws];
+      if (DT == DT_INT4) a[r] = word_int4(wv, xr, a[r]);
+      else if (DT == DT_INT8) a[r] = word_int8(wv, xr, a[r]);
+      else a[r] = word_bf16(wv, xr, a[r]);
+    }
+  }
+  if (DT == DT_INT4) {
+    const float xg = S.xsum[g];
+    const uint32_t* szp = reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF) + lane;
+#pragma unroll
+    for (int r = 0; r < HROWS; ++r) {
+      const uint32_t sz = szp[r * L];
+      v[r] = fmaf(__uint_as_float(sz << 16), a[r].x + a[r].y, fmaf(__uint_as_float(sz & 0xFFFF0000u), xg, v[r]));
+    }
+  } else {
+    if (DT == DT_INT8) bias += S.xsum[g];
+#pragma unroll
+    for (int r = 0; r < HROWS; ++r) acc[r] = a[r];
+  }
+}
+
+// Waits until combine buffer buf may take half-tile cs.useq (the last
+// combiner of half-tile useq - NTB hands it on).  Bounded.
+__device__ __forceinline__ bool tb_claim(const Smem& S, const Cons& cs, int buf, int* err) {
+  int ok = 1;
+  if (cs.lane == 0) {
+    volatile int* g = S.tbg + buf;
+    if (*g != (int)cs.useq) {
+      const uint64_t t0 = gtimer();
+      while (*g != (int)cs.useq) {
+        __nanosleep(32);
+        if (gtimer() - t0 > WAIT_NS) {
+          atomicCAS(err, 0, ERR_WAIT_COMBINE);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence_block();
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // One GEMV phase for this CTA.  Slot X of the stream (in producer order)
 // belongs to warp X % NCW.  A warp accumulates its K-blocks of a half-tile in
 // registers (16 rows per lane), reduces them over the lanes, and deposits the
@@ -778,6 +835,7 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
   const int tps = (Ns + TR - 1) / TR, ntiles = nseg * tps;
   const int lane = cs.lane, w = cs.warp;
   const float4* xs4 = reinterpret_cast<const float4*>(S.xs);
+  const float fac = cs.rnorm * (DT == DT_BF16 ? 1.0f : DQ_UP);
   uint32_t j = 0;  // slot index within the phase
   for (int t = first_unit(cta, ph.rot, G); t < ntiles; t += G) {
     const int seg = t / tps, lt = t % tps;
@@ -792,6 +850,20 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
       const int bfirst = (w - own0 + NCW) % NCW;                               // this warp's first K-block
       const int ncontrib = nb < NCW ? nb : NCW;
       if (bfirst < nb) {
+        // the epilogue's own inputs, fetched now so that their latency is
+        // hidden behind the K-blocks: lane r < 16 for row r0 + r
+        float pf = fac;  // output factor: RMSNorm, 2^64, int8 row scale
+        float2 rp = make_float2(1.f, 0.f);  // RoPE (cos, sin) of the row pair
+        {
+          const int n = lt * TR + r0 + lane;
+          if (lane < HROWS && r0 + lane < Rt) {
+            if (DT == DT_INT8) pf *= bf2f(s8[n]);
+            if (ph.epi == EPI_QKV && n < ph.q_rows + ph.kv_rows) {
+              const int nn = n < ph.q_rows ? n : n - ph.q_rows;
+              rp = P.rope[(size_t)pos * (ph.hd / 2) + (nn % ph.hd) / 2];
+            }
+          }
+        }
         // int4: v[r] collects s * (codes . x) + z * (sum of x) per group, x 2^-64;
         // int8 / bf16: acc[r] collects the row's dot product over the blocks
         float v[HROWS];
@@ -807,36 +879,11 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
           const uint8_t* base;
           if (!slot_acquire(S, cs, it, P.err, base)) return false;
           const int Lb = min(KBLK, C - b * KBLK);
-          // lane l takes chunk l of every row of the slot; rows past the tile
-          // read in-bounds stale bytes of the slot and are discarded later
+          // lane l takes chunk l of every row of the slot (rows past the
+          // tile read in-bounds stale bytes of the slot and are discarded)
           if (lane < Lb) {
-            const int g = b * KBLK + lane;
-            const int sw = swz(g, U);
-            float2 xr[E / 2];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const float4 t = xs4[g * U + (u ^ sw)];
-              xr[2 * u] = make_float2(t.x, t.y);
-              xr[2 * u + 1] = make_float2(t.z, t.w);
-            }
-            const uint4* wq = reinterpret_cast<const uint4*>(base) + lane;
-            if (DT == DT_INT4) {
-              const float xg = S.xsum[g];
-              const uint32_t* szp = reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF) + lane;
-#pragma unroll
-              for (int r = 0; r < HROWS; ++r) {
-                const float2 a = chunk_int4(wq[r * Lb], xr, make_float2(0.f, 0.f));
-                const uint32_t sz = szp[r * Lb];
-                v[r] = fmaf(__uint_as_float(sz << 16), a.x + a.y, fmaf(__uint_as_float(sz & 0xFFFF0000u), xg, v[r]));
-              }
-            } else if (DT == DT_INT8) {
-              bias += S.xsum[g];
-#pragma unroll
-              for (int r = 0; r < HROWS; ++r) acc[r] = chunk_int8(wq[r * Lb], xr, acc[r]);
-            } else {
-#pragma unroll
-              for (int r = 0; r < HROWS; ++r) acc[r] = chunk_bf16(wq[r * Lb], xr, acc[r]);
-            }
+            if (Lb == KBLK) slot_rows<DT, KBLK>(base, Lb, lane, b * KBLK + lane, xs4, S, v, acc, bias);
+            else slot_rows<DT, 0>(base, Lb, lane, b * KBLK + lane, xs4, S, v, acc, bias);
           }
           slot_release(S, cs, it);
         }
@@ -848,6 +895,9 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
         const float y = warp_rows16(v, lane);
         const int buf = (int)(cs.useq % NTB);
         float* tb = S.tb + (size_t)buf * NCW * HROWS;
+        // the buffer's previous half-tile has been combined (bounded wait;
+        // in practice it was long ago)
+        if (!tb_claim(S, cs, buf, P.err)) return false;
         if ((lane & 1) == 0) tb[w * HROWS + (lane >> 1)] = y;
         __syncwarp();
         int last = 0;
@@ -865,12 +915,16 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
               if (bw < nb) tot += tb[ww * HROWS + lane];
             }
           }
-          if (lane == 0) S.tbc[buf] = 0;
+          __syncwarp();
+          if (lane == 0) {
+            S.tbc[buf] = 0;
+            __threadfence_block();
+            *reinterpret_cast<volatile int*>(S.tbg + buf) = (int)(cs.useq + NTB);  // hand the buffer on
+          }
           const int r = r0 + lane, n = lt * TR + r;
-          if (DT == DT_INT4) tot *= DQ_UP;
-          if (DT == DT_INT8 && lane < HROWS && r < Rt) tot *= DQ_UP * bf2f(s8[n]);
+          tot *= pf;
           const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
-          if (lane < HROWS && r < Rt) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, am);
+          if (lane < HROWS && r < Rt) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, rp, am);
         }
       }
       j += (uint32_t)nb;
@@ -1323,7 +1377,8 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
 #pragma unroll
               for (int m = 0; m < MAX_M; ++m) a[r][m] = make_float2(0.f, 0.f);
 #pragma unroll 1
-            for (int jw = 0; jw < 4; ++jw) {
+            for (int jw0 = 0; jw0 < 4; ++jw0) {
+              const int jw = (jw0 + (lane >> 3)) & 3;  // per-lane word order: conflict-free loads
               float2 xp[MAX_M][WP];
 #pragma unroll
               for (int m = 0; m < MAX_M; ++m) {
@@ -1352,13 +1407,13 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
               for (int r = 0; r < 4; ++r) {
                 const uint32_t wv = wbase[(rb + r) * Lb * 4 + jw];
                 float2 qv[WP];
-                if (DT == DT_INT4) {  // the subnormal reading of chunk_int4
+                if (DT == DT_INT4) {  // the subnormal reading of word_int4
                   const uint32_t hv = wv >> 8;
                   qv[0] = bits2(wv & 0x0000000Fu, wv & 0x000000F0u);
                   qv[1 % WP] = bits2(wv & 0x00000F00u, wv & 0x0000F000u);
                   qv[2 % WP] = bits2(wv & 0x000F0000u, wv & 0x00F00000u);
                   qv[3 % WP] = bits2(hv & 0x000F0000u, hv & 0x00F00000u);
-                } else if (DT == DT_INT8) {  // as chunk_int8
+                } else if (DT == DT_INT8) {  // as word_int8
                   const uint32_t w8 = wv ^ 0x80808080u, hv = w8 >> 8;
                   qv[0] = bits2(w8 & 0x000000FFu, w8 & 0x0000FF00u);
                   qv[1 % WP] = bits2(w8 & 0x00FF0000u, hv & 0x00FF0000u);
@@ -1510,7 +1565,7 @@ __device__ bool route_experts(const Phase& ph, const Params& P, const Smem& S, C
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (cs.lane == 0) S.red[32 + e] = acc;
+    if (cs.lane == 0) S.red[32 + e] = acc * cs.rnorm;
   }
   if (!cta_sync(S, cs, P.err)) return false;
   if (cs.ctid == 0) {
@@ -1577,7 +1632,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     mbar_init(S.cbar, NCW * 32);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (tid < NTB) S.tbc[tid] = 0;
+  if (tid < NTB) {
+    S.tbc[tid] = 0;
+    S.tbg[tid] = tid;
+  }
   if (tid == 0) S.bcast[34] = 0;
   __syncthreads();
   const int pos = P.d_pos ? *P.d_pos : P.pos_const;
@@ -1614,6 +1672,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   cs.lane = lane;
   cs.ctid = tid;
   cs.starved = 0;
+  cs.rnorm = 1.0f;
   const int G = P.nctas;
   ArgMax am = {-INFINITY, 0x7fffffff};
   ArgMax amv[MAX_M];
@@ -1621,8 +1680,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   for (int m = 0; m < MAX_M; ++m) amv[m] = am;
   bool any_logits = false;
 
+  // The consumers read phase descriptors from shared memory: the copy of
+  // phase pi + 1 is requested at the start of phase pi (16 threads, 16 bytes
+  // each) and completes before that phase's closing CTA barrier, so its L2
+  // latency never sits on a phase's critical path.
+  constexpr int PH16 = (int)(sizeof(Phase) / 16);
+  if (P.prog) {
+    if (tid < PH16) {
+      cp_async16(reinterpret_cast<uint4*>(S.phb) + tid, reinterpret_cast<const uint4*>(P.prog) + tid);
+      cp_async_wait_all();
+    }
+    if (!cta_sync(S, cs, P.err)) return;
+  }
   for (int pi = 0; pi < P.nphases; ++pi) {
-    const Phase& ph = phase_at(P, pi);
+    const Phase& ph = P.prog ? S.phb[pi & 1] : P.single;
+    if (P.prog && pi + 1 < P.nphases && tid < PH16)
+      cp_async16(reinterpret_cast<uint4*>(S.phb + ((pi + 1) & 1)) + tid,
+                 reinterpret_cast<const uint4*>(P.prog + pi + 1) + tid);
     unsigned long long* tr = (P.trace && tid == 0) ? P.trace + ((size_t)pi * G + cta) * TRACE_W : nullptr;
     if (tr) tr[0] = gtimer();
     if (ph.wait_bar >= 0) {
@@ -1669,6 +1743,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
       tr[6] = cs.starved;
     }
     cs.starved = 0;
+    if (tid < PH16) cp_async_wait_all();  // the next phase's descriptor has landed
     // every warp of this CTA has finished the phase (its global writes made)
     if (!cta_sync(S, cs, P.err)) return;
     if (ph.signal_bar >= 0 && tid == 0) grid_arrive(P.bars + ph.signal_bar);

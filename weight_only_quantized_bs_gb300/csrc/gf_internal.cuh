@@ -55,15 +55,20 @@ constexpr int SLOT_SZ_OFF = 8192;            // int4 scale words inside a slot
 // use of the entry a warp waits on is that warp's own, already consumed slot,
 // and the mbarrier phase parity it waits for is never ambiguous.
 constexpr int NSLOT = 14;
-constexpr int NTB = 16;                      // tile-half combine buffers
+// Half-tile combine buffers, used round-robin by half-tile number; a guard
+// word per buffer holds the number of the half-tile allowed to use it next.
+constexpr int NTB = 16;
 constexpr int OFF_RING = 0;
 constexpr int OFF_X = OFF_RING + NSLOT * SLOT_BYTES;     // fp32 x, swizzled
 constexpr int OFF_XSUM = OFF_X + KMAX * 4;               // fp32 sums of x per chunk (int8) / group (int4)
 constexpr int OFF_TB = OFF_XSUM + (KMAX / 16) * 4 + 256;  // [NTB][NCW][HROWS] partial row sums
-constexpr int OFF_TBC = OFF_TB + NTB * NCW * HROWS * 4;  // [NTB] arrival counters
-constexpr int OFF_BAR = OFF_TBC + NTB * 4;               // mbarriers
+constexpr int OFF_TBC = OFF_TB + NTB * NCW * HROWS * 4;  // [NTB] arrival counters, then [NTB] guards
+constexpr int OFF_BAR = OFF_TBC + 2 * NTB * 4;           // mbarriers
 constexpr int OFF_MISC = OFF_BAR + 320;
-constexpr int SMEM_BYTES = OFF_MISC + 1024;  // red[64] f32, bcast[64] i32, moew[64] f32, spare
+constexpr int OFF_PHB = OFF_MISC + 1024;  // red[64] f32, bcast[64] i32, moew[64] f32, spare
+constexpr int PHB_BYTES = 256;            // one phase descriptor (two buffers)
+constexpr int SMEM_BYTES = OFF_PHB + 2 * PHB_BYTES;
+static_assert(OFF_PHB % 16 == 0, "phase descriptor buffers take 16-byte copies");
 static_assert(NSLOT % NCW == 0, "ring entries must map to a fixed warp");
 static_assert((2 * NSLOT + 1) * 8 <= 320, "mbarrier area");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
@@ -102,10 +107,11 @@ enum ErrCode {
   ERR_BAD_PROGRAM = 6,
   ERR_BAD_POS = 7,    // *d_pos outside [0, Tmax)
   ERR_BAD_TOKEN = 8,  // token id outside [0, vocab)
-  ERR_WAIT_ROUTER = 9 // the producer gave up waiting for the expert choice
+  ERR_WAIT_ROUTER = 9, // the producer gave up waiting for the expert choice
+  ERR_WAIT_COMBINE = 10 // a half-tile combine buffer was not handed on in time
 };
 
-struct Phase {
+struct alignas(16) Phase {
   int kind;
   int wait_bar;    // grid barrier to wait on before the phase (-1: none)
   int signal_bar;  // grid barrier to arrive on after the phase (-1: none)
@@ -141,6 +147,7 @@ struct Phase {
   long long x_sstride;     // floats between experts (MOE_DOWNU)
   long long out_mstride;   // elements between rows of the epilogue target
 };
+static_assert(sizeof(Phase) % 16 == 0 && sizeof(Phase) <= PHB_BYTES, "phase descriptor copies");
 
 // Split of a decode attention over positions 0..T-1 into nch chunks of CH
 // positions per kv head (CH a multiple of the slot size, chunks of at least
