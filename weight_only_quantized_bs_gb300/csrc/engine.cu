@@ -78,6 +78,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
+__device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -165,6 +170,7 @@ struct Smem {
   uint64_t* full;   // [NSLOT]
   uint64_t* empty;  // [NSLOT]
   uint64_t* cbar;   // consumer-warps barrier
+  uint64_t* xbar;   // completion of the bulk copy of a phase's input vector
   float* red;       // [64] reduction scratch; [32..39] router logits, [40..41] expert weights
   int* bcast;       // [64] broadcast ints; [32..33] chosen experts, [34] phase they were chosen in,
                     // [48..55] verify: union of the rows' experts, [56] its size
@@ -183,6 +189,7 @@ __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
   s.full = reinterpret_cast<uint64_t*>(base + OFF_BAR);
   s.empty = s.full + NSLOT;
   s.cbar = s.empty + NSLOT;
+  s.xbar = s.cbar + 1;
   s.red = reinterpret_cast<float*>(base + OFF_MISC);
   s.bcast = reinterpret_cast<int*>(base + OFF_MISC + 256);
   s.moew = reinterpret_cast<float*>(base + OFF_MISC + 512);
@@ -461,6 +468,7 @@ struct Cons {
   int warp, lane, ctid;
   uint32_t starved;  // slot waits that found the slot still in flight (warp 0)
   float rnorm;       // RMSNorm factor of the staged input (1 if none)
+  uint32_t xphase;   // parity of the input-copy barrier
 };
 
 // all consumer warps meet; false if the wait gave up
@@ -558,7 +566,7 @@ __device__ __forceinline__ void stage_store(const Smem& S, const Cons& cs, int d
 // the gain is applied here: the factor 1/rms needs the whole vector, and as
 // the GEMV is linear it is applied to the outputs in the epilogue instead
 // (cs.rnorm, 1 for other inputs), which keeps the reduction off the path.
-__device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
+__device__ bool stage_x_regs(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
   constexpr int NT = NCW * 32, MAXIT = (KMAX / 4 + NT - 1) / NT;
   const int K = ph.K, dt = ph.dtype, U = per_chunk(dt) / 4, K4 = K / 4;
   const bool norm = ph.xsrc == X_NORM || ph.xsrc == X_EMBED_NORM;
@@ -609,6 +617,65 @@ __device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& c
       }
       stage_store(S, cs, dt, U, k4, k4 < K4, a[t]);
     }
+  }
+  if (norm) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (cs.lane == 0) S.red[cs.warp] = ss;
+  }
+  if (!cta_sync(S, cs, P.err)) return false;
+  cs.rnorm = 1.0f;
+  if (norm) {
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) tot += S.red[w];
+    cs.rnorm = 1.0f / sqrtf(tot / (float)K + ph.eps);
+  }
+  return true;
+}
+
+// Stages an fp32 input vector (X_F32, or X_NORM with its bf16 gain) with
+// per-thread asynchronous copies into the x area (the gain into the top of
+// that area), then converts it in place with a short loop: gain, 1/rms
+// partial sums, the dequantisation multipliers, the per-chunk swizzle and the
+// chunk sums.  Warp w copies and converts the runs of 32 float4 starting at
+// 32 w + 224 i (whole chunks): its lanes' copies are complete and visible to
+// the warp after wait_all and __syncwarp, and all lanes load a run before any
+// lane stores into it, so the in-place permutation inside a chunk is safe.
+// The copies use the load/store path, not the bulk-copy engine, whose queue
+// holds the producer's weight prefetches.  Other inputs (bf16 vectors, the
+// embedding row) go through stage_x_regs.
+__device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
+  const int K = ph.K, dt = ph.dtype, U = per_chunk(dt) / 4, K4 = K / 4;
+  const bool norm = ph.xsrc == X_NORM;
+  const bool fast = (ph.xsrc == X_F32 || norm) && (!norm || (K * 6 <= KMAX * 4 && ((uintptr_t)ph.gain & 7) == 0)) &&
+                    ((uintptr_t)ph.xptr & 15) == 0;
+  if (!fast) return stage_x_regs(ph, P, S, cs, cta);
+  float4* xs4 = reinterpret_cast<float4*>(S.xs);
+  uint2* gs = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(S.xs) + KMAX * 4 - K * 2);
+  const float4* src = reinterpret_cast<const float4*>(ph.xptr);
+  const uint2* gsrc = reinterpret_cast<const uint2*>(ph.gain);
+#pragma unroll 1
+  for (int f = cs.warp * 32 + cs.lane; f < K4; f += NCW * 32) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(xs4 + f)), "l"(src + f) : "memory");
+    if (norm) asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(gs + f)), "l"(gsrc + f) : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  cp_async_wait_all();
+  __syncwarp();
+  float ss = 0.0f;
+#pragma unroll 1
+  for (int base = cs.warp * 32; base < K4; base += NCW * 32) {  // warp-uniform trip count
+    const int f = base + cs.lane;
+    const bool in = f < K4;
+    float4 a = in ? xs4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (norm) {
+      ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+      const float4 g = bf4(in ? gs[f] : make_uint2(0u, 0u));
+      a = make_float4(a.x * g.x, a.y * g.y, a.z * g.z, a.w * g.w);
+    }
+    __syncwarp();  // every lane has read the run before any lane overwrites it
+    stage_store(S, cs, dt, U, f, in, a);
   }
   if (norm) {
 #pragma unroll
@@ -740,15 +807,15 @@ __device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, 
   }
 }
 
-// The work of one lane on one slot: its chunk (number g of the row) of
-// every row of the slot.  LBC is the slot's width in chunks when known at
-// compile time (full K-blocks: row offsets become immediates), else 0.
-template <int DT, int LBC>
+// The work of one lane on one slot of Lb chunks per row: its chunk (number g
+// of the row) of every row of the slot.  One copy of this code serves every
+// slot width, which keeps the engine's hot code small.
+template <int DT>
 __device__ __forceinline__ void slot_rows(const uint8_t* base, int Lb, int lane, int g, const float4* xs4, const Smem& S,
                                           float* v, float2* acc, float& bias) {
   constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
   constexpr int U = E / 4;
-  const int L = LBC ? LBC : Lb;
+  const int L = Lb;
   // The four words of the chunk go by in a run-time loop (a small loop body
   // stays in the instruction cache); in step jw lane l reads word
   // (jw + l / 8) % 4, so that the 32 lanes' 4-byte loads hit 32 banks.
@@ -881,10 +948,7 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
           const int Lb = min(KBLK, C - b * KBLK);
           // lane l takes chunk l of every row of the slot (rows past the
           // tile read in-bounds stale bytes of the slot and are discarded)
-          if (lane < Lb) {
-            if (Lb == KBLK) slot_rows<DT, KBLK>(base, Lb, lane, b * KBLK + lane, xs4, S, v, acc, bias);
-            else slot_rows<DT, 0>(base, Lb, lane, b * KBLK + lane, xs4, S, v, acc, bias);
-          }
+          if (lane < Lb) slot_rows<DT>(base, Lb, lane, b * KBLK + lane, xs4, S, v, acc, bias);
           slot_release(S, cs, it);
         }
         if (DT != DT_INT4) {
@@ -935,15 +999,113 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
 }
 
 // ----------------------------------------------------------- attention ---
-// One unit = one kv head x one chunk of positions.  Each slot (16 positions
-// of K and V) belongs to the warp given by its stream index; lane l owns dims
-// l*DPL..l*DPL+DPL-1.  Each warp keeps an online softmax (m, l, o) per q head
-// of the group; the warps merge in shared memory; a head split over several
+// One unit = one query row x one kv head x one chunk of positions.  Each slot
+// (16 positions of K and V) belongs to the warp given by its stream index.
+// A warp takes the 16 positions of a block at once: lane l holds dims
+// l*DPL .. l*DPL+DPL-1 (DPL = HD/32) of every position; it forms the 16
+// partial dot products of its dims, a reduce-scatter over the lanes leaves
+// lane l with the score of position l/2, and the block updates the warp's
+// online softmax (m, l, o) once per q head: one rescale, one exponential per
+// position, and the V sum weighted by each position's probability broadcast
+// from its lane.  The warps merge in shared memory; a head split over several
 // chunks merges its chunks' (m, l, o) in the CTA that finishes last
 // (log-sum-exp combine).
+// Rows of one block, this lane's dims (bf16 pairs): NP positions of K or V.
+template <int HD, int NP>
+struct AttnRows {
+  uint32_t w[NP][HD / 64];
+};
+// Loads positions 0..np-1 of NP rows (HD bf16 each, consecutive) starting at
+// R; rows past np are zero.  GLOBAL: rows written during this launch, read
+// around the L1 cache.
+template <int HD, int NP, bool GLOBAL>
+__device__ __forceinline__ void attn_rows(AttnRows<HD, NP>& r, const uint16_t* R, int np, int lane) {
+  constexpr int DPL = HD / 32;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const uint16_t* src = R + (size_t)i * HD + lane * DPL;
+    if constexpr (DPL == 4) {
+      uint2 t = make_uint2(0u, 0u);
+      if (i < np) t = GLOBAL ? __ldcg(reinterpret_cast<const uint2*>(src)) : *reinterpret_cast<const uint2*>(src);
+      r.w[i][0] = t.x;
+      r.w[i][1] = t.y;
+    } else {
+      uint32_t t = 0u;
+      if (i < np) t = GLOBAL ? __ldcg(reinterpret_cast<const unsigned*>(src)) : *reinterpret_cast<const uint32_t*>(src);
+      r.w[i][0] = t;
+    }
+  }
+}
+// Scores of a block of np positions (K rows kr) for the gq q heads (q: this
+// lane's dims of each head, pre-scaled by 1/sqrt(HD)); updates m and l and
+// returns in pr[jj] the probability of position lane/2 (0 past np) and in
+// cr[jj] the factor that rescales the head's running output.
+template <int HD, int NP>
+__device__ __forceinline__ void attn_scores(const AttnRows<HD, NP>& kr, int np, int gq, const float (*q)[HD / 32],
+                                            float* m, float* l, float* pr, float* cr, int lane) {
+  constexpr int DPL = HD / 32;
+  const bool valid = (lane >> 1) < np;
+#pragma unroll
+  for (int jj = 0; jj < MAX_GQ; ++jj) {
+    pr[jj] = 0.f;
+    cr[jj] = 1.f;
+    if (jj < gq) {
+      float part[ATT_POS_PER_SLOT];
+#pragma unroll
+      for (int i = 0; i < ATT_POS_PER_SLOT; ++i) {
+        float d = 0.f;
+        if (i < NP) {
+#pragma unroll
+          for (int e = 0; e < DPL / 2; ++e) {
+            d = fmaf(q[jj][2 * e], __uint_as_float(kr.w[i][e] << 16), d);
+            d = fmaf(q[jj][2 * e + 1], __uint_as_float(kr.w[i][e] & 0xFFFF0000u), d);
+          }
+        }
+        part[i] = d;
+      }
+      float sc = warp_rows16(part, lane);  // score of position lane / 2 (all lanes shuffle)
+      if (!valid) sc = -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int of = 2; of < 32; of <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, of));
+      const float mn = fmaxf(m[jj], mx);
+      cr[jj] = expf(m[jj] - mn);  // 0 while the state is empty (m = -inf)
+      pr[jj] = valid ? expf(sc - mn) : 0.f;
+      float ps = 0.5f * pr[jj];  // each position sits in two lanes
+#pragma unroll
+      for (int of = 1; of < 32; of <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, of);
+      l[jj] = fmaf(l[jj], cr[jj], ps);
+      m[jj] = mn;
+    }
+  }
+}
+// o = o * cr + sum_i pr_i v_i for each head (V rows vr).
+template <int HD, int NP>
+__device__ __forceinline__ void attn_values(const AttnRows<HD, NP>& vr, int gq, const float* pr, const float* cr,
+                                            float (*o)[HD / 32]) {
+  constexpr int DPL = HD / 32;
+#pragma unroll
+  for (int jj = 0; jj < MAX_GQ; ++jj) {
+    if (jj < gq) {
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) o[jj][d] *= cr[jj];
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        const float pi = __shfl_sync(0xffffffffu, pr[jj], 2 * i);
+#pragma unroll
+        for (int e = 0; e < DPL / 2; ++e) {
+          o[jj][2 * e] = fmaf(pi, __uint_as_float(vr.w[i][e] << 16), o[jj][2 * e]);
+          o[jj][2 * e + 1] = fmaf(pi, __uint_as_float(vr.w[i][e] & 0xFFFF0000u), o[jj][2 * e + 1]);
+        }
+      }
+    }
+  }
+}
+
 template <int HD>
 __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, const AttnUnit& au, int pos,
                           uint32_t& j) {
+  constexpr int DPL = HD / 32;
   const int gq = ph.Hq / ph.Hkv;
   const int kvh = au.kvh, c = au.c, nch = au.nch;
   const int p0 = au.p0, p1 = au.p1, pe = min(p1, au.Ts);
@@ -952,29 +1114,20 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   float* qs = S.xs;                       // [gq][HD], pre-scaled by 1/sqrt(HD)
   float* sc = S.xs + MAX_GQ * HD;         // [NCW][gq][HD + 2]
   const int nslots = pe > p0 ? (pe - p0 + ATT_POS_PER_SLOT - 1) / ATT_POS_PER_SLOT : 0;
-  // positions not streamed (rows written during this launch) go to the warp
-  // after the last slot's owner; the first two are loaded up front
+  // positions not streamed (rows written during this launch, at most 8) go
+  // to the warp after the last slot's owner, which loads them right away
   const int pg = max(pe, p0);
   const int gw = (int)((cs.it + j + (uint32_t)nslots) % NCW);
   const bool has_g = (w == gw) && pg < p1;
-  uint32_t gk[HD / 32], gv[HD / 32];
-#pragma unroll
-  for (int e = 0; e < HD / 32; ++e) gk[e] = gv[e] = 0u;
-  auto load_global = [&](int p, uint32_t* kw, uint32_t* vw) {
-    const size_t off = ((size_t)kvh * ph.Tmax + p) * HD + (lane & 15) * (HD / 16);
-    if constexpr (HD / 16 == 8) {
-      const uint4 kk = __ldcg(reinterpret_cast<const uint4*>(ph.kc + off));
-      const uint4 vv = __ldcg(reinterpret_cast<const uint4*>(ph.vc + off));
-      kw[0] = kk.x; kw[1] = kk.y; kw[2] = kk.z; kw[3] = kk.w;
-      vw[0] = vv.x; vw[1] = vv.y; vw[2] = vv.z; vw[3] = vv.w;
-    } else {
-      const uint2 kk = __ldcg(reinterpret_cast<const uint2*>(ph.kc + off));
-      const uint2 vv = __ldcg(reinterpret_cast<const uint2*>(ph.vc + off));
-      kw[0] = kk.x; kw[1] = kk.y;
-      vw[0] = vv.x; vw[1] = vv.y;
-    }
-  };
-  if (has_g && pg + (lane >> 4) < p1) load_global(pg + (lane >> 4), gk, gv);
+  // rows written during this launch: a verify pass's own rows (at most
+  // MAX_M) or a decode step's current row
+  constexpr int NPG = MAX_M;
+  AttnRows<HD, NPG> gk, gv;
+  if (has_g) {
+    const size_t off = ((size_t)kvh * ph.Tmax + pg) * HD;
+    attn_rows<HD, NPG, true>(gk, ph.kc + off, p1 - pg, lane);
+    attn_rows<HD, NPG, true>(gv, ph.vc + off, p1 - pg, lane);
+  }
   const float scale = rsqrtf((float)HD);
   for (int i = cs.ctid; i < gq * HD; i += NCW * 32) {
     const size_t qi = qrow + (size_t)kvh * gq * HD + i;
@@ -984,107 +1137,51 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   }
   if (!cta_sync(S, cs, P.err)) return false;
 
-  // Each warp takes two positions per step: lanes 0..15 one, 16..31 the
-  // other; lane l owns dims (l % 16) * DP2 .. + DP2 - 1 of its position.
-  constexpr int DP2 = HD / 16;
-  const int half = lane >> 4, hl = lane & 15;
-  float m[MAX_GQ], l[MAX_GQ], o[MAX_GQ][DP2];
+  float q[MAX_GQ][DPL], m[MAX_GQ], l[MAX_GQ], o[MAX_GQ][DPL];
 #pragma unroll
   for (int jj = 0; jj < MAX_GQ; ++jj) {
     m[jj] = -INFINITY;
     l[jj] = 0.f;
 #pragma unroll
-    for (int d = 0; d < DP2; ++d) o[jj][d] = 0.f;
+    for (int d = 0; d < DPL; ++d) {
+      q[jj][d] = jj < gq ? qs[jj * HD + lane * DPL + d] : 0.f;
+      o[jj][d] = 0.f;
+    }
   }
-  // one position per half-warp: kw / vw hold this lane's DP2 dims of the
-  // position's K and V rows (bf16 pairs); `valid` false leaves the state as is
-  auto load_kv = [&](const uint16_t* klane, const uint16_t* vlane, uint32_t* kw, uint32_t* vw) {
-    if constexpr (DP2 == 8) {
-      const uint4 kk = *reinterpret_cast<const uint4*>(klane), vv = *reinterpret_cast<const uint4*>(vlane);
-      kw[0] = kk.x; kw[1] = kk.y; kw[2] = kk.z; kw[3] = kk.w;
-      vw[0] = vv.x; vw[1] = vv.y; vw[2] = vv.z; vw[3] = vv.w;
-    } else {
-      const uint2 kk = *reinterpret_cast<const uint2*>(klane), vv = *reinterpret_cast<const uint2*>(vlane);
-      kw[0] = kk.x; kw[1] = kk.y;
-      vw[0] = vv.x; vw[1] = vv.y;
-    }
-  };
-  auto consume2 = [&](const uint32_t* kw, const uint32_t* vw, bool valid) {
-    float kf[DP2], vf[DP2];
-#pragma unroll
-    for (int e = 0; e < DP2 / 2; ++e) {
-      kf[2 * e] = __uint_as_float(kw[e] << 16);
-      kf[2 * e + 1] = __uint_as_float(kw[e] & 0xFFFF0000u);
-      vf[2 * e] = __uint_as_float(vw[e] << 16);
-      vf[2 * e + 1] = __uint_as_float(vw[e] & 0xFFFF0000u);
-    }
-#pragma unroll
-    for (int jj = 0; jj < MAX_GQ; ++jj) {
-      if (jj < gq) {
-        float dot = 0.f;
-#pragma unroll
-        for (int d = 0; d < DP2; ++d) dot = fmaf(qs[jj * HD + hl * DP2 + d], kf[d], dot);
-#pragma unroll
-        for (int of = 8; of; of >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, of);
-        if (valid) {
-          const float mn = fmaxf(m[jj], dot);
-          const float corr = expf(m[jj] - mn), p = expf(dot - mn);
-          l[jj] = fmaf(l[jj], corr, p);
-#pragma unroll
-          for (int d = 0; d < DP2; ++d) o[jj][d] = fmaf(o[jj][d], corr, p * vf[d]);
-          m[jj] = mn;
-        }
-      }
-    }
-  };
+  float pr[MAX_GQ], cr[MAX_GQ];
+  if (has_g) {
+    attn_scores<HD, NPG>(gk, p1 - pg, gq, q, m, l, pr, cr, lane);
+    attn_values<HD, NPG>(gv, gq, pr, cr, o);
+  }
   for (int k = (w - (int)((cs.it + j) % NCW) + NCW) % NCW; k < nslots; k += NCW) {
     const uint32_t it = cs.it + j + (uint32_t)k;
     const int np = min(ATT_POS_PER_SLOT, pe - (p0 + k * ATT_POS_PER_SLOT));
     const uint8_t* base;
     if (!slot_acquire(S, cs, it, P.err, base)) return false;
     const uint16_t* kb = reinterpret_cast<const uint16_t*>(base);
-    const uint16_t* vb = kb + ATT_POS_PER_SLOT * HD;
-    for (int q = 0; q < np; q += 2) {
-      const int qq = q + half;
-      uint32_t kw[DP2 / 2], vw[DP2 / 2];
-#pragma unroll
-      for (int e = 0; e < DP2 / 2; ++e) kw[e] = vw[e] = 0u;
-      if (qq < np) load_kv(kb + qq * HD + hl * DP2, vb + qq * HD + hl * DP2, kw, vw);
-      consume2(kw, vw, qq < np);
+    {
+      AttnRows<HD, ATT_POS_PER_SLOT> kr;
+      attn_rows<HD, ATT_POS_PER_SLOT, false>(kr, kb, np, lane);
+      attn_scores<HD, ATT_POS_PER_SLOT>(kr, np, gq, q, m, l, pr, cr, lane);
     }
-    slot_release(S, cs, it);
+    {
+      AttnRows<HD, ATT_POS_PER_SLOT> vr;
+      attn_rows<HD, ATT_POS_PER_SLOT, false>(vr, kb + ATT_POS_PER_SLOT * HD, np, lane);
+      slot_release(S, cs, it);  // the slot's rows are in registers
+      attn_values<HD, ATT_POS_PER_SLOT>(vr, gq, pr, cr, o);
+    }
   }
   j += (uint32_t)nslots;
-  if (has_g) {
-    consume2(gk, gv, pg + half < p1);
-    for (int p = pg + 2; p < p1; p += 2) {
-      uint32_t kw[DP2 / 2], vw[DP2 / 2];
-#pragma unroll
-      for (int e = 0; e < DP2 / 2; ++e) kw[e] = vw[e] = 0u;
-      if (p + half < p1) load_global(p + half, kw, vw);
-      consume2(kw, vw, p + half < p1);
-    }
-  }
-  // merge the two half-warps (xor 16), then the warps of this CTA
+  // the warps of this CTA merge in shared memory
 #pragma unroll
   for (int jj = 0; jj < MAX_GQ; ++jj) {
     if (jj < gq) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m[jj], 16);
-      const float lo = __shfl_xor_sync(0xffffffffu, l[jj], 16);
-      const float mn = fmaxf(m[jj], mo);
-      const float ea = l[jj] > 0.f ? expf(m[jj] - mn) : 0.f, eb = lo > 0.f ? expf(mo - mn) : 0.f;
+      float* dst = sc + (w * gq + jj) * (HD + 2);
 #pragma unroll
-      for (int d = 0; d < DP2; ++d) o[jj][d] = o[jj][d] * ea + __shfl_xor_sync(0xffffffffu, o[jj][d], 16) * eb;
-      l[jj] = l[jj] * ea + lo * eb;
-      m[jj] = mn;
-      if (half == 0) {
-        float* dst = sc + (w * gq + jj) * (HD + 2);
-#pragma unroll
-        for (int d = 0; d < DP2; ++d) dst[2 + hl * DP2 + d] = o[jj][d];
-        if (hl == 0) {
-          dst[0] = m[jj];
-          dst[1] = l[jj];
-        }
+      for (int d = 0; d < DPL; ++d) dst[2 + lane * DPL + d] = o[jj][d];
+      if (lane == 0) {
+        dst[0] = m[jj];
+        dst[1] = l[jj];
       }
     }
   }
@@ -1630,6 +1727,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
       mbar_init(&S.empty[i], 1);
     }
     mbar_init(S.cbar, NCW * 32);
+    mbar_init(S.xbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < NTB) {
@@ -1673,6 +1771,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   cs.ctid = tid;
   cs.starved = 0;
   cs.rnorm = 1.0f;
+  cs.xphase = 0;
   const int G = P.nctas;
   ArgMax am = {-INFINITY, 0x7fffffff};
   ArgMax amv[MAX_M];
