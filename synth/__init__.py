@@ -79,6 +79,7 @@ def bf16_to_f32(u16):
 
 # Tensor ids of a decoder model: every tensor of layer l gets its own stream.
 TID_EMBED, TID_LM_HEAD, TID_FINAL_NORM, TID_PROMPT, TID_X = 1, 2, 3, 4, 5
+TID_KV_BASE = 900_000  # pre-filled KV cache rows: TID_KV_BASE + 2 * layer (+1 for V)
 _LAYER_BASE = 1000
 LAYER_TENSORS = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "g_attn", "g_ffn", "router")
 

@@ -8,7 +8,7 @@ This module only draws numbers: it neither quantises nor computes.
 """
 import numpy as np
 
-from . import (TID_EMBED, TID_FINAL_NORM, TID_LM_HEAD, TID_PROMPT, layer_tid, normal_bf16,
+from . import (TID_EMBED, TID_FINAL_NORM, TID_KV_BASE, TID_LM_HEAD, TID_PROMPT, layer_tid, normal_bf16,
                uniform_int)
 
 
@@ -77,6 +77,15 @@ def global_weights(cfg, seed):
         "lm_head": normal_bf16(seed, TID_LM_HEAD, (V, d), SIGMA_W),
         "g_final": normal_bf16(seed, TID_FINAL_NORM, (d,), SIGMA_W, mu=1.0),
     }
+
+
+def kv_prefill(cfg, seed, layer, n_pos):
+    """A context of n_pos positions written straight into layer `layer`'s KV
+    cache (the long-context decode workloads fix the context length without
+    running a prefill): K and V rows bf16 N(0, 1), shape [n_kv_heads, n_pos,
+    head_dim] each."""
+    shape = (cfg["n_kv_heads"], n_pos, cfg["head_dim"])
+    return (normal_bf16(seed, TID_KV_BASE + 2 * layer, shape), normal_bf16(seed, TID_KV_BASE + 2 * layer + 1, shape))
 
 
 def prompt(cfg, seed, n, tid=TID_PROMPT):
