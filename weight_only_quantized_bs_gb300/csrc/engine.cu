@@ -417,6 +417,59 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
           }
         }
       }
+    } else if (ph.kind == PH_FFN) {
+      // per gate/up tile: its two half-tiles' K-blocks, then the rows of the
+      // matching 16-column slice of the down projection
+      const int dt = ph.dtype, C = ph.K / per_chunk(dt), nb = (C + KBLK - 1) / KBLK;
+      const int tps = ph.N / TR, d = ph.N2;
+      int nsl, DR;
+      ffn_split(dt, d, nsl, DR);
+      // the down slice of a tile follows the next tile's gate/up blocks, so
+      // that its SwiGLU outputs are ready when its rows arrive
+      auto down_slice = [&](int t) {
+        for (int k = 0; k < nsl && ok; ++k) {
+          const int r0 = k * DR, nr = min(DR, d - r0);  // > 0 (ffn_split)
+          const uint8_t* src;
+          const uint8_t* szs = nullptr;
+          uint32_t cb;
+          if (dt == DT_INT4) {
+            const uint8_t* g = ph.W2 + (size_t)(t >> 1) * d * 20;
+            src = g + (size_t)(t & 1) * d * 8 + (size_t)r0 * 8;
+            szs = g + (size_t)d * 16 + (size_t)r0 * 4;
+            cb = (uint32_t)nr * 8;
+          } else {
+            const int rb = dt == DT_INT8 ? 16 : 32;
+            src = ph.W2 + ((size_t)t * d + r0) * rb;
+            cb = (uint32_t)(nr * rb);
+          }
+          uint8_t* dst;
+          uint64_t* fb;
+          if (!(ok = prod_slot(S, pr, err, dst, fb))) break;
+          mbar_expect_tx(fb, cb + (szs ? (uint32_t)nr * 4 : 0u));
+          bulk_g2s(dst, src, cb, fb, pr.pol);
+          if (szs) bulk_g2s(dst + (size_t)DR * 8, szs, (uint32_t)nr * 4, fb, pr.pol);
+        }
+      };
+      int prev = -1;
+      for (int t = first_unit(cta, ph.rot, G); t < tps && ok; t += G) {
+        for (int h = 0; h < 2 && ok; ++h) {
+          for (int b = 0; b < nb && ok; ++b) {
+            const int Lb = min(KBLK, C - b * KBLK);
+            const uint8_t* blk = ph.W + block_offset(dt, C, t, TR, b);
+            const uint32_t cb = (uint32_t)(HROWS * Lb * 16);
+            const uint32_t sb = dt == DT_INT4 ? (uint32_t)(HROWS * Lb * 4) : 0u;
+            uint8_t* dst;
+            uint64_t* fb;
+            if (!(ok = prod_slot(S, pr, err, dst, fb))) break;
+            mbar_expect_tx(fb, cb + sb);
+            bulk_g2s(dst, blk + (size_t)h * HROWS * Lb * 16, cb, fb, pr.pol);
+            if (sb) bulk_g2s(dst + SLOT_SZ_OFF, blk + (size_t)TR * Lb * 16 + (size_t)h * HROWS * Lb * 4, sb, fb, pr.pol);
+          }
+        }
+        if (prev >= 0) down_slice(prev);
+        prev = t;
+      }
+      if (prev >= 0 && ok) down_slice(prev);
     } else if (ph.kind == PH_ATTN) {
       const uint32_t rowb = (uint32_t)ph.hd * 2;
       const int nunits = attn_units(ph, P, pos, -1, nullptr);
@@ -892,109 +945,280 @@ __device__ __forceinline__ bool tb_claim(const Smem& S, const Cons& cs, int buf,
 // registers (16 rows per lane), reduces them over the lanes, and deposits the
 // 16 row sums in the half-tile's combine buffer; the last contributing warp
 // adds the deposits in warp order and runs the epilogue.
+// One half-tile (16 rows r0.. of tile lt of segment seg; its nb K-blocks are
+// the CTA's local slots j0 ..) for the calling warp: its K-blocks, the lane
+// reduction, the deposit, and for the last contributing warp the combine.
+// Returns -1 if a wait gave up, 1 for the combining warp (lanes r < 16 hold
+// in tot the row sum of row r0 + r, already multiplied by the row's output
+// factor, and in rp its RoPE pair), else 0.
+template <int DT>
+__device__ __forceinline__ int gemv_half(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int seg, int lt,
+                                         int r0, int Rt, uint32_t j0, int pos, float& tot, float2& rp) {
+  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
+  const int C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
+  const int nseg = ph.moe == MOE_GU ? 2 : 1, Ns = ph.N / nseg;
+  const int lane = cs.lane, w = cs.warp;
+  const int own0 = (int)((cs.it + j0) % NCW);  // owner of K-block 0
+  const int bfirst = (w - own0 + NCW) % NCW;   // this warp's first K-block
+  const int ncontrib = nb < NCW ? nb : NCW;
+  if (bfirst >= nb) return 0;
+  const float4* xs4 = reinterpret_cast<const float4*>(S.xs);
+  // int8 row scales of the segment's matrix (the chosen expert's, for MoE)
+  const uint16_t* s8 = ph.s8;
+  if (DT == DT_INT8 && ph.moe != MOE_NONE)
+    s8 += (size_t)S.bcast[32 + (ph.moe == MOE_GU ? seg : ph.moe - MOE_DOWN0)] * Ns;
+  // the epilogue's own inputs, fetched now so that their latency is hidden
+  // behind the K-blocks: lane r < 16 for row r0 + r
+  float pf = cs.rnorm * (DT == DT_BF16 ? 1.0f : DQ_UP);  // RMSNorm, 2^64, int8 row scale
+  rp = make_float2(1.f, 0.f);
+  {
+    const int n = lt * TR + r0 + lane;
+    if (lane < HROWS && r0 + lane < Rt) {
+      if (DT == DT_INT8) pf *= bf2f(s8[n]);
+      if (ph.epi == EPI_QKV && n < ph.q_rows + ph.kv_rows) {
+        const int nn = n < ph.q_rows ? n : n - ph.q_rows;
+        rp = P.rope[(size_t)pos * (ph.hd / 2) + (nn % ph.hd) / 2];
+      }
+    }
+  }
+  // int4: v[r] collects s * (codes . x) + z * (sum of x) per group, x 2^-64;
+  // int8 / bf16: acc[r] collects the row's dot product over the blocks
+  float v[HROWS];
+  float2 acc[HROWS];
+#pragma unroll
+  for (int r = 0; r < HROWS; ++r) {
+    v[r] = 0.0f;
+    acc[r] = make_float2(0.f, 0.f);
+  }
+  float bias = 0.0f;  // int8: 128 * sum x * 2^-64 over this lane's chunks
+  for (int b = bfirst; b < nb; b += NCW) {
+    const uint32_t it = cs.it + j0 + (uint32_t)b;
+    const uint8_t* base;
+    if (!slot_acquire(S, cs, it, P.err, base)) return -1;
+    const int Lb = min(KBLK, C - b * KBLK);
+    // lane l takes chunk l of every row of the slot (rows past the tile read
+    // in-bounds stale bytes of the slot and are discarded)
+    if (lane < Lb) slot_rows<DT>(base, Lb, lane, b * KBLK + lane, xs4, S, v, acc, bias);
+    slot_release(S, cs, it);
+  }
+  if (DT != DT_INT4) {
+#pragma unroll
+    for (int r = 0; r < HROWS; ++r) v[r] = (acc[r].x + acc[r].y) - bias;
+  }
+  // deposit this warp's 16 row sums, then the last contributor combines
+  const float y = warp_rows16(v, lane);
+  const int buf = (int)(cs.useq % NTB);
+  float* tb = S.tb + (size_t)buf * NCW * HROWS;
+  // the buffer's previous half-tile has been combined (bounded wait; in
+  // practice it was long ago)
+  if (!tb_claim(S, cs, buf, P.err)) return -1;
+  if ((lane & 1) == 0) tb[w * HROWS + (lane >> 1)] = y;
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) {
+    __threadfence_block();
+    last = atomicAdd(S.tbc + buf, 1) == ncontrib - 1;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return 0;
+  __threadfence_block();
+  float t = 0.0f;
+  if (lane < HROWS) {
+    for (int ww = 0; ww < NCW; ++ww) {
+      const int bw = (ww - own0 + NCW) % NCW;
+      if (bw < nb) t += tb[ww * HROWS + lane];
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    S.tbc[buf] = 0;
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(S.tbg + buf) = (int)(cs.useq + NTB);  // hand the buffer on
+  }
+  tot = t * pf;
+  return 1;
+}
+
+// One GEMV phase for this CTA: its tiles (round-robin over the CTAs), two
+// half-tiles each; the combining warp of a half-tile runs the epilogue.
 template <int DT>
 __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta, int pos, ArgMax& am) {
   constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
-  constexpr int U = E / 4;
   const int G = P.nctas;
   const int C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
   const int nseg = ph.moe == MOE_GU ? 2 : 1, Ns = ph.N / nseg;
   const int tps = (Ns + TR - 1) / TR, ntiles = nseg * tps;
-  const int lane = cs.lane, w = cs.warp;
-  const float4* xs4 = reinterpret_cast<const float4*>(S.xs);
-  const float fac = cs.rnorm * (DT == DT_BF16 ? 1.0f : DQ_UP);
+  const int lane = cs.lane;
   uint32_t j = 0;  // slot index within the phase
   for (int t = first_unit(cta, ph.rot, G); t < ntiles; t += G) {
     const int seg = t / tps, lt = t % tps;
     const int Rt = min(TR, Ns - lt * TR);
-    // int8 row scales of the segment's matrix (the chosen expert's, for MoE)
-    const uint16_t* s8 = ph.s8;
-    if (DT == DT_INT8 && ph.moe != MOE_NONE)
-      s8 += (size_t)S.bcast[32 + (ph.moe == MOE_GU ? seg : ph.moe - MOE_DOWN0)] * Ns;
-    for (int h = 0; h * HROWS < Rt; ++h, ++cs.useq) {
-      const int r0 = h * HROWS;
-      const int own0 = (int)((cs.it + j) % NCW);                              // owner of K-block 0
-      const int bfirst = (w - own0 + NCW) % NCW;                               // this warp's first K-block
-      const int ncontrib = nb < NCW ? nb : NCW;
-      if (bfirst < nb) {
-        // the epilogue's own inputs, fetched now so that their latency is
-        // hidden behind the K-blocks: lane r < 16 for row r0 + r
-        float pf = fac;  // output factor: RMSNorm, 2^64, int8 row scale
-        float2 rp = make_float2(1.f, 0.f);  // RoPE (cos, sin) of the row pair
-        {
-          const int n = lt * TR + r0 + lane;
-          if (lane < HROWS && r0 + lane < Rt) {
-            if (DT == DT_INT8) pf *= bf2f(s8[n]);
-            if (ph.epi == EPI_QKV && n < ph.q_rows + ph.kv_rows) {
-              const int nn = n < ph.q_rows ? n : n - ph.q_rows;
-              rp = P.rope[(size_t)pos * (ph.hd / 2) + (nn % ph.hd) / 2];
-            }
-          }
-        }
-        // int4: v[r] collects s * (codes . x) + z * (sum of x) per group, x 2^-64;
-        // int8 / bf16: acc[r] collects the row's dot product over the blocks
-        float v[HROWS];
-        float2 acc[HROWS];
-#pragma unroll
-        for (int r = 0; r < HROWS; ++r) {
-          v[r] = 0.0f;
-          acc[r] = make_float2(0.f, 0.f);
-        }
-        float bias = 0.0f;  // int8: 128 * sum x * 2^-64 over this lane's chunks
-        for (int b = bfirst; b < nb; b += NCW) {
-          const uint32_t it = cs.it + j + (uint32_t)b;
-          const uint8_t* base;
-          if (!slot_acquire(S, cs, it, P.err, base)) return false;
-          const int Lb = min(KBLK, C - b * KBLK);
-          // lane l takes chunk l of every row of the slot (rows past the
-          // tile read in-bounds stale bytes of the slot and are discarded)
-          if (lane < Lb) slot_rows<DT>(base, Lb, lane, b * KBLK + lane, xs4, S, v, acc, bias);
-          slot_release(S, cs, it);
-        }
-        if (DT != DT_INT4) {
-#pragma unroll
-          for (int r = 0; r < HROWS; ++r) v[r] = (acc[r].x + acc[r].y) - bias;
-        }
-        // deposit this warp's 16 row sums, then the last contributor combines
-        const float y = warp_rows16(v, lane);
-        const int buf = (int)(cs.useq % NTB);
-        float* tb = S.tb + (size_t)buf * NCW * HROWS;
-        // the buffer's previous half-tile has been combined (bounded wait;
-        // in practice it was long ago)
-        if (!tb_claim(S, cs, buf, P.err)) return false;
-        if ((lane & 1) == 0) tb[w * HROWS + (lane >> 1)] = y;
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-          __threadfence_block();
-          last = atomicAdd(S.tbc + buf, 1) == ncontrib - 1;
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence_block();
-          float tot = 0.0f;
-          if (lane < HROWS) {
-            for (int ww = 0; ww < NCW; ++ww) {
-              const int bw = (ww - own0 + NCW) % NCW;
-              if (bw < nb) tot += tb[ww * HROWS + lane];
-            }
-          }
-          __syncwarp();
-          if (lane == 0) {
-            S.tbc[buf] = 0;
-            __threadfence_block();
-            *reinterpret_cast<volatile int*>(S.tbg + buf) = (int)(cs.useq + NTB);  // hand the buffer on
-          }
-          const int r = r0 + lane, n = lt * TR + r;
-          tot *= pf;
-          const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
-          if (lane < HROWS && r < Rt) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, rp, am);
-        }
-      }
-      j += (uint32_t)nb;
+    for (int h = 0; h * HROWS < Rt; ++h, ++cs.useq, j += (uint32_t)nb) {
+      float tot;
+      float2 rp;
+      const int k = gemv_half<DT>(ph, P, S, cs, seg, lt, h * HROWS, Rt, j, pos, tot, rp);
+      if (k < 0) return false;
+      if (k == 0) continue;
+      const int r = h * HROWS + lane, n = lt * TR + r;
+      const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
+      if (lane < HROWS && r < Rt) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, rp, am);
     }
   }
   cs.it += j;
+  return true;
+}
+
+// A dense FFN in one phase (PH_FFN).  For each of this CTA's gate/up tiles
+// (round-robin): the two half-tiles as in a GEMV phase, whose combining warps
+// write silu(gate) * up of their 8 pairs into a shared buffer instead of
+// memory; then the tile's 16-column slice of the down projection, split into
+// slots of rows: lane l takes rows l, l + 32, ... of a slot, multiplies the
+// slot's codes by the 16 SwiGLU outputs (dequantised as in the GEMV) and adds
+// into the CTA's partial down outputs in shared memory.  At the end the CTA
+// adds its partial outputs to the residual (vector atomics): the down
+// projection needs no phase, no grid barrier and no staging of its own.
+template <int DT>
+__device__ bool ffn_phase(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta, int pos) {
+  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
+  const int G = P.nctas, C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
+  const int tps = ph.N / TR, d = ph.N2;
+  int nsl, DR;
+  ffn_split(DT, d, nsl, DR);
+  const int lane = cs.lane, w = cs.warp;
+  float* dacc = S.xs + ph.K;  // [d] this CTA's partial down outputs
+  float* hb = dacc + d;       // [FFN_HN][16] SwiGLU outputs of the tiles in flight
+  int* hcnt = reinterpret_cast<int*>(hb + FFN_HN * 16);  // [FFN_HN] half-tiles finished per buffer
+  for (int i = cs.ctid; i < d; i += NCW * 32) dacc[i] = 0.0f;
+  if (cs.ctid < FFN_HN) hcnt[cs.ctid] = 0;
+  if (!cta_sync(S, cs, P.err)) return false;
+  uint32_t j = 0;
+  int kt = 0;  // this CTA's tiles so far
+  // the down slice of local tile kp (buffer e), slots j .. j + nsl - 1
+  auto down = [&](int kp) -> bool {
+    const int e = kp % FFN_HN, target = 2 * (kp / FFN_HN + 1);
+    for (int k = (w - (int)((cs.it + j) % NCW) + NCW) % NCW; k < nsl; k += NCW) {
+      // this tile's SwiGLU outputs (both half-tiles combined; bounded wait)
+      int ok = 1;
+      if (lane == 0) {
+        volatile int* c = hcnt + e;
+        if (*c < target) {
+          const uint64_t t0 = gtimer();
+          while (*c < target) {
+            __nanosleep(32);
+            if (gtimer() - t0 > WAIT_NS) {
+              atomicCAS(P.err, 0, ERR_WAIT_COMBINE);
+              ok = 0;
+              break;
+            }
+          }
+        }
+        __threadfence_block();
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      float hv[16];
+#pragma unroll
+      for (int c = 0; c < 16; c += 4) {
+        const float4 t4 = reinterpret_cast<const float4*>(hb)[e * 4 + c / 4];
+        hv[c] = t4.x;
+        hv[c + 1] = t4.y;
+        hv[c + 2] = t4.z;
+        hv[c + 3] = t4.w;
+      }
+      // the inputs as the subnormal dequantisation reads them (natural k order)
+      float2 xr[8];
+      float hs = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 16; c += 4) {
+        const float4 m = dq_mult(DT, DT == DT_INT4 ? (c >> 2) & 1 : 0);
+        xr[c / 2] = make_float2(hv[c] * m.x, hv[c + 1] * m.y);
+        xr[c / 2 + 1] = make_float2(hv[c + 2] * m.z, hv[c + 3] * m.w);
+        hs += (hv[c] + hv[c + 1]) + (hv[c + 2] + hv[c + 3]);
+      }
+      const float xz = DT == DT_INT4 ? hs * DQ_DOWN : DT == DT_INT8 ? 128.0f * hs * DQ_DOWN : 0.0f;
+      const uint32_t it = cs.it + j + (uint32_t)k;
+      const uint8_t* base;
+      if (!slot_acquire(S, cs, it, P.err, base)) return false;
+      const int r0 = k * DR, nr = min(DR, d - r0);
+#pragma unroll 4
+      for (int i = 0; i < (DR + 31) / 32; ++i) {
+        const int rl = lane + 32 * i;
+        if (rl < nr) {
+          float2 a = make_float2(0.f, 0.f);
+          float c;
+          if (DT == DT_INT4) {
+            const uint2 q = reinterpret_cast<const uint2*>(base)[rl];
+            a = word_int4(q.x, xr, a);
+            a = word_int4(q.y, xr + 4, a);
+            const uint32_t sz = reinterpret_cast<const uint32_t*>(base + (size_t)DR * 8)[rl];
+            c = fmaf(__uint_as_float(sz << 16), a.x + a.y, __uint_as_float(sz & 0xFFFF0000u) * xz);
+          } else if (DT == DT_INT8) {
+            const uint4 q = reinterpret_cast<const uint4*>(base)[rl];
+            a = word_int8(q.x, xr, a);
+            a = word_int8(q.y, xr + 2, a);
+            a = word_int8(q.z, xr + 4, a);
+            a = word_int8(q.w, xr + 6, a);
+            c = (a.x + a.y) - xz;
+          } else {
+            const uint4 q0 = reinterpret_cast<const uint4*>(base)[2 * rl], q1 = reinterpret_cast<const uint4*>(base)[2 * rl + 1];
+            a = word_bf16(q0.x, xr, a);
+            a = word_bf16(q0.y, xr + 1, a);
+            a = word_bf16(q0.z, xr + 2, a);
+            a = word_bf16(q0.w, xr + 3, a);
+            a = word_bf16(q1.x, xr + 4, a);
+            a = word_bf16(q1.y, xr + 5, a);
+            a = word_bf16(q1.z, xr + 6, a);
+            a = word_bf16(q1.w, xr + 7, a);
+            c = a.x + a.y;
+          }
+          atomicAdd(dacc + r0 + rl, c);  // slices of several tiles may be in flight
+        }
+      }
+      slot_release(S, cs, it);
+    }
+    j += (uint32_t)nsl;
+    return true;
+  };
+  for (int t = first_unit(cta, ph.rot, G); t < tps; t += G, ++kt) {
+    const int e = kt % FFN_HN;
+    for (int h = 0; h < 2; ++h, ++cs.useq, j += (uint32_t)nb) {
+      float tot;
+      float2 rp;
+      const int k = gemv_half<DT>(ph, P, S, cs, 0, t, h * HROWS, TR, j, pos, tot, rp);
+      if (k < 0) return false;
+      if (k == 0) continue;
+      const float up = __shfl_xor_sync(0xffffffffu, tot, 1);
+      if (lane < HROWS && (lane & 1) == 0) hb[e * 16 + h * 8 + (lane >> 1)] = tot / (1.0f + expf(-tot)) * up;
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        atomicAdd(hcnt + e, 1);
+      }
+    }
+    // the previous tile's down slice follows this tile's gate/up blocks
+    if (kt > 0 && !down(kt - 1)) return false;
+  }
+  if (kt > 0 && !down(kt - 1)) return false;
+  cs.it += j;
+  // every warp's partial outputs are in dacc: add them to the residual
+  if (!cta_sync(S, cs, P.err)) return false;
+  if (kt > 0) {
+    float4* out = reinterpret_cast<float4*>(ph.out);
+    for (int n4 = cs.ctid; n4 < d / 4; n4 += NCW * 32) {
+      float4 v = reinterpret_cast<const float4*>(dacc)[n4];
+      if (DT != DT_BF16) {
+        float f[4] = {DQ_UP, DQ_UP, DQ_UP, DQ_UP};
+        if (DT == DT_INT8) {
+          const uint2 s2 = *reinterpret_cast<const uint2*>(ph.s8b + 4 * n4);
+          f[0] *= __uint_as_float(s2.x << 16);
+          f[1] *= __uint_as_float(s2.x & 0xFFFF0000u);
+          f[2] *= __uint_as_float(s2.y << 16);
+          f[3] *= __uint_as_float(s2.y & 0xFFFF0000u);
+        }
+        v = make_float4(v.x * f[0], v.y * f[1], v.z * f[2], v.w * f[3]);
+      }
+      atomicAdd(out + n4, v);
+    }
+  }
   return true;
 }
 
@@ -1824,6 +2048,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
       else ok = gemv_phase<DT_BF16>(ph, P, S, cs, cta, pos, am);
       if (!ok) return;
       if (ph.epi == EPI_LOGITS) any_logits = true;
+    } else if (ph.kind == PH_FFN) {
+      if (!stage_x(ph, P, S, cs, cta)) return;
+      if (tr) tr[2] = gtimer();
+      bool ok;
+      if (ph.dtype == DT_INT4) ok = ffn_phase<DT_INT4>(ph, P, S, cs, cta, pos);
+      else if (ph.dtype == DT_INT8) ok = ffn_phase<DT_INT8>(ph, P, S, cs, cta, pos);
+      else ok = ffn_phase<DT_BF16>(ph, P, S, cs, cta, pos);
+      if (!ok) return;
     } else if (ph.kind == PH_ATTN) {
       if (tr) tr[2] = tr[1];
       const int nunits = attn_units(ph, P, pos, -1, nullptr);

@@ -73,12 +73,29 @@ static_assert(NSLOT % NCW == 0, "ring entries must map to a fixed warp");
 static_assert((2 * NSLOT + 1) * 8 <= 320, "mbarrier area");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr int ATT_POS_PER_SLOT = 16;
+constexpr int FFN_HN = 8;                    // SwiGLU output buffers of a PH_FFN phase (tiles in flight)
+// Slots of a down slice in a PH_FFN phase: nsl slots of DR rows, as full as
+// the slot size allows (DR a multiple of 8, so every bulk copy is 16-byte
+// sized and aligned; the last slot may hold fewer rows), int4 scale words
+// right after a slot's DR rows of codes.
+__host__ __device__ inline void ffn_split(int dt, int d, int& nsl, int& DR) {
+  const int rowb = dt == DT_INT4 ? 12 : dt == DT_INT8 ? 16 : 32;  // slot bytes per row
+  const int maxr = (SLOT_BYTES / rowb) / 8 * 8;
+  nsl = (d + maxr - 1) / maxr;
+  DR = ((d + nsl - 1) / nsl + 7) / 8 * 8;
+}
+// shared floats a PH_FFN phase needs above its input: partial outputs, SwiGLU
+// buffers and their counters
+__host__ __device__ constexpr int ffn_smem_floats(int d) { return d + FFN_HN * 16 + FFN_HN; }
 constexpr int MAX_GQ = 4;                    // q heads per kv head (GQA group)
 constexpr int MAX_M = 8;                     // rows of a verify pass
 constexpr int VTG = 4;                       // tiles per group of a multi-row GEMV phase
 
 // --------------------------------------------------------------- phases --
-enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1 };
+// PH_FFN: a dense FFN in one phase -- the gate/up GEMV (rows interleaved) and,
+// per gate/up tile, the matching 16-column slice of the down projection
+// (column-sliced copy W2), accumulated per CTA and added to the residual.
+enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1, PH_FFN = 2 };
 enum XSrc { X_NONE = 0, X_BF16 = 1, X_NORM = 2, X_EMBED_NORM = 3, X_F32 = 4 };
 enum Epi {
   EPI_STORE_BF16 = 0,
@@ -121,6 +138,9 @@ struct alignas(16) Phase {
   int epi;
   const uint8_t* W;        // packed weights
   const uint16_t* s8;      // int8 row scales
+  const uint8_t* W2;       // PH_FFN: column-sliced down projection [N2][N/2]
+  const uint16_t* s8b;     // PH_FFN: its int8 row scales
+  int N2;                  // PH_FFN: rows of the down projection (the model width)
   int xsrc;
   const void* xptr;        // bf16 or fp32 vector, or the fp32 residual for X_NORM
   const uint16_t* gain;    // RMSNorm gain
@@ -206,6 +226,8 @@ __host__ __device__ __forceinline__ bool verifying(const Params& P) { return P.t
 
 // ------------------------------------------------------------ host side --
 void set_error(const char* fmt, ...);
+long long cols_bytes(int dt, int N, int K);
+int pack_cols(int dt, const void* packed, int N, int K, void* out, cudaStream_t s);
 int cuda_fail(cudaError_t e, const char* what);
 #define GF_CUDA(call)                                        \
   do {                                                       \

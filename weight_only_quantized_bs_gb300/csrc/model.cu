@@ -17,6 +17,8 @@ struct gf_model {
     int N = 0, K = 0;
   };
   std::vector<Mat> qkv, o, gu, dn;  // per layer (MoE: gu / dn hold all experts back to back)
+  std::vector<uint8_t*> dn_cols;    // dense: column-sliced copy of dn for the fused FFN phase
+  bool ffn_fused = false;
   std::vector<uint16_t*> g_attn, g_ffn, router;
   long long gu_stride = 0, dn_stride = 0;  // MoE: bytes between experts
   Mat lm;
@@ -157,7 +159,11 @@ int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w,
   m->g_attn.resize(c.n_layers);
   m->g_ffn.resize(c.n_layers);
   m->router.resize(c.n_layers);
+  m->dn_cols.resize(c.n_layers, nullptr);
   const int E = c.n_experts;
+  // dense FFNs run as one phase when the partial down outputs fit in shared
+  // memory beside the staged input
+  m->ffn_fused = !E && c.d + ffn_smem_floats(c.d) <= KMAX && c.d % 16 == 0;
   for (int l = 0; l < c.n_layers && !rc; ++l) {
     if (!w->wqkv[l] || !w->wo[l] || !w->g_attn[l] || !w->g_ffn[l] || (E && !w->router[l])) {
       set_error("gf_model_create: null weight pointer in layer %d", l);
@@ -182,6 +188,12 @@ int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w,
       }
       if ((rc = make_mat(m, w->wgu[l], 2 * c.ffn, c.d, m->gu[l]))) break;
       if ((rc = make_mat(m, w->wd[l], c.d, c.ffn, m->dn[l]))) break;
+      if (m->ffn_fused) {
+        // the decode step streams this copy instead of dn (same bytes); the
+        // verify pass keeps using dn
+        if ((rc = dev_alloc(m->allocs, (void**)&m->dn_cols[l], (size_t)cols_bytes(wdtype, c.d, c.ffn)))) break;
+        if ((rc = pack_cols(wdtype, m->dn[l].W, c.d, c.ffn, m->dn_cols[l], nullptr))) break;
+      }
     }
     if ((rc = copy_vec(m, w->g_attn[l], c.d, &m->g_attn[l]))) break;
     if ((rc = copy_vec(m, w->g_ffn[l], c.d, &m->g_ffn[l]))) break;
@@ -229,7 +241,7 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
   const size_t cache_elems = (size_t)L * Hkv * Tmax * hd;
   const int nch_max = (G + Hkv - 1) / Hkv;
   const int E = c.n_experts;
-  const int ppl = E ? 6 : 5;  // phases per layer
+  const int ppl = E ? 6 : m->ffn_fused ? 4 : 5;  // phases per layer
   const int nph = ppl * L + 1;
   const int nbars = nph;
   const size_t nticks = (size_t)L * MAX_M * Hkv;
@@ -326,7 +338,20 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[2].xptr = kv->attn;
     P[2].epi = EPI_RESID;
     P[2].out = kv->resid;
-    if (!E) {
+    if (!E && m->ffn_fused) {
+      // gate/up + SwiGLU + down + residual in one phase
+      gemv(P[3], m->gu[l]);
+      P[3].kind = PH_FFN;
+      P[3].xsrc = X_NORM;
+      P[3].xptr = kv->resid;
+      P[3].gain = m->g_ffn[l];
+      P[3].eps = c.eps;
+      P[3].epi = EPI_SWIGLU;
+      P[3].out = kv->resid;
+      P[3].W2 = m->dn_cols[l];
+      P[3].s8b = m->dn[l].s8;
+      P[3].N2 = c.d;
+    } else if (!E) {
       // gate/up + SwiGLU
       gemv(P[3], m->gu[l]);
       P[3].xsrc = X_NORM;
@@ -401,10 +426,21 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[2].x_mstride = Hq * hd;
     P[2].out_mstride = c.d;
     if (!E) {
-      P[3] = D[3];
+      // gate/up + SwiGLU, then down + residual, as separate phases
+      gemv(P[3], m->gu[l]);
+      P[3].xsrc = X_NORM;
+      P[3].xptr = kv->resid;
+      P[3].gain = m->g_ffn[l];
+      P[3].eps = c.eps;
+      P[3].epi = EPI_SWIGLU;
+      P[3].out = kv->h;
       P[3].out_mstride = c.ffn;
-      P[4] = D[4];
+      gemv(P[4], m->dn[l]);
+      P[4].xsrc = X_F32;
+      P[4].xptr = kv->h;
       P[4].x_mstride = c.ffn;
+      P[4].epi = EPI_RESID;
+      P[4].out = kv->resid;
       P[4].out_mstride = c.d;
     } else {
       P[3] = D[3];  // router + gate/up of the union of experts

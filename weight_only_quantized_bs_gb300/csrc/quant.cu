@@ -185,6 +185,52 @@ static int grid_for_rows(int N) {
   return blocks < sms * 16 ? blocks : sms * 16;
 }
 
+// Column-sliced copy of a packed matrix, for a down projection fused behind
+// its gate/up GEMV: slice j holds columns 16j .. 16j+15 of every row, rows
+// consecutive (int4: 8 bytes = 16 codes a row, the two slices of a 32-wide
+// group followed by that group's scale/zero words, one per row; int8: 16
+// bytes a row; bf16: 32 bytes a row).  One thread per (row, slice).
+__global__ void __launch_bounds__(256) k_pack_cols(int dt, const uint8_t* __restrict__ P, int N, int K,
+                                                   uint8_t* __restrict__ out) {
+  const int C = K / per_chunk(dt), nsl = K / 16;
+  const long long total = (long long)N * nsl;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const int n = (int)(i % N), j = (int)(i / N);
+    if (dt == DT_INT4) {
+      const ChunkAddr a = chunk_addr(DT_INT4, N, C, n, j >> 1);
+      const uint2 w = *reinterpret_cast<const uint2*>(P + a.code + (j & 1) * 8);
+      uint8_t* g = out + (size_t)(j >> 1) * N * 20;
+      *reinterpret_cast<uint2*>(g + (size_t)(j & 1) * N * 8 + (size_t)n * 8) = w;
+      if ((j & 1) == 0) *reinterpret_cast<uint32_t*>(g + (size_t)N * 16 + (size_t)n * 4) =
+          *reinterpret_cast<const uint32_t*>(P + a.sz);
+    } else if (dt == DT_INT8) {
+      const ChunkAddr a = chunk_addr(DT_INT8, N, C, n, j);
+      *reinterpret_cast<uint4*>(out + ((size_t)j * N + n) * 16) = *reinterpret_cast<const uint4*>(P + a.code);
+    } else {
+      const ChunkAddr a0 = chunk_addr(DT_BF16, N, C, n, 2 * j), a1 = chunk_addr(DT_BF16, N, C, n, 2 * j + 1);
+      uint4* o = reinterpret_cast<uint4*>(out + ((size_t)j * N + n) * 32);
+      o[0] = *reinterpret_cast<const uint4*>(P + a0.code);
+      o[1] = *reinterpret_cast<const uint4*>(P + a1.code);
+    }
+  }
+}
+
+long long cols_bytes(int dt, int N, int K) {
+  return dt == DT_INT4 ? (long long)(K / 32) * N * 20 : (long long)(K / 16) * N * (dt == DT_INT8 ? 16 : 32);
+}
+
+int pack_cols(int dt, const void* packed, int N, int K, void* out, cudaStream_t s) {
+  if (K % 32 || N <= 0) {
+    set_error("column-sliced copy: K must be a multiple of 32 (got %d)", K);
+    return GF_EINVAL;
+  }
+  const long long total = (long long)N * (K / 16);
+  const int blocks = (int)((total + 255) / 256 < 65535 ? (total + 255) / 256 : 65535);
+  k_pack_cols<<<blocks, 256, 0, s>>>(dt, (const uint8_t*)packed, N, K, (uint8_t*)out);
+  GF_CUDA(cudaGetLastError());
+  return GF_OK;
+}
+
 }  // namespace gf
 
 using namespace gf;
