@@ -54,6 +54,18 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x, world, device=None):
+    """x reduced with MAX over the ranks of the default process group (the
+    slowest replica's time decides a multi-GPU number); x itself on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------- clocks -----
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
@@ -250,11 +262,7 @@ def run_ours(args):
             gf.decode_step(m, kv, tok, pos, logits, tok)
         ev1.record(stream)
         ev1.synchronize()
-        ms = ev0.elapsed_time(ev1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
         # repeat the timed loop for the clock record (not used for the number)
         if dt == args.dtype:
             for _ in range(max(1, int(1500 / max(ms, 1)))):
@@ -286,11 +294,7 @@ def run_ours(args):
             h_out.copy_(tok, non_blocking=True)
             stream.synchronize()
             h_tok[0] = h_out[0]
-        e2e_s = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
         results[dt] = {"tok_s": toks * world, "ms_per_token": ms / args.steps, "gbs": gbs,
                        "frac_of_peak": gbs / hbm_peak, "frac_of_copy": gbs / copy_gbs,
                        "bytes_per_token": alg_bytes / args.steps, "weight_bytes": wbytes,
