@@ -66,7 +66,7 @@ long long gf_packed_bytes(int wdtype, int N, int K);
  * 16 (r Lb + l)); for int4 it is followed by Rt x Lb 32-bit words s | z << 16
  * (the bf16 scale and zero of chunk (r, l)'s group) padded with zeros to a
  * multiple of 16 bytes.  Chunks hold their weights in k order: bf16 values,
- * int8 codes one byte each (two's complement), int4 codes two per byte (code
+ * int8 codes one byte each as the offset code q + 128, int4 codes two per byte (code
  * 2i in the low nibble of byte i, code 2i+1 in the high nibble).
  */
 

@@ -132,7 +132,7 @@ void orc_quant_w4g(const uint16_t* W, long N, long K, int G, uint8_t* q, uint16_
  *                int4 followed by Rt*Lb 4-byte words (s | z << 16) at
  *                4*(r*Lb + l), zero-padded to a multiple of 16 bytes
  *   chunk body = bf16: 8 values, k ascending.  int8: 16 codes, k ascending,
- *                one byte each (two's complement).  int4: byte i holds code
+ *                one byte each, stored offset binary (q + 128).  int4: byte i holds code
  *                k=2i in bits 0..3 and code k=2i+1 in bits 4..7 (as 32-bit
  *                little-endian words: word j has code 8j+i in bits 4i..4i+3). */
 enum { ORC_BF16 = 0, ORC_INT8 = 1, ORC_INT4 = 2 };
@@ -182,7 +182,7 @@ void orc_pack(int dt, long N, long K, int TR, const void* src, const uint16_t* s
             for (int i = 0; i < 8; ++i) { ch[2 * i] = (uint8_t)w[i]; ch[2 * i + 1] = (uint8_t)(w[i] >> 8); }
           } else if (dt == ORC_INT8) {
             const int8_t* c = (const int8_t*)src + n * K + k0;
-            for (int i = 0; i < 16; ++i) ch[i] = (uint8_t)c[i];
+            for (int i = 0; i < 16; ++i) ch[i] = (uint8_t)(c[i] + 128);
           } else {
             const uint8_t* c = (const uint8_t*)src + n * K + k0;
             for (int i = 0; i < 16; ++i) ch[i] = (uint8_t)((c[2 * i] & 15u) | ((c[2 * i + 1] & 15u) << 4));
@@ -216,7 +216,7 @@ void orc_unpack(int dt, long N, long K, int TR, const uint8_t* in, void* dst, ui
             for (int i = 0; i < 8; ++i) w[i] = (uint16_t)(ch[2 * i] | (ch[2 * i + 1] << 8));
           } else if (dt == ORC_INT8) {
             int8_t* c = (int8_t*)dst + n * K + k0;
-            for (int i = 0; i < 16; ++i) c[i] = (int8_t)ch[i];
+            for (int i = 0; i < 16; ++i) c[i] = (int8_t)(ch[i] - 128);
           } else {
             uint8_t* c = (uint8_t*)dst + n * K + k0;
             for (int i = 0; i < 16; ++i) {

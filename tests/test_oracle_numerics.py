@@ -164,13 +164,13 @@ def _subnormal_decode_int4(word):
 
 
 def _subnormal_decode_int8(word):
-    """int8 as the GEMV reads it: byte i (two's complement) XOR 0x80 is the
-    offset code q + 128 in bits p..p+7 of the word (i < 3, p = 8i) or of the
-    word shifted right by 8 (i = 3, p = 16), read as binary32."""
+    """int8 as the GEMV reads it: byte i is the offset code q + 128, in bits
+    p..p+7 of the word (i < 3, p = 8i) or of the word shifted right by 8
+    (i = 3, p = 16), read as binary32."""
     out = []
     for i in range(4):
         v, p = (word, 8 * i) if i < 3 else (word >> 8, 16)
-        f = np.array([(v ^ 0x80808080) & (255 << p)], dtype=np.uint32).view(np.float32)[0]
+        f = np.array([v & (255 << p)], dtype=np.uint32).view(np.float32)[0]
         out.append(int(float(f) * 2.0 ** (149 - p)) - 128)
     return out
 

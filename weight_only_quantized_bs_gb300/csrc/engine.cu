@@ -762,10 +762,9 @@ __device__ __forceinline__ float2 word_int4(const uint32_t w, const float2* x, f
   acc = ffma2(bits2(h & 0x000F0000u, h & 0x00F00000u), x[3], acc);
   return acc;
 }
-// int8: 4 consecutive codes, one byte each (two's complement; the XOR with
-// 0x80 makes the offset code c + 128).
+// int8: 4 consecutive codes, one byte each, stored as the offset code c + 128.
 __device__ __forceinline__ float2 word_int8(const uint32_t wq, const float2* x, float2 acc) {
-  const uint32_t w = wq ^ 0x80808080u, h = w >> 8;
+  const uint32_t w = wq, h = w >> 8;
   acc = ffma2(bits2(w & 0x000000FFu, w & 0x0000FF00u), x[0], acc);
   acc = ffma2(bits2(w & 0x00FF0000u, h & 0x00FF0000u), x[1], acc);
   return acc;
@@ -1735,7 +1734,7 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
                   qv[2 % WP] = bits2(wv & 0x000F0000u, wv & 0x00F00000u);
                   qv[3 % WP] = bits2(hv & 0x000F0000u, hv & 0x00F00000u);
                 } else if (DT == DT_INT8) {  // as word_int8
-                  const uint32_t w8 = wv ^ 0x80808080u, hv = w8 >> 8;
+                  const uint32_t w8 = wv, hv = w8 >> 8;
                   qv[0] = bits2(w8 & 0x000000FFu, w8 & 0x0000FF00u);
                   qv[1 % WP] = bits2(w8 & 0x00FF0000u, hv & 0x00FF0000u);
                 } else {

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) k_quant_w8(const uint16_t* __restrict__ W
             code = (int)rintf(bf2f(wb) / sv);
             code = max(-127, min(127, code));
           }
-          word |= (uint32_t)(uint8_t)(int8_t)code << (8 * i);
+          word |= (uint32_t)(code + 128) << (8 * i);  // offset binary
         }
         words[j] = word;
       }
@@ -152,8 +152,9 @@ __global__ void __launch_bounds__(256) k_unpack(int dt, const uint8_t* __restric
       const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
       if (dt == DT_BF16) {
         *reinterpret_cast<uint4*>((uint16_t*)Q + (size_t)n * K + c * 8) = v;
-      } else if (dt == DT_INT8) {
-        *reinterpret_cast<uint4*>((uint8_t*)Q + (size_t)n * K + c * 16) = v;
+      } else if (dt == DT_INT8) {  // offset binary back to two's complement
+        *reinterpret_cast<uint4*>((uint8_t*)Q + (size_t)n * K + c * 16) =
+            make_uint4(v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u);
       } else {
         uint8_t* q = (uint8_t*)Q + (size_t)n * K + c * 32;
         for (int j = 0; j < 4; ++j) {
