@@ -128,8 +128,11 @@ def measured_traffic(workload, dtype):
         return None
     with open(p) as f:
         rec = json.load(f)
-    src = os.path.join(ROOT, "weight_only_quantized_bs_gb300", "csrc", "engine.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("engine.cu", "gf_internal.cuh"):  # the sources of k_engine
+        with open(os.path.join(ROOT, "weight_only_quantized_bs_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()[:16]
     r = rec.get("%s/%s" % (workload, dtype))
     if not r or r.get("engine_sha") != sha:
         return None

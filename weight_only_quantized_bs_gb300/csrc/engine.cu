@@ -424,11 +424,21 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
       const int tps = ph.N / TR, d = ph.N2;
       int nsl, DR;
       ffn_split(dt, d, nsl, DR);
+      // an empty slot: completed by the arrival alone
+      auto empty_slot = [&]() {
+        uint8_t* dst;
+        uint64_t* fb;
+        if ((ok = prod_slot(S, pr, err, dst, fb))) mbar_arrive(fb);
+      };
       // the down slice of a tile follows the next tile's gate/up blocks, so
       // that its SwiGLU outputs are ready when its rows arrive
       auto down_slice = [&](int t) {
         for (int k = 0; k < nsl && ok; ++k) {
-          const int r0 = k * DR, nr = min(DR, d - r0);  // > 0 (ffn_split)
+          const int r0 = k * DR, nr = min(DR, d - r0);
+          if (nr <= 0) {
+            empty_slot();
+            continue;
+          }
           const uint8_t* src;
           const uint8_t* szs = nullptr;
           uint32_t cb;
@@ -536,17 +546,14 @@ __device__ __forceinline__ bool cta_sync(const Smem& S, Cons& cs, int* err) {
   return ok != 0;
 }
 
+// Every lane waits on the slot's barrier itself (each lane's completed wait
+// orders its reads of the slot after the copy).
 __device__ __forceinline__ bool slot_acquire(const Smem& S, Cons& cs, uint32_t it, int* err, const uint8_t*& base) {
   const uint32_t slot = it % NSLOT, par = (it / NSLOT) & 1u;
-  int ok = 1;
-  if (cs.lane == 0) {
-    if (cs.warp == 0 && !mbar_probe(&S.full[slot], par)) ++cs.starved;
-    ok = mbar_wait(&S.full[slot], par, err, ERR_WAIT_FULL);
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok && cs.lane) mbar_test(&S.full[slot], par);
+  if (cs.warp == 0 && cs.lane == 0 && !mbar_probe(&S.full[slot], par)) ++cs.starved;
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&S.full[slot], par, err, ERR_WAIT_FULL));
   base = S.ring + slot * SLOT_BYTES;
-  return ok != 0;
+  return ok;
 }
 __device__ __forceinline__ void slot_release(const Smem& S, const Cons& cs, uint32_t it) {
   __syncwarp();
@@ -1067,6 +1074,40 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
   return true;
 }
 
+// One row of a down slot (DR rows of 16 columns: the SwiGLU outputs of one
+// gate/up tile) against those outputs, staged as the subnormal
+// dequantisation reads them (xr; xz: their sum for the int4 zeros, or 128
+// times it for the int8 offset), without the 2^64 and int8 row scale that the
+// phase end applies.
+template <int DT>
+__device__ __forceinline__ float down_row(const uint8_t* base, int rl, int DR, const float2* xr, float xz) {
+  if (DT == DT_INT4) {
+    const uint2 q = reinterpret_cast<const uint2*>(base)[rl];
+    const uint32_t sz = reinterpret_cast<const uint32_t*>(base + (size_t)DR * 8)[rl];
+    const float2 a0 = word_int4(q.x, xr, make_float2(0.f, 0.f));
+    const float2 a1 = word_int4(q.y, xr + 4, make_float2(0.f, 0.f));
+    return fmaf(__uint_as_float(sz << 16), (a0.x + a1.x) + (a0.y + a1.y), __uint_as_float(sz & 0xFFFF0000u) * xz);
+  } else if (DT == DT_INT8) {
+    const uint4 q = reinterpret_cast<const uint4*>(base)[rl];
+    float2 a0 = word_int8(q.x, xr, make_float2(0.f, 0.f));
+    float2 a1 = word_int8(q.z, xr + 4, make_float2(0.f, 0.f));
+    a0 = word_int8(q.y, xr + 2, a0);
+    a1 = word_int8(q.w, xr + 6, a1);
+    return ((a0.x + a1.x) + (a0.y + a1.y)) - xz;
+  } else {
+    const uint4 q0 = reinterpret_cast<const uint4*>(base)[2 * rl], q1 = reinterpret_cast<const uint4*>(base)[2 * rl + 1];
+    float2 a0 = word_bf16(q0.x, xr, make_float2(0.f, 0.f));
+    float2 a1 = word_bf16(q1.x, xr + 4, make_float2(0.f, 0.f));
+    a0 = word_bf16(q0.y, xr + 1, a0);
+    a1 = word_bf16(q1.y, xr + 5, a1);
+    a0 = word_bf16(q0.z, xr + 2, a0);
+    a1 = word_bf16(q1.z, xr + 6, a1);
+    a0 = word_bf16(q0.w, xr + 3, a0);
+    a1 = word_bf16(q1.w, xr + 7, a1);
+    return (a0.x + a1.x) + (a0.y + a1.y);
+  }
+}
+
 // A dense FFN in one phase (PH_FFN).  For each of this CTA's gate/up tiles
 // (round-robin): the two half-tiles as in a GEMV phase, whose combining warps
 // write silu(gate) * up of their 8 pairs into a shared buffer instead of
@@ -1084,11 +1125,24 @@ __device__ bool ffn_phase(const Phase& ph, const Params& P, const Smem& S, Cons&
   int nsl, DR;
   ffn_split(DT, d, nsl, DR);
   const int lane = cs.lane, w = cs.warp;
-  float* dacc = S.xs + ph.K;  // [d] this CTA's partial down outputs
-  float* hb = dacc + d;       // [FFN_HN][16] SwiGLU outputs of the tiles in flight
+  // The CTA's partial down outputs.  int8 / bf16 slots add in turn with plain
+  // adds (below), into two buffers where they fit (local tile kp into buffer
+  // kp % nbuf); int4 slots, whose tiles span fewer slots, use shared atomic
+  // adds into one buffer (measured faster on this path; the order of the adds
+  // then varies, the sum only by rounding).
+  constexpr bool ORDERED = DT != DT_INT4;
+  const int nbuf = ORDERED && ph.K + d + ffn_smem_floats(d) <= KMAX ? 2 : 1;
+  float* dacc = S.xs + ph.K;   // [nbuf][d]
+  float* hb = dacc + nbuf * d;  // [FFN_HN][16] SwiGLU outputs of the tiles in flight
   int* hcnt = reinterpret_cast<int*>(hb + FFN_HN * 16);  // [FFN_HN] half-tiles finished per buffer
-  for (int i = cs.ctid; i < d; i += NCW * 32) dacc[i] = 0.0f;
+  // dturn[b][k]: tiles of buffer b whose down slot k has been added; the
+  // buffer's next tile waits for it, so each row of a buffer is added to by
+  // one warp at a time, tile after tile (plain adds, a fixed order), while
+  // with two buffers consecutive tiles never wait for each other
+  int* dturn = hcnt + FFN_HN;  // [2][FFN_MAXSL]
+  for (int i = cs.ctid; i < nbuf * d; i += NCW * 32) dacc[i] = 0.0f;
   if (cs.ctid < FFN_HN) hcnt[cs.ctid] = 0;
+  if (cs.ctid < 2 * FFN_MAXSL) dturn[cs.ctid] = 0;
   if (!cta_sync(S, cs, P.err)) return false;
   uint32_t j = 0;
   int kt = 0;  // this CTA's tiles so far
@@ -1137,40 +1191,58 @@ __device__ bool ffn_phase(const Phase& ph, const Params& P, const Smem& S, Cons&
       const uint32_t it = cs.it + j + (uint32_t)k;
       const uint8_t* base;
       if (!slot_acquire(S, cs, it, P.err, base)) return false;
-      const int r0 = k * DR, nr = min(DR, d - r0);
-#pragma unroll 4
-      for (int i = 0; i < (DR + 31) / 32; ++i) {
-        const int rl = lane + 32 * i;
-        if (rl < nr) {
-          float2 a = make_float2(0.f, 0.f);
-          float c;
-          if (DT == DT_INT4) {
-            const uint2 q = reinterpret_cast<const uint2*>(base)[rl];
-            a = word_int4(q.x, xr, a);
-            a = word_int4(q.y, xr + 4, a);
-            const uint32_t sz = reinterpret_cast<const uint32_t*>(base + (size_t)DR * 8)[rl];
-            c = fmaf(__uint_as_float(sz << 16), a.x + a.y, __uint_as_float(sz & 0xFFFF0000u) * xz);
-          } else if (DT == DT_INT8) {
-            const uint4 q = reinterpret_cast<const uint4*>(base)[rl];
-            a = word_int8(q.x, xr, a);
-            a = word_int8(q.y, xr + 2, a);
-            a = word_int8(q.z, xr + 4, a);
-            a = word_int8(q.w, xr + 6, a);
-            c = (a.x + a.y) - xz;
-          } else {
-            const uint4 q0 = reinterpret_cast<const uint4*>(base)[2 * rl], q1 = reinterpret_cast<const uint4*>(base)[2 * rl + 1];
-            a = word_bf16(q0.x, xr, a);
-            a = word_bf16(q0.y, xr + 1, a);
-            a = word_bf16(q0.z, xr + 2, a);
-            a = word_bf16(q0.w, xr + 3, a);
-            a = word_bf16(q1.x, xr + 4, a);
-            a = word_bf16(q1.y, xr + 5, a);
-            a = word_bf16(q1.z, xr + 6, a);
-            a = word_bf16(q1.w, xr + 7, a);
-            c = a.x + a.y;
+      // the buffer's previous tile has added its slot k (bounded wait)
+      const int bsel = kp % nbuf, turn = kp / nbuf;
+      float* acc = dacc + bsel * d;
+      int* tp = dturn + bsel * FFN_MAXSL + k;
+      if (ORDERED && lane == 0) {
+        volatile int* c = tp;
+        if (*c != turn) {
+          const uint64_t t0 = gtimer();
+          while (*c != turn) {
+            __nanosleep(32);
+            if (gtimer() - t0 > WAIT_NS) {
+              atomicCAS(P.err, 0, ERR_WAIT_COMBINE);
+              ok = 0;
+              break;
+            }
           }
-          atomicAdd(dacc + r0 + rl, c);  // slices of several tiles may be in flight
         }
+        __threadfence_block();
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      const int r0 = k * DR, nr = min(DR, d - r0);
+      if (!ORDERED) {
+#pragma unroll 4
+        for (int i = 0; i * 32 < nr; ++i) {
+          const int rl = lane + 32 * i;
+          if (rl < nr) atomicAdd(acc + r0 + rl, down_row<DT>(base, rl, DR, xr, xz));
+        }
+      }
+      // groups of four rows per lane: their loads (codes, scales and the
+      // partial outputs, which no other warp touches now) go out first
+      for (int i0 = 0; ORDERED && i0 * 32 < nr; i0 += 4) {
+        float c[4], a0[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rl = lane + 32 * (i0 + u);
+          c[u] = 0.f;
+          a0[u] = 0.f;
+          if (rl < nr) {
+            a0[u] = acc[r0 + rl];
+            c[u] = down_row<DT>(base, rl, DR, xr, xz);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rl = lane + 32 * (i0 + u);
+          if (rl < nr) acc[r0 + rl] = a0[u] + c[u];
+        }
+      }
+      __syncwarp();
+      if (ORDERED && lane == 0) {
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(tp) = turn + 1;
       }
       slot_release(S, cs, it);
     }
@@ -1204,6 +1276,10 @@ __device__ bool ffn_phase(const Phase& ph, const Params& P, const Smem& S, Cons&
     float4* out = reinterpret_cast<float4*>(ph.out);
     for (int n4 = cs.ctid; n4 < d / 4; n4 += NCW * 32) {
       float4 v = reinterpret_cast<const float4*>(dacc)[n4];
+      if (nbuf == 2) {
+        const float4 v1 = reinterpret_cast<const float4*>(dacc + d)[n4];
+        v = make_float4(v.x + v1.x, v.y + v1.y, v.z + v1.z, v.w + v1.w);
+      }
       if (DT != DT_BF16) {
         float f[4] = {DQ_UP, DQ_UP, DQ_UP, DQ_UP};
         if (DT == DT_INT8) {

@@ -78,6 +78,7 @@ constexpr int FFN_HN = 8;                    // SwiGLU output buffers of a PH_FF
 // the slot size allows (DR a multiple of 8, so every bulk copy is 16-byte
 // sized and aligned; the last slot may hold fewer rows), int4 scale words
 // right after a slot's DR rows of codes.
+constexpr int FFN_MAXSL = 32;                // most down slots per tile
 __host__ __device__ inline void ffn_split(int dt, int d, int& nsl, int& DR) {
   const int rowb = dt == DT_INT4 ? 12 : dt == DT_INT8 ? 16 : 32;  // slot bytes per row
   const int maxr = (SLOT_BYTES / rowb) / 8 * 8;
@@ -85,8 +86,8 @@ __host__ __device__ inline void ffn_split(int dt, int d, int& nsl, int& DR) {
   DR = ((d + nsl - 1) / nsl + 7) / 8 * 8;
 }
 // shared floats a PH_FFN phase needs above its input: partial outputs, SwiGLU
-// buffers and their counters
-__host__ __device__ constexpr int ffn_smem_floats(int d) { return d + FFN_HN * 16 + FFN_HN; }
+// buffers and their counters, the down slots' turn counters
+__host__ __device__ constexpr int ffn_smem_floats(int d) { return d + FFN_HN * 16 + FFN_HN + 2 * FFN_MAXSL; }
 constexpr int MAX_GQ = 4;                    // q heads per kv head (GQA group)
 constexpr int MAX_M = 8;                     // rows of a verify pass
 constexpr int VTG = 4;                       // tiles per group of a multi-row GEMV phase

@@ -162,8 +162,10 @@ int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w,
   m->dn_cols.resize(c.n_layers, nullptr);
   const int E = c.n_experts;
   // dense FFNs run as one phase when the partial down outputs fit in shared
-  // memory beside the staged input
-  m->ffn_fused = !E && c.d + ffn_smem_floats(c.d) <= KMAX && c.d % 16 == 0;
+  // memory beside the staged input and a down slice takes few enough slots
+  int nsl = 0, DR = 0;
+  ffn_split(wdtype, c.d, nsl, DR);
+  m->ffn_fused = !E && c.d + ffn_smem_floats(c.d) <= KMAX && c.d % 16 == 0 && nsl <= FFN_MAXSL;
   for (int l = 0; l < c.n_layers && !rc; ++l) {
     if (!w->wqkv[l] || !w->wo[l] || !w->g_attn[l] || !w->g_ffn[l] || (E && !w->router[l])) {
       set_error("gf_model_create: null weight pointer in layer %d", l);
