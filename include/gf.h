@@ -101,7 +101,11 @@ int gf_unpack_bf16(const void* packed, int N, int K, void* W, gf_stream stream);
  * size 1: y[n] = sum_k x[k] What[n,k], fp32 accumulation, What = W (bf16),
  * q s_n (int8) or q s + z (int4 G=32).  x: bf16 [K].  y: [N] bf16 (rounded to
  * nearest even) or fp32, by ydtype.  Weights stream through shared memory by
- * bulk asynchronous copies; codes are dequantised in registers. */
+ * bulk asynchronous copies; codes are dequantised in registers.
+ * Input range (int8, int4): the codes are read as subnormal floats and the
+ * inputs staged multiplied by powers of two up to 2^85, so |x[k]| must stay
+ * below 2^43 (larger inputs overflow to inf); inputs below about 2^-60 in
+ * magnitude lose relative precision gradually.  bf16 has no such limit. */
 int gf_gemv_bf16(const void* x, const void* Wpacked, int N, int K, void* y, int ydtype,
                  gf_stream stream);
 int gf_gemv_w8(const void* x, const void* qpacked, const void* s, int N, int K, void* y,
