@@ -13,7 +13,14 @@ host memory and the argmax read back every step.  The model (4.1-13.5 GB) is
 far larger than L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--dtype int4|int8|bf16]
-                  [--impl ours|reference] [--workload llama2-7b|llama3.1-8b]
+                  [--impl ours|reference] [--workload llama2-7b|llama3.1-8b|mixtral-8x7b]
+                  [--ctx L1,L2,...] [--verify-k K]
+
+--ctx times the decode from contexts of L positions written straight into the
+KV cache (seeded bf16 N(0, 1) rows; the Llama-3.1-8B sweep uses 128, 1024 and
+8192), --verify-k adds speculative-verification passes of K draft tokens after
+the decode measurement (drafts = the model's own greedy continuation, all
+accepted, and uniform random drafts, about none accepted).
 """
 import argparse
 import json
@@ -42,7 +49,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--dtype", default="int4", choices=["int4", "int8", "bf16"])
-    ap.add_argument("--workload", default="llama2-7b", choices=["llama2-7b", "llama3.1-8b", "gemv-set", "gemv"])
+    ap.add_argument("--workload", default="llama2-7b",
+                    choices=["llama2-7b", "llama3.1-8b", "mixtral-8x7b", "gemv-set", "gemv"])
+    ap.add_argument("--ctx", default="", help="comma-separated context lengths written into the KV cache")
+    ap.add_argument("--verify-k", type=int, default=0, help="also time verification passes of k drafts")
     ap.add_argument("--only-headline", action="store_true", help="skip the other two weight dtypes")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
@@ -177,6 +187,82 @@ def oracle_sampler(cfg, dtype, seed, n_layers_sample):
     return sample
 
 
+# ------------------------------------------------- decode variants -----
+class _DevPtr:
+    """A device address where the binding expects a tensor."""
+
+    def __init__(self, p):
+        self.p = p
+
+    def data_ptr(self):
+        return self.p
+
+
+def fill_context(gf, kv, cfg, seed, ctx, tmax, dev):
+    """Writes a context of ctx positions (seeded bf16 N(0, 1) K and V rows)
+    straight into every layer's KV cache, [kv head][tmax][head_dim] per layer."""
+    import numpy as np
+    import torch
+    from synth import models
+    kp, vp = kv.cache_ptrs()
+    Hkv, hd = cfg["n_kv_heads"], cfg["head_dim"]
+    layer_bytes = Hkv * tmax * hd * 2
+    for l in range(cfg["n_layers"]):
+        k, v = models.kv_prefill(cfg, seed, l, ctx)
+        for src, base in ((k, kp), (v, vp)):
+            full = np.zeros((Hkv, tmax, hd), dtype=np.uint16)
+            full[:, :ctx, :] = src
+            t = torch.from_numpy(full.view(np.int16)).to(dev)
+            gf.copy_ceiling(t, _DevPtr(base + l * layer_bytes), layer_bytes)
+    torch.cuda.synchronize()
+
+
+def measure_verify(gf, m, kv, cfg, prompt, k, rounds, seed, dev):
+    """Verification passes of k drafts (gf_verify_k, k + 1 rows per pass) after
+    the prompt: `rounds` passes whose drafts are the model's own greedy
+    continuation (each pass accepts all k when no near-tie flips a token),
+    then `rounds` passes with uniform random drafts (about none accepted).
+    Returns the time per pass and the tokens each pass yields (accepted + 1)."""
+    import numpy as np
+    import torch
+    tok = torch.zeros(1, dtype=torch.int32, device=dev)
+    pos = torch.zeros(1, dtype=torch.int32, device=dev)
+    logits = torch.empty(cfg["vocab"], dtype=torch.float32, device=dev)
+    seq = [int(t) for t in prompt]
+    for t in prompt:
+        tok.fill_(int(t))
+        gf.decode_step(m, kv, tok, pos, logits, tok)
+    seq.append(int(tok.item()))
+    while len(seq) < N_PROMPT + rounds * (k + 1) + 1:
+        gf.decode_step(m, kv, tok, pos, logits, tok)
+        seq.append(int(tok.item()))
+    starts = [N_PROMPT + r * (k + 1) for r in range(rounds)]
+    rng = np.random.default_rng(seed)
+
+    def passes(rows):
+        pos_r = [torch.tensor([p], dtype=torch.int32, device=dev) for p in starts]
+        tok_r = [torch.tensor(r_, dtype=torch.int32, device=dev) for r_ in rows]
+        n_r = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in starts]
+        x_r = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in starts]
+        warm = torch.tensor([starts[0]], dtype=torch.int32, device=dev)
+        gf.verify_k(m, kv, tok_r[0], k, warm, n_r[0], x_r[0])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        e0.record()
+        for r in range(rounds):
+            gf.verify_k(m, kv, tok_r[r], k, pos_r[r], n_r[r], x_r[r])
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / rounds
+        acc = float(np.mean([int(n.item()) for n in n_r]))
+        return {"ms_per_pass": round(ms, 4), "accepted_per_pass": acc, "tok_s": round((acc + 1) / (ms * 1e-3), 2)}
+
+    greedy = passes([seq[p:p + k + 1] for p in starts])
+    rand = passes([[seq[p]] + [int(x) for x in rng.integers(0, cfg["vocab"], k)] for p in starts])
+    return {"k": k, "passes": rounds, "greedy_drafts": greedy, "random_drafts": rand,
+            "device_error": gf.device_error()}
+
+
 # ------------------------------------------------------------ our arm -----
 def run_ours(args):
     import numpy as np
@@ -201,7 +287,8 @@ def run_ours(args):
     cfg = models.config(args.workload)
     if args.layers:
         cfg["n_layers"] = args.layers
-    tmax = 2048
+    ctxs = [int(c) for c in args.ctx.split(",") if c]
+    tmax = 2048 if not ctxs else max(ctxs) + max(args.warmup, N_PROMPT) + args.steps + 8
     dtypes = [args.dtype] if args.only_headline else [d for d in ("int4", "int8", "bf16")
                                                        if args.workload == "llama2-7b" or d != "int4"]
     if args.dtype not in dtypes:
@@ -238,6 +325,9 @@ def run_ours(args):
     sampler = ClockSampler(local)
     results = {}
     stream = torch.cuda.current_stream()
+    L, Hkv, hd = cfg["n_layers"], cfg["n_kv_heads"], cfg["head_dim"]
+    row = 2 * L * Hkv * hd * 2   # K and V bytes of one position, all layers
+    clocks = None
     for dt in dtypes:
         m = gf.Model(cfg, dt, glob, layers)
         kv = gf.KV(m, tmax)
@@ -245,63 +335,80 @@ def run_ours(args):
         tok = torch.zeros(1, dtype=torch.int32, device=dev)
         pos = torch.zeros(1, dtype=torch.int32, device=dev)
         logits = torch.empty(cfg["vocab"], dtype=torch.float32, device=dev)
-        # warm-up: the prompt, one token per step, then greedy steps
-        n_warm = max(args.warmup, N_PROMPT)
-        for i in range(n_warm):
-            if i < N_PROMPT:
-                tok.fill_(int(prompt[i]))
-            gf.decode_step(m, kv, tok, pos, logits, tok)   # argmax -> next token
-        torch.cuda.synchronize()
-        p0 = int(pos.item())
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        if dt == args.dtype:
-            sampler.start()
-            time.sleep(0.3)
-        ev0, ev1 = torch.cuda.Event(True), torch.cuda.Event(True)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            gf.decode_step(m, kv, tok, pos, logits, tok)
-        ev1.record(stream)
-        ev1.synchronize()
-        ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-        # repeat the timed loop for the clock record (not used for the number)
-        if dt == args.dtype:
-            for _ in range(max(1, int(1500 / max(ms, 1)))):
-                for _ in range(args.steps):
+        per_ctx = {}
+        for ci, ctx in enumerate(ctxs or [None]):
+            if ctx is None:
+                # warm-up: the prompt, one token per step, then greedy steps
+                for i in range(max(args.warmup, N_PROMPT)):
+                    if i < N_PROMPT:
+                        tok.fill_(int(prompt[i]))
+                    gf.decode_step(m, kv, tok, pos, logits, tok)   # argmax -> next token
+            else:
+                # a context of ctx positions written into the cache, then greedy steps
+                fill_context(gf, kv, cfg, args.seed, ctx, tmax, dev)
+                pos.fill_(ctx)
+                tok.fill_(int(prompt[0]))
+                for i in range(args.warmup):
                     gf.decode_step(m, kv, tok, pos, logits, tok)
-                torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            p0 = int(pos.item())
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            head = dt == args.dtype and ci == 0
+            if head:
+                sampler.start()
+                time.sleep(0.3)
+            ev0, ev1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            ev0.record(stream)
+            for _ in range(args.steps):
+                gf.decode_step(m, kv, tok, pos, logits, tok)
+            ev1.record(stream)
+            ev1.synchronize()
+            ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+            # repeat the timed loop for the clock record (not used for the number)
+            if head:
+                for _ in range(max(1, int(1500 / max(ms, 1)))):
+                    for _ in range(args.steps):
+                        gf.decode_step(m, kv, tok, pos, logits, tok)
+                    torch.cuda.synchronize()
+                    pos.fill_(p0)
+                clocks = sampler.stop()
+            err = gf.device_error()
+            # algorithmic bytes: weights + KV rows 0..pos read + one row written, per token
+            kv_bytes = sum(row * (p + 1) + row for p in range(p0, p0 + args.steps))
+            alg_bytes = wbytes * args.steps + kv_bytes
+            toks = args.steps / (ms * 1e-3)
+            gbs = alg_bytes / (ms * 1e-3) / 1e9
+            rec = {"tok_s": toks * world, "ms_per_token": ms / args.steps, "gbs": gbs,
+                   "frac_of_peak": gbs / hbm_peak, "frac_of_copy": gbs / copy_gbs,
+                   "bytes_per_token": alg_bytes / args.steps, "weight_bytes": wbytes, "device_error": err}
+            if ctx is not None:
+                rec["ctx"] = ctx
+            if ci == 0:
+                # end to end through the C-ABI: token in from pinned host memory,
+                # argmax out to pinned host memory, every step
                 pos.fill_(p0)
-            clocks = sampler.stop()
-        err = gf.device_error()
-        # algorithmic bytes: weights + KV rows 0..pos read + one row written, per token
-        L, Hkv, hd = cfg["n_layers"], cfg["n_kv_heads"], cfg["head_dim"]
-        row = 2 * L * Hkv * hd * 2
-        kv_bytes = sum(row * (p + 1) + row for p in range(p0, p0 + args.steps))
-        alg_bytes = wbytes * args.steps + kv_bytes
-        toks = args.steps / (ms * 1e-3)
-        gbs = alg_bytes / (ms * 1e-3) / 1e9
-
-        # end to end through the C-ABI: token in from pinned host memory,
-        # argmax out to pinned host memory, every step
-        pos.fill_(p0)
-        h_tok = torch.zeros(1, dtype=torch.int32).pin_memory()
-        h_out = torch.zeros(1, dtype=torch.int32).pin_memory()
-        h_tok[0] = int(prompt[-1])
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            tok.copy_(h_tok, non_blocking=True)
-            gf.decode_step(m, kv, tok, pos, logits, tok)
-            h_out.copy_(tok, non_blocking=True)
-            stream.synchronize()
-            h_tok[0] = h_out[0]
-        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
-        results[dt] = {"tok_s": toks * world, "ms_per_token": ms / args.steps, "gbs": gbs,
-                       "frac_of_peak": gbs / hbm_peak, "frac_of_copy": gbs / copy_gbs,
-                       "bytes_per_token": alg_bytes / args.steps, "weight_bytes": wbytes,
-                       "e2e_tok_s": args.steps / e2e_s * world, "device_error": err}
+                h_tok = torch.zeros(1, dtype=torch.int32).pin_memory()
+                h_out = torch.zeros(1, dtype=torch.int32).pin_memory()
+                h_tok[0] = int(prompt[-1])
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                for _ in range(args.steps):
+                    tok.copy_(h_tok, non_blocking=True)
+                    gf.decode_step(m, kv, tok, pos, logits, tok)
+                    h_out.copy_(tok, non_blocking=True)
+                    stream.synchronize()
+                    h_tok[0] = h_out[0]
+                e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+                rec["e2e_tok_s"] = args.steps / e2e_s * world
+            per_ctx[ctx] = rec
+        res = dict(per_ctx[(ctxs or [None])[0]])
+        if ctxs:
+            res["per_ctx"] = {str(c): per_ctx[c] for c in ctxs}
+        if args.verify_k:
+            res["verify"] = measure_verify(gf, m, kv, cfg, prompt, args.verify_k, 20, args.seed, dev)
+        results[dt] = res
         kv.close()
         m.close()
         torch.cuda.synchronize()
