@@ -415,6 +415,8 @@ def run_ours(args):
     del layers, glob
 
     head = results[args.dtype]
+    # first timed position (the headline context, after the warm-up steps)
+    p_first = ctxs[0] + args.warmup if ctxs else max(args.warmup, N_PROMPT)
     out = {
         "metric": METRIC,
         "value": round(head["tok_s"], 2),
@@ -431,9 +433,8 @@ def run_ours(args):
         "data": "synthetic (seeded random-init weights, uniform random prompt)",
         "config": {"workload": "%s-shaped greedy decode, %s weights" % (args.workload, args.dtype),
                    "model": args.workload, "n_layers": cfg["n_layers"], "weights": args.dtype + ("-g32" if args.dtype == "int4" else ""),
-                   "global_batch": 1, "prompt": N_PROMPT, "tmax": tmax,
-                   "positions": [N_PROMPT if args.warmup <= N_PROMPT else args.warmup,
-                                 max(args.warmup, N_PROMPT) + args.steps],
+                   "global_batch": 1, "prompt": 1 if ctxs else N_PROMPT, "tmax": tmax,
+                   "positions": [p_first, p_first + args.steps],
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: the model's %d MB stream per step is far above L2" %
                          int(head["weight_bytes"] / 1e6)},
@@ -453,6 +454,8 @@ def run_ours(args):
         "clocks": clocks,
         "setup_s": round(gen_s, 1),
     }
+    if ctxs:
+        out["config"]["contexts"] = ctxs
     if rank == 0 and not args.no_cpu_baseline:
         sample = oracle_sampler(cfg, args.dtype, args.seed, n_layers_sample=2)
         ts, spent = [], 0.0
