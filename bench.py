@@ -187,6 +187,17 @@ def oracle_sampler(cfg, dtype, seed, n_layers_sample):
     return sample
 
 
+# ------------------------------------------------- byte accounting -----
+def decode_bytes(cfg, weight_bytes, p0, steps):
+    """Algorithmic bytes of `steps` decode tokens at positions p0 .. p0 +
+    steps - 1: per token the model's streamed weight bytes (gf_model_weight_bytes:
+    linear weights incl. lm_head, scales, norm gains, one embedding row) plus
+    the bf16 K and V rows 0..pos of every layer read and the row at pos
+    written."""
+    row = 2 * cfg["n_layers"] * cfg["n_kv_heads"] * cfg["head_dim"] * 2  # K and V of one position
+    return weight_bytes * steps + sum(row * (p + 1) + row for p in range(p0, p0 + steps))
+
+
 # ------------------------------------------------- decode variants -----
 class _DevPtr:
     """A device address where the binding expects a tensor."""
@@ -325,8 +336,6 @@ def run_ours(args):
     sampler = ClockSampler(local)
     results = {}
     stream = torch.cuda.current_stream()
-    L, Hkv, hd = cfg["n_layers"], cfg["n_kv_heads"], cfg["head_dim"]
-    row = 2 * L * Hkv * hd * 2   # K and V bytes of one position, all layers
     clocks = None
     for dt in dtypes:
         m = gf.Model(cfg, dt, glob, layers)
@@ -376,8 +385,7 @@ def run_ours(args):
                 clocks = sampler.stop()
             err = gf.device_error()
             # algorithmic bytes: weights + KV rows 0..pos read + one row written, per token
-            kv_bytes = sum(row * (p + 1) + row for p in range(p0, p0 + args.steps))
-            alg_bytes = wbytes * args.steps + kv_bytes
+            alg_bytes = decode_bytes(cfg, wbytes, p0, args.steps)
             toks = args.steps / (ms * 1e-3)
             gbs = alg_bytes / (ms * 1e-3) / 1e9
             rec = {"tok_s": toks * world, "ms_per_token": ms / args.steps, "gbs": gbs,
