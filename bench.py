@@ -440,8 +440,8 @@ def run_ours(args):
         "dtype": "f32",
         "data": "synthetic (seeded random-init weights, uniform random prompt)",
         "config": {"workload": "%s-shaped greedy decode, %s weights" % (args.workload, args.dtype),
-                   "model": args.workload, "n_layers": cfg["n_layers"], "weights": args.dtype + ("-g32" if args.dtype == "int4" else ""),
-                   "global_batch": 1, "prompt": 1 if ctxs else N_PROMPT, "tmax": tmax,
+                   "shapes": args.workload, "n_layers": cfg["n_layers"], "weights": args.dtype + ("-g32" if args.dtype == "int4" else ""),
+                   "batch": 1, "prompt": 1 if ctxs else N_PROMPT, "tmax": tmax,
                    "positions": [p_first, p_first + args.steps],
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: the model's %d MB stream per step is far above L2" %
@@ -574,9 +574,9 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded random-init weights)",
         "config": {"workload": "%s-shaped greedy decode, %s weights" % (args.workload, args.dtype),
-                   "model": args.workload, "n_layers": cfg["n_layers"],
+                   "shapes": args.workload, "n_layers": cfg["n_layers"],
                    "weights": args.dtype + ("-g32" if args.dtype == "int4" else ""),
-                   "global_batch": 1, "prompt": N_PROMPT, "tmax": 2048,
+                   "batch": 1, "prompt": N_PROMPT, "tmax": 2048,
                    "positions": [N_PROMPT if args.warmup <= N_PROMPT else args.warmup,
                                  max(args.warmup, N_PROMPT) + args.steps],
                    "parallelism": "single", "l2": "not applicable (the oracle runs on the host)"},
