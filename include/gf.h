@@ -1,8 +1,8 @@
 /*
  * gf.h — C-ABI of libgf, a GB300 (sm_103a) engine for the batch-size-1
  * decode step of Llama-style transformers with bf16, int8 weight-only and
- * int4 group-32 weight-only linear layers (the workload of the gpt-fast
- * README, sections "Benchmarks" and "Quantization").
+ * int4 grouped (G = 32, 64, 128) weight-only linear layers (the workload of
+ * the gpt-fast README, sections "Benchmarks" and "Quantization").
  *
  * Conventions for every call below:
  *  - Return value: 0 (GF_OK) or a gf_status code; gf_last_error() returns a
@@ -17,8 +17,8 @@
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *    asynchronous on that stream unless stated; errors raised inside a kernel
  *    (a bounded wait that gave up) are reported by gf_device_error().
- *  - K must be a multiple of 8 (bf16), 16 (int8) or 32 (int4 G=32), and at
- *    most GF_KMAX; otherwise GF_EINVAL.
+ *  - K must be a multiple of 8 (bf16), 16 (int8) or 32 (int4, and of its
+ *    group size G), and at most GF_KMAX; otherwise GF_EINVAL.
  */
 #ifndef GF_H_
 #define GF_H_
@@ -52,46 +52,47 @@ const char* gf_last_error(void);
 int gf_version(void);
 
 /* Size in bytes of a packed weight buffer for an N x K matrix of `wdtype`
- * (the device tile layout below), or -1 for a bad argument. */
+ * (the device layout below; int4 with G = 32), or -1 for a bad argument. */
 long long gf_packed_bytes(int wdtype, int N, int K);
 
 /*
- * Packed tile layout (the "offline weight repack into a 128-bit-vectorised,
- * coalesced tile layout").  A chunk is 16 bytes of one row: 8 bf16, 16 int8
- * or 32 int4 weights, C = K / (weights per chunk) chunks per row.  Rows are
- * grouped in tiles of GF_TILE_ROWS (the last tile may hold fewer, Rt), tiles
- * are stored one after another, and inside a tile K-blocks of up to 32 chunks
- * (Lb chunks; only the last block of a row may be narrower) one after
- * another.  A block holds its Rt x Lb chunks row-major (chunk (r, l) at byte
- * 16 (r Lb + l)); for int4 it is followed by Rt x Lb 32-bit words s | z << 16
- * (the bf16 scale and zero of chunk (r, l)'s group) padded with zeros to a
- * multiple of 16 bytes.  Chunks hold their weights in k order: bf16 values,
- * int8 codes one byte each as the offset code q + 128, int4 codes two per byte (code
- * 2i in the low nibble of byte i, code 2i+1 in the high nibble).
+ * Device layout of the weights ("offline weight repack"; the kernels load
+ * boxes of 32 rows x 128 bytes of it with the tensor-memory accelerator,
+ * which lays each box out in shared memory with the 128-byte swizzle, so the
+ * matrices keep their logical row-major order in memory):
+ *  - bf16: the matrix itself, [N][K] 16-bit values.
+ *  - int8: [N][K] bytes, the offset code q + 128.
+ *  - int4 (group G): [N][K/2] bytes, byte i of a row = code 2i in the low
+ *    nibble, code 2i+1 in the high nibble; then, from byte
+ *    round_up(N K / 2, 256), the scale/zero words [K/G][Np] (32 bits each,
+ *    s | z << 16, bf16 scale and zero of (row, group); Np = N rounded up to 32,
+ *    the padding rows zero).  gf_packed_bytes_w4g() gives the size.
  */
+long long gf_packed_bytes_w4g(int N, int K, int G);
 
 /* int8 weight-only quantisation (gpt-fast README, "Int8 weight-only
  * quantization"): per output row n, s_n = bf16(max_k |W[n,k]| / 127) (fp32
  * divide) and q = clamp(rint(W / s_n), -127, 127) (fp32 divide, ties to
  * even); an all-zero row gets s = 0, q = 0.
  * W: bf16 [N][K] row-major.  packed: gf_packed_bytes(GF_W_INT8, N, K) bytes
- * in the tile layout.  s: bf16 [N]. */
+ * in the device layout.  s: bf16 [N]. */
 int gf_quantize_w8(const void* W, int N, int K, void* packed, void* s, gf_stream stream);
 
-/* int4 weight-only grouped quantisation, group G = 32 along K (gpt-fast
- * README, "Int4 weight-only quantization", --groupsize 32): per row and group
+/* int4 weight-only grouped quantisation, group G along K (gpt-fast README,
+ * "Int4 weight-only quantization", --groupsize): per row and group
  * z = min (bf16, exact), s = bf16((max - min) / 15) (fp32 subtract and
  * divide), q = clamp(rint((W - min) / s), 0, 15) (fp32); s == 0 gives q = 0.
- * The dequantised weight is q s + z.  packed receives codes, s and z in the
- * tile layout.  G must be 32. */
+ * The dequantised weight is q s + z.  packed (gf_packed_bytes_w4g bytes)
+ * receives codes, s and z in the device layout.  G must be 32, 64 or 128 and
+ * divide K (GF_EUNSUPPORTED otherwise). */
 int gf_quantize_w4g(const void* W, int N, int K, int G, void* packed, gf_stream stream);
 
-/* bf16 weights into the tile layout (no arithmetic). */
+/* bf16 weights into the device layout (a copy: the layout is the matrix). */
 int gf_repack_bf16(const void* W, int N, int K, void* packed, gf_stream stream);
 
 /* Inverses of the above, for bit-exact checks: packed -> logical.
  * gf_unpack_w8: q int8 [N][K].  gf_unpack_w4g: q uint8 [N][K] (one code per
- * byte), s, z bf16 [N][K/32].  gf_unpack_bf16: W bf16 [N][K]. */
+ * byte), s, z bf16 [N][K/G].  gf_unpack_bf16: W bf16 [N][K]. */
 int gf_unpack_w8(const void* packed, int N, int K, void* q, gf_stream stream);
 int gf_unpack_w4g(const void* packed, int N, int K, int G, void* q, void* s, void* z,
                   gf_stream stream);
@@ -99,9 +100,10 @@ int gf_unpack_bf16(const void* packed, int N, int K, void* W, gf_stream stream);
 
 /* Matrix-vector products y = x W^T of the pages' linear layers at batch
  * size 1: y[n] = sum_k x[k] What[n,k], fp32 accumulation, What = W (bf16),
- * q s_n (int8) or q s + z (int4 G=32).  x: bf16 [K].  y: [N] bf16 (rounded to
- * nearest even) or fp32, by ydtype.  Weights stream through shared memory by
- * bulk asynchronous copies; codes are dequantised in registers.
+ * q s_n (int8) or q s + z (int4, group G = 32, 64 or 128).  x: bf16 [K].
+ * y: [N] bf16 (rounded to nearest even) or fp32, by ydtype.  Weights stream
+ * through shared memory by tensor-memory-accelerator copies; codes are
+ * dequantised in registers, one output row per lane.
  * Input range (int8, int4): the codes are read as subnormal floats and the
  * inputs staged multiplied by powers of two up to 2^85, so |x[k]| must stay
  * below 2^43 (larger inputs overflow to inf); inputs below about 2^-60 in
@@ -138,9 +140,11 @@ int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq
  * head rounded up to 256)
  * return GF_EINVAL with the size in gf_last_error().  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  Every call
- * shares the one array: calls that overlap on the same GPU (for example from two
- * streams at once) race and give wrong results; serialise them.  No cudaMalloc / cudaFree is made. */
+ * device current and keeps it for the life of the process (a cudaDeviceReset
+ * would move the array: do not call this again after one); make that first
+ * call before any stream capture.  Every call shares the one array: calls
+ * that overlap on the same GPU (for example from two streams at once) race
+ * and give wrong results; serialise them.  No cudaMalloc / cudaFree is made. */
 #define GF_NOALLOC_ATTN_SCRATCH (2 << 20)
 int gf_decode_attn_noalloc(const void* q, const void* kcache, const void* vcache, int Hq, int Hkv, int hd,
                            int Tmax, int pos, void* out, gf_stream stream);
@@ -157,6 +161,7 @@ typedef struct {
   int n_experts;   /* 0 = dense FFN; else a top-2 mixture of experts */
   float eps;       /* RMSNorm epsilon */
   double theta;    /* RoPE base */
+  int group_size;  /* int4 weights: group size along K, 32, 64 or 128 (0 = 32) */
 } gf_model_config;
 
 /* Weights as bf16 device arrays owned by the caller (read during
@@ -196,6 +201,11 @@ long long gf_model_weight_bytes(const gf_model* m);
  * scratch and the decode program, for contexts of up to Tmax positions. */
 int gf_kv_create(gf_model* m, int Tmax, gf_kv** out);
 int gf_kv_destroy(gf_kv* kv);
+/* Clears the cache for a new context without allocating: zeroes every K and V
+ * row and the engine's step counters (asynchronous on `stream`).  The
+ * position lives with the caller (the device int32 passed as d_pos to
+ * gf_decode_step / gf_verify_k): set it to 0 to start again from position 0. */
+int gf_kv_reset(gf_kv* kv, gf_stream stream);
 /* Device pointers of the K and V caches (for tests that pre-fill them). */
 int gf_kv_cache_ptrs(gf_kv* kv, void** kcache, void** vcache);
 
@@ -237,7 +247,11 @@ int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t*
                 int32_t* d_n_accepted, int32_t* d_next_token, float* d_logits, gf_stream stream);
 
 /* Reads and clears the device error word of the engine (0 = none; otherwise
- * a code naming the wait that gave up).  Synchronises the device. */
+ * a code naming the wait that gave up, or 7 / 8 for a position / token id
+ * that a kernel refused).  Synchronises the device.  The word is shared by
+ * every call in the process.  The library keeps per-device state (the
+ * addresses of its device variables, kernel attributes) for the life of the
+ * process: do not use it again on a device after cudaDeviceReset. */
 int gf_device_error(void);
 
 /* Device-to-device copy at full bandwidth (16-byte vector loads and stores),

@@ -55,7 +55,7 @@ def lib():
         L.orc_packed_bytes.restype = lg
         L.orc_pack.argtypes = [i32, lg, lg, i32, vp, vp, vp, vp]
         L.orc_unpack.argtypes = [i32, lg, lg, i32, vp, vp, vp, vp]
-        L.orc_linear.argtypes = [i32, lg, lg, vp, vp, vp, vp, lg, vp]
+        L.orc_linear.argtypes = [i32, lg, lg, i32, vp, vp, vp, vp, lg, vp]
         L.orc_attention.argtypes = [i32, i32, i32, lg, vp, vp, vp, vp]
         L.orc_rmsnorm.argtypes = [vp, vp, lg, dbl, vp]
         L.orc_rope.argtypes = [vp, i32, i32, lg, dbl]
@@ -121,32 +121,39 @@ def quant_w4g(W, G=32):
     return q, s, z
 
 
+def group_of(q, s):
+    """Group size of int4 codes q [N, K] with per-group scales s [N, K/G]."""
+    return q.shape[1] // s.shape[1]
+
+
 def dequant(dt, q, s=None, z=None):
-    """The dequantised weight as fp64 (exact): q*s (int8), q*s+z (int4 G=32)."""
+    """The dequantised weight as fp64 (exact): q*s (int8), q*s+z (int4, the
+    group size read off the shapes of q and s)."""
     if dt == BF16:
         return bf16_to_double(q)
     if dt == INT8:
         return q.astype(np.float64) * bf16_to_double(s)[:, None]
-    sd = np.repeat(bf16_to_double(s), 32, axis=1)
-    zd = np.repeat(bf16_to_double(z), 32, axis=1)
+    G = group_of(q, s)
+    sd = np.repeat(bf16_to_double(s), G, axis=1)
+    zd = np.repeat(bf16_to_double(z), G, axis=1)
     return q.astype(np.float64) * sd + zd
 
 
 # --------------------------------------------------------------- layout --
-def packed_bytes(dt, N, K, TR):
-    return int(lib().orc_packed_bytes(dt, N, K, TR))
+def packed_bytes(dt, N, K, G=32):
+    return int(lib().orc_packed_bytes(dt, N, K, G))
 
 
-def pack(dt, N, K, TR, src, s=None, z=None):
-    out = np.empty(packed_bytes(dt, N, K, TR), dtype=np.uint8)
+def pack(dt, N, K, src, s=None, z=None, G=32):
+    out = np.empty(packed_bytes(dt, N, K, G), dtype=np.uint8)
     src = np.ascontiguousarray(src)
     s = None if s is None else _c(s, np.uint16)
     z = None if z is None else _c(z, np.uint16)
-    lib().orc_pack(dt, N, K, TR, _p(src), _p(s), _p(z), _p(out))
+    lib().orc_pack(dt, N, K, G, _p(src), _p(s), _p(z), _p(out))
     return out
 
 
-def unpack(dt, N, K, TR, packed):
+def unpack(dt, N, K, packed, G=32):
     packed = _c(packed, np.uint8)
     if dt == BF16:
         dst = np.empty((N, K), dtype=np.uint16)
@@ -156,15 +163,16 @@ def unpack(dt, N, K, TR, packed):
         dst = np.empty((N, K), dtype=np.uint8)
     s = z = None
     if dt == INT4:
-        s = np.empty((N, K // 32), dtype=np.uint16)
-        z = np.empty((N, K // 32), dtype=np.uint16)
-    lib().orc_unpack(dt, N, K, TR, _p(packed), _p(dst), _p(s), _p(z))
+        s = np.empty((N, K // G), dtype=np.uint16)
+        z = np.empty((N, K // G), dtype=np.uint16)
+    lib().orc_unpack(dt, N, K, G, _p(packed), _p(dst), _p(s), _p(z))
     return dst, s, z
 
 
 # --------------------------------------------------------------- linear --
 def linear(dt, w, s, z, X):
-    """Y[t] = X[t] . What^T in fp64; X [T, K] (or [K]); w = W / codes [N, K]."""
+    """Y[t] = X[t] . What^T in fp64; X [T, K] (or [K]); w = W / codes [N, K];
+    for int4 the group size is K / (columns of s)."""
     w = np.ascontiguousarray(w)
     N, K = w.shape
     X = _c(X, np.float64)
@@ -173,7 +181,8 @@ def linear(dt, w, s, z, X):
     Y = np.empty((X2.shape[0], N), dtype=np.float64)
     s = None if s is None else _c(s, np.uint16)
     z = None if z is None else _c(z, np.uint16)
-    lib().orc_linear(dt, N, K, _p(w), _p(s), _p(z), _p(X2), X2.shape[0], _p(Y))
+    G = group_of(w, s) if dt == INT4 else 32
+    lib().orc_linear(dt, N, K, G, _p(w), _p(s), _p(z), _p(X2), X2.shape[0], _p(Y))
     return Y[0] if one else Y
 
 

@@ -23,9 +23,10 @@ from . import (BF16, INT4, INT8, argmax, attention, bf16_to_double, linear, quan
 
 
 class _Mat:
-    """One weight matrix as the method stores it: bf16, int8 + s, int4 + s + z."""
+    """One weight matrix as the method stores it: bf16, int8 + s, int4 + s + z
+    (group size G along K)."""
 
-    def __init__(self, dt, W):
+    def __init__(self, dt, W, G=32):
         self.dt = dt
         self.N, self.K = W.shape
         if dt == BF16:
@@ -34,7 +35,7 @@ class _Mat:
             self.w, self.s = quant_w8(W)
             self.z = None
         else:
-            self.w, self.s, self.z = quant_w4g(W, 32)
+            self.w, self.s, self.z = quant_w4g(W, G)
 
     def __call__(self, X):
         return linear(self.dt, self.w, self.s, self.z, X)
@@ -42,10 +43,12 @@ class _Mat:
 
 class OracleModel:
     """fp64 decoder.  `weights` is a synth.models.WeightCache-like object
-    (`.glob`, `.layer(l)`).  Quantised layers are kept when `keep` is set."""
+    (`.glob`, `.layer(l)`).  Quantised layers are kept when `keep` is set.
+    int4 weights use the group size cfg["group"] (32 when absent)."""
 
     def __init__(self, cfg, dtype, weights, tmax, keep=True):
         self.cfg, self.weights, self.keep = cfg, weights, keep
+        self.G = int(cfg.get("group", 32))
         self.dt = {"bf16": BF16, "int8": INT8, "int4": INT4}[dtype] if isinstance(dtype, str) else dtype
         self.tmax = tmax
         c = cfg
@@ -56,24 +59,25 @@ class OracleModel:
         g = weights.glob
         self.embed = g["embed"]
         self.g_final = g["g_final"]
-        self.lm_head = _Mat(self.dt, g["lm_head"])
+        self.lm_head = _Mat(self.dt, g["lm_head"], self.G)
 
     def _layer(self, l):
         if l in self._layers:
             return self._layers[l]
         w = self.weights.layer(l)
-        L = {"wq": _Mat(self.dt, w["wq"]), "wk": _Mat(self.dt, w["wk"]),
-             "wv": _Mat(self.dt, w["wv"]), "wo": _Mat(self.dt, w["wo"]),
+        G = self.G
+        L = {"wq": _Mat(self.dt, w["wq"], G), "wk": _Mat(self.dt, w["wk"], G),
+             "wv": _Mat(self.dt, w["wv"], G), "wo": _Mat(self.dt, w["wo"], G),
              "g_attn": w["g_attn"], "g_ffn": w["g_ffn"]}
         if "experts" in w:
             # The router stays bf16: the pages quantise linear weights, and a
             # gate of 8 outputs carries no measurable bytes (READING).
             L["router"] = _Mat(BF16, w["router"])
-            L["experts"] = [{k: _Mat(self.dt, e[k]) for k in ("wg", "wu", "wd")}
+            L["experts"] = [{k: _Mat(self.dt, e[k], G) for k in ("wg", "wu", "wd")}
                             for e in w["experts"]]
         else:
             for k in ("wg", "wu", "wd"):
-                L[k] = _Mat(self.dt, w[k])
+                L[k] = _Mat(self.dt, w[k], G)
         if self.keep:
             self._layers[l] = L
         return L

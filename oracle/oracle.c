@@ -120,38 +120,40 @@ void orc_quant_w4g(const uint16_t* W, long N, long K, int G, uint8_t* q, uint16_
   }
 }
 
-/* ------------------------------------------------ packed tile layout ---- */
-/* The device layout ("offline weight repack into a 128-bit-vectorised,
- * coalesced tile layout"), restated from its definition:
- *   chunk      = 16 bytes of one row: E = 8 (bf16), 16 (int8), 32 (int4) weights
- *   C          = K / E chunks per row; K-block b holds chunks [32b, 32b+Lb),
- *                Lb = min(32, C - 32b)
- *   row tile t = rows [t*TR, min(N, t*TR + TR)), Rt rows; tiles are stored one
- *                after another, and inside a tile its K-blocks one after another
- *   block      = Rt*Lb code chunks, chunk (r, l) at byte 16*(r*Lb + l); for
- *                int4 followed by Rt*Lb 4-byte words (s | z << 16) at
- *                4*(r*Lb + l), zero-padded to a multiple of 16 bytes
- *   chunk body = bf16: 8 values, k ascending.  int8: 16 codes, k ascending,
- *                one byte each, stored offset binary (q + 128).  int4: byte i holds code
- *                k=2i in bits 0..3 and code k=2i+1 in bits 4..7 (as 32-bit
- *                little-endian words: word j has code 8j+i in bits 4i..4i+3). */
+/* ------------------------------------------------------ packed layout ---- */
+/* The device layout of each weight type, restated from its definition: the
+ * matrix is cut into slots of 32 rows (a tile) by 256 bytes of each row's
+ * code bytes (a K-slot), stored one after another, tile-major (slot of tile
+ * t, K-slot b at index t * nb + b, nb = ceil(row bytes / 256)).  A slot is
+ * 128-byte lines: line h * 32 + r (h = 0, 1) holds bytes
+ * [256 b + 128 h, 256 b + 128 h + 128) of the code bytes of row 32 t + r;
+ * int4 slots add lines 64 + g (g < 512 / G), whose 32-bit word r is
+ * s | z << 16 for row 32 t + r and group (512 / G) b + g.  Inside line L the
+ * 16-byte unit u is stored at unit u XOR (L mod 8).  Bytes past a row, past
+ * the last row or past the last group are zero.
+ *   code bytes of a row: bf16 values (2 bytes each, little endian); int8
+ *   q + 128 (offset binary); int4 byte i = q[2i] | q[2i+1] << 4. */
 enum { ORC_BF16 = 0, ORC_INT8 = 1, ORC_INT4 = 2 };
 
-static int per_chunk(int dt) { return dt == ORC_BF16 ? 8 : dt == ORC_INT8 ? 16 : 32; }
+static long row_bytes(int dt, long K) { return dt == ORC_BF16 ? 2 * K : dt == ORC_INT8 ? K : K / 2; }
+static long slot_size(int dt, int G) { return 8192 + (dt == ORC_INT4 ? (512 / G) * 128 : 0); }
+static long nslots_k(int dt, long K) { return (row_bytes(dt, K) + 255) / 256; }
+/* byte b of line L of a slot, with the units of the line swizzled */
+static long line_pos(long L, long b) { return L * 128 + (((b / 16) ^ (L % 8)) * 16) + b % 16; }
 
-static long block_bytes(int dt, long Rt, long Lb) {
-  long b = Rt * Lb * 16;
-  if (dt == ORC_INT4) b += ((Rt * Lb * 4 + 15) / 16) * 16;
-  return b;
+long orc_packed_bytes(int dt, long N, long K, int G) {
+  return (N + 31) / 32 * nslots_k(dt, K) * slot_size(dt, G);
 }
 
-long orc_packed_bytes(int dt, long N, long K, int TR) {
-  long C = K / per_chunk(dt), total = 0;
-  for (long r0 = 0; r0 < N; r0 += TR) {
-    long Rt = (N - r0 < TR) ? N - r0 : TR;
-    for (long c0 = 0; c0 < C; c0 += 32) total += block_bytes(dt, Rt, (C - c0 < 32) ? C - c0 : 32);
-  }
-  return total;
+/* position in the packed buffer of code byte j of row n */
+static long code_pos(int dt, long K, int G, long n, long j) {
+  long t = n / 32, r = n % 32, b = j / 256, h = (j % 256) / 128;
+  return (t * nslots_k(dt, K) + b) * slot_size(dt, G) + line_pos(h * 32 + r, j % 128);
+}
+/* position of the scale/zero word of (row n, group g) */
+static long sz_pos(long K, int G, long n, long g) {
+  long gps = 512 / G, t = n / 32, r = n % 32;
+  return (t * nslots_k(ORC_INT4, K) + g / gps) * slot_size(ORC_INT4, G) + line_pos(64 + g % gps, 4 * r);
 }
 
 static void put32(uint8_t* p, uint32_t v) {
@@ -161,88 +163,71 @@ static uint32_t get32(const uint8_t* p) {
   return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
 }
 
+/* code byte j of row n, from the logical source */
+static uint8_t code_byte(int dt, long K, const void* src, long n, long j) {
+  if (dt == ORC_BF16) {
+    uint16_t w = ((const uint16_t*)src)[n * K + j / 2];
+    return (uint8_t)(j % 2 ? w >> 8 : w);
+  }
+  if (dt == ORC_INT8) return (uint8_t)(((const int8_t*)src)[n * K + j] + 128);
+  const uint8_t* c = (const uint8_t*)src + n * K + 2 * j;
+  return (uint8_t)((c[0] & 15u) | ((c[1] & 15u) << 4));
+}
+
 /* src: bf16 W [N][K] (uint16), int8 codes [N][K], or int4 codes [N][K] one per
- * byte; s,z: int4 [N][K/32] bf16 (ignored otherwise). */
-void orc_pack(int dt, long N, long K, int TR, const void* src, const uint16_t* s,
+ * byte; s, z: int4 [N][K/G] bf16 (ignored otherwise). */
+void orc_pack(int dt, long N, long K, int G, const void* src, const uint16_t* s,
               const uint16_t* z, uint8_t* out) {
-  long E = per_chunk(dt), C = K / E, off = 0, ng = K / 32;
-  for (long r0 = 0; r0 < N; r0 += TR) {
-    long Rt = (N - r0 < TR) ? N - r0 : TR;
-    for (long c0 = 0; c0 < C; c0 += 32) {
-      long Lb = (C - c0 < 32) ? C - c0 : 32;
-      uint8_t* blk = out + off;
-      memset(blk, 0, (size_t)block_bytes(dt, Rt, Lb));
-      for (long r = 0; r < Rt; ++r) {
-        long n = r0 + r;
-        for (long l = 0; l < Lb; ++l) {
-          long k0 = (c0 + l) * E;
-          uint8_t* ch = blk + 16 * (r * Lb + l);
-          if (dt == ORC_BF16) {
-            const uint16_t* w = (const uint16_t*)src + n * K + k0;
-            for (int i = 0; i < 8; ++i) { ch[2 * i] = (uint8_t)w[i]; ch[2 * i + 1] = (uint8_t)(w[i] >> 8); }
-          } else if (dt == ORC_INT8) {
-            const int8_t* c = (const int8_t*)src + n * K + k0;
-            for (int i = 0; i < 16; ++i) ch[i] = (uint8_t)(c[i] + 128);
-          } else {
-            const uint8_t* c = (const uint8_t*)src + n * K + k0;
-            for (int i = 0; i < 16; ++i) ch[i] = (uint8_t)((c[2 * i] & 15u) | ((c[2 * i + 1] & 15u) << 4));
-            long g = k0 / 32;
-            put32(blk + Rt * Lb * 16 + 4 * (r * Lb + l),
-                  (uint32_t)s[n * ng + g] | ((uint32_t)z[n * ng + g] << 16));
-          }
-        }
-      }
-      off += block_bytes(dt, Rt, Lb);
-    }
+  memset(out, 0, (size_t)orc_packed_bytes(dt, N, K, G));
+  long rb = row_bytes(dt, K);
+  for (long n = 0; n < N; ++n)
+    for (long j = 0; j < rb; ++j) out[code_pos(dt, K, G, n, j)] = code_byte(dt, K, src, n, j);
+  if (dt == ORC_INT4) {
+    long ng = K / G;
+    for (long n = 0; n < N; ++n)
+      for (long g = 0; g < ng; ++g)
+        put32(out + sz_pos(K, G, n, g), (uint32_t)s[n * ng + g] | ((uint32_t)z[n * ng + g] << 16));
   }
 }
 
 /* Inverse of orc_pack (used only to show the layout is a bijection). */
-void orc_unpack(int dt, long N, long K, int TR, const uint8_t* in, void* dst, uint16_t* s,
+void orc_unpack(int dt, long N, long K, int G, const uint8_t* in, void* dst, uint16_t* s,
                 uint16_t* z) {
-  long E = per_chunk(dt), C = K / E, off = 0, ng = K / 32;
-  for (long r0 = 0; r0 < N; r0 += TR) {
-    long Rt = (N - r0 < TR) ? N - r0 : TR;
-    for (long c0 = 0; c0 < C; c0 += 32) {
-      long Lb = (C - c0 < 32) ? C - c0 : 32;
-      const uint8_t* blk = in + off;
-      for (long r = 0; r < Rt; ++r) {
-        long n = r0 + r;
-        for (long l = 0; l < Lb; ++l) {
-          long k0 = (c0 + l) * E;
-          const uint8_t* ch = blk + 16 * (r * Lb + l);
-          if (dt == ORC_BF16) {
-            uint16_t* w = (uint16_t*)dst + n * K + k0;
-            for (int i = 0; i < 8; ++i) w[i] = (uint16_t)(ch[2 * i] | (ch[2 * i + 1] << 8));
-          } else if (dt == ORC_INT8) {
-            int8_t* c = (int8_t*)dst + n * K + k0;
-            for (int i = 0; i < 16; ++i) c[i] = (int8_t)(ch[i] - 128);
-          } else {
-            uint8_t* c = (uint8_t*)dst + n * K + k0;
-            for (int i = 0; i < 16; ++i) {
-              c[2 * i] = (uint8_t)(ch[i] & 15u);
-              c[2 * i + 1] = (uint8_t)(ch[i] >> 4);
-            }
-            uint32_t v = get32(blk + Rt * Lb * 16 + 4 * (r * Lb + l));
-            s[n * ng + k0 / 32] = (uint16_t)v;
-            z[n * ng + k0 / 32] = (uint16_t)(v >> 16);
-          }
-        }
+  long rb = row_bytes(dt, K);
+  for (long n = 0; n < N; ++n)
+    for (long j = 0; j < rb; ++j) {
+      uint8_t v = in[code_pos(dt, K, G, n, j)];
+      if (dt == ORC_BF16) {
+        uint16_t* w = (uint16_t*)dst + n * K + j / 2;
+        *w = (uint16_t)(j % 2 ? (*w & 0x00FF) | (v << 8) : (*w & 0xFF00) | v);
+      } else if (dt == ORC_INT8) {
+        ((int8_t*)dst)[n * K + j] = (int8_t)(v - 128);
+      } else {
+        uint8_t* c = (uint8_t*)dst + n * K + 2 * j;
+        c[0] = (uint8_t)(v & 15u);
+        c[1] = (uint8_t)(v >> 4);
       }
-      off += block_bytes(dt, Rt, Lb);
     }
+  if (dt == ORC_INT4) {
+    long ng = K / G;
+    for (long n = 0; n < N; ++n)
+      for (long g = 0; g < ng; ++g) {
+        uint32_t v = get32(in + sz_pos(K, G, n, g));
+        s[n * ng + g] = (uint16_t)v;
+        z[n * ng + g] = (uint16_t)(v >> 16);
+      }
   }
 }
 
 /* ---------------------------------------------------------- linear ---- */
 /* Y[t][n] = sum_k X[t][k] * What[n][k] for t < T, in fp64, k ascending, with
- * What = W (bf16), q*s_n (int8) or q*s_{n,g} + z_{n,g} (int4, g = k/32): the
+ * What = W (bf16), q*s_n (int8) or q*s_{n,g} + z_{n,g} (int4, g = k/G): the
  * product y = x W^T of the pages' linear layers, against the dequantised
  * weight. */
-void orc_linear(int dt, long N, long K, const void* w, const uint16_t* s, const uint16_t* z,
+void orc_linear(int dt, long N, long K, int G, const void* w, const uint16_t* s, const uint16_t* z,
                 const double* X, long T, double* Y) {
   double* row = (double*)malloc(sizeof(double) * (size_t)K);
-  long ng = K / 32;
+  long ng = K / G;
   for (long n = 0; n < N; ++n) {
     for (long k = 0; k < K; ++k) {
       if (dt == ORC_BF16) {
@@ -250,7 +235,7 @@ void orc_linear(int dt, long N, long K, const void* w, const uint16_t* s, const 
       } else if (dt == ORC_INT8) {
         row[k] = (double)((const int8_t*)w)[n * K + k] * (double)orc_f32_from_bf16(s[n]);
       } else {
-        long g = k / 32;
+        long g = k / G;
         row[k] = (double)((const uint8_t*)w)[n * K + k] * (double)orc_f32_from_bf16(s[n * ng + g]) +
                  (double)orc_f32_from_bf16(z[n * ng + g]);
       }

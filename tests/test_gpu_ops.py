@@ -38,7 +38,7 @@ def test_quantize_w8_bit_exact(N, K):
     packed, s = gf.quantize_w8(to_dev(W))
     q_ref, s_ref = _q8(W)
     assert np.array_equal(bf16_host(s), s_ref)
-    assert np.array_equal(packed.cpu().numpy(), oracle.pack(oracle.INT8, N, K, gf.TILE_ROWS, q_ref))
+    assert np.array_equal(packed.cpu().numpy(), oracle.pack(oracle.INT8, N, K, q_ref))
     assert np.array_equal(gf.unpack_w8(packed, N, K).cpu().numpy(), q_ref)
 
 
@@ -48,7 +48,7 @@ def test_quantize_w4g_bit_exact(N, K):
     W[0, :32] = W[0, 5]                     # a degenerate group
     packed = gf.quantize_w4g(to_dev(W))
     q_ref, s_ref, z_ref = oracle.quant_w4g(W)
-    assert np.array_equal(packed.cpu().numpy(), oracle.pack(oracle.INT4, N, K, gf.TILE_ROWS, q_ref, s_ref, z_ref))
+    assert np.array_equal(packed.cpu().numpy(), oracle.pack(oracle.INT4, N, K, q_ref, s_ref, z_ref))
     q, s, z = gf.unpack_w4g(packed, N, K)
     assert np.array_equal(q.cpu().numpy(), q_ref)
     assert np.array_equal(bf16_host(s), s_ref) and np.array_equal(bf16_host(z), z_ref)
@@ -58,7 +58,7 @@ def test_quantize_w4g_bit_exact(N, K):
 def test_repack_bf16_bit_exact(N, K):
     W = weights(N, K, 13)
     packed = gf.repack_bf16(to_dev(W))
-    assert np.array_equal(packed.cpu().numpy(), oracle.pack(oracle.BF16, N, K, gf.TILE_ROWS, W))
+    assert np.array_equal(packed.cpu().numpy(), oracle.pack(oracle.BF16, N, K, W))
     assert np.array_equal(bf16_host(gf.unpack_bf16(packed, N, K)), W)
 
 

@@ -130,20 +130,33 @@ def _golden_rows():
             line = line.strip()
             if line and not line.startswith("#"):
                 parts = line.split()
-                rows.append((parts[0], int(parts[1]), int(parts[2]), [int(p, 0) for p in parts[3:]]))
+                words = []
+                for p in parts[4:]:
+                    if "*" in p:
+                        n, v = p.split("*")
+                        words += [int(v, 0)] * int(n)
+                    else:
+                        words.append(int(p, 0))
+                rows.append((parts[0], int(parts[1]), int(parts[2]), int(parts[3]), words))
     return rows
 
 
 def test_layout_hand_words():
-    for kind, N, K, words in _golden_rows():
+    rows = _golden_rows()
+    assert [r[0] for r in rows] == ["int4", "int4", "int8"]
+    for kind, N, K, G, words in rows:
         if kind == "int4":
-            codes = (np.arange(K) % 16).astype(np.uint8).reshape(N, K)
-            s = np.full((N, K // 32), 0x3E04, np.uint16)
-            z = np.zeros((N, K // 32), np.uint16)
-            packed = oracle.pack(oracle.INT4, N, K, 32, codes, s, z)
+            codes = ((np.arange(K)[None, :] + np.arange(N)[:, None]) % 16).astype(np.uint8)
+            if G == 32:
+                s = np.full((N, K // G), 0x3E04, np.uint16)
+                z = np.zeros((N, K // G), np.uint16)
+            else:
+                s = (0x3C00 + np.arange(N)[:, None] + np.zeros((1, K // G), np.int64)).astype(np.uint16)
+                z = (0xBC00 + np.arange(N)[:, None] + np.zeros((1, K // G), np.int64)).astype(np.uint16)
+            packed = oracle.pack(oracle.INT4, N, K, codes, s, z, G=G)
         else:
-            codes = np.array([-1, 2, -3, 4] * (K // 4), np.int8).reshape(N, K)
-            packed = oracle.pack(oracle.INT8, N, K, 32, codes)
+            codes = np.array([-1, 2, -3, 4] * (N * K // 4), np.int8).reshape(N, K)
+            packed = oracle.pack(oracle.INT8, N, K, codes)
         assert list(packed.view("<u4")) == words
 
 
@@ -175,31 +188,42 @@ def _subnormal_decode_int8(word):
     return out
 
 
+def _unswizzle(words, line):
+    """The 32 words of slot line `line`, with its 16-byte units put back in
+    order (unit u is stored at unit u XOR (line mod 8))."""
+    raw = words[line * 32:(line + 1) * 32].reshape(8, 4)
+    return np.concatenate([raw[u ^ (line % 8)] for u in range(8)])
+
+
 def test_layout_views_recover_codes():
     rng = np.random.default_rng(1)
     codes = rng.integers(0, 16, size=(3, 64)).astype(np.uint8)
     s = rng.integers(0, 1 << 16, size=(3, 2)).astype(np.uint16)
     z = rng.integers(0, 1 << 16, size=(3, 2)).astype(np.uint16)
-    packed = oracle.pack(oracle.INT4, 3, 64, 32, codes, s, z)
+    packed = oracle.pack(oracle.INT4, 3, 64, codes, s, z)
     words = packed.view("<u4")
-    # 3 rows x 2 chunks x 4 words of codes, then 6 scale words (+2 pad words)
+    # one slot: row r's 32 code bytes open line r; the scale lines start at
+    # line 64, group g's line holding row r's word r
     for r in range(3):
-        for c in range(2):
-            got = []
-            for j in range(4):
-                got += _subnormal_decode_int4(int(words[(r * 2 + c) * 4 + j]))
-            assert got == list(codes[r, 32 * c:32 * c + 32])
-    sz = words[24:30]
-    assert list(sz & 0xFFFF) == list(s.reshape(-1)) and list(sz >> 16) == list(z.reshape(-1))
+        line = _unswizzle(words, r)
+        got = []
+        for j in range(8):
+            got += _subnormal_decode_int4(int(line[j]))
+        assert got == list(codes[r])
+    for g in range(2):
+        line = _unswizzle(words, 64 + g)
+        assert list(line[:3] & 0xFFFF) == list(s[:, g]) and list(line[:3] >> 16) == list(z[:, g])
+        assert not line[3:].any()
     codes8 = rng.integers(-127, 128, size=(2, 32)).astype(np.int8)
-    words8 = oracle.pack(oracle.INT8, 2, 32, 32, codes8).view("<u4")
-    got8 = [c for w in words8 for c in _subnormal_decode_int8(int(w))]
+    words8 = oracle.pack(oracle.INT8, 2, 32, codes8).view("<u4")
+    got8 = [c for r in range(2) for w in _unswizzle(words8, r)[:8] for c in _subnormal_decode_int8(int(w))]
     assert got8 == list(codes8.reshape(-1))
 
 
-@pytest.mark.parametrize("dt,N,K", [(0, 45, 8 * 40), (1, 70, 16 * 37), (2, 33, 32 * 45),
-                                    (2, 64, 4096), (1, 1, 16), (0, 31, 8)])
-def test_layout_bijection(dt, N, K):
+@pytest.mark.parametrize("dt,N,K,G", [(0, 45, 8 * 40, 32), (1, 70, 16 * 37, 32), (2, 33, 32 * 45, 32),
+                                      (2, 64, 4096, 32), (2, 45, 128 * 3, 128), (2, 7, 64 * 5, 64),
+                                      (1, 1, 16, 32), (0, 31, 8, 32)])
+def test_layout_bijection(dt, N, K, G):
     rng = np.random.default_rng(dt * 1000 + N)
     if dt == 0:
         src = rng.integers(0, 1 << 16, size=(N, K)).astype(np.uint16)
@@ -209,17 +233,21 @@ def test_layout_bijection(dt, N, K):
         src = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
     s = z = None
     if dt == 2:
-        s = rng.integers(0, 1 << 16, size=(N, K // 32)).astype(np.uint16)
-        z = rng.integers(0, 1 << 16, size=(N, K // 32)).astype(np.uint16)
-    packed = oracle.pack(dt, N, K, 32, src, s, z)
-    back, s2, z2 = oracle.unpack(dt, N, K, 32, packed)
+        s = rng.integers(0, 1 << 16, size=(N, K // G)).astype(np.uint16)
+        z = rng.integers(0, 1 << 16, size=(N, K // G)).astype(np.uint16)
+    packed = oracle.pack(dt, N, K, src, s, z, G=G)
+    back, s2, z2 = oracle.unpack(dt, N, K, packed, G=G)
     assert np.array_equal(back, src)
     if dt == 2:
         assert np.array_equal(s2, s) and np.array_equal(z2, z)
-    # every code byte is used exactly once: the size equals the logical size
-    # (plus the 16-byte padding of int4 scale words in a ragged tile)
-    logical = N * K * (2 if dt == 0 else 1 if dt == 1 else 0.5) + (N * K // 32 * 4 if dt == 2 else 0)
-    assert logical <= packed.size <= logical + 16 * math.ceil(N / 32) * math.ceil(K / 1024)
+    # slots of 32 rows x 256 code bytes (+ 512 / G scale lines of 128 bytes
+    # for int4), the ragged tile and K-slot padded
+    rowb = K * 2 if dt == 0 else K if dt == 1 else K // 2
+    slot = 8192 + ((512 // G) * 128 if dt == 2 else 0)
+    assert packed.size == -(-N // 32) * -(-rowb // 256) * slot
+    # every code byte of the matrix lands in a distinct byte; the rest is zero
+    nz = np.count_nonzero(packed)
+    assert nz <= N * rowb + (N * (K // G) * 4 if dt == 2 else 0)
 
 
 # ------------------------------------------------------------ linear ------

@@ -38,6 +38,7 @@ def lib():
             "gf_last_error": ([], ctypes.c_char_p),
             "gf_version": ([], i32),
             "gf_packed_bytes": ([i32, i32, i32], i64),
+            "gf_packed_bytes_w4g": ([i32, i32, i32], i64),
             "gf_quantize_w8": ([vp, i32, i32, vp, vp, vp], i32),
             "gf_quantize_w4g": ([vp, i32, i32, i32, vp, vp], i32),
             "gf_repack_bf16": ([vp, i32, i32, vp, vp], i32),
@@ -55,6 +56,7 @@ def lib():
             "gf_model_weight_bytes": ([vp], i64),
             "gf_kv_create": ([vp, i32, vp], i32),
             "gf_kv_destroy": ([vp], i32),
+            "gf_kv_reset": ([vp, vp], i32),
             "gf_kv_cache_ptrs": ([vp, vp, vp], i32),
             "gf_decode_step": ([vp, vp, vp, vp, vp, vp, vp], i32),
             "gf_verify_k": ([vp, vp, vp, i32, vp, vp, vp, vp, vp], i32),
@@ -87,10 +89,10 @@ def _s(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def packed_bytes(wdtype, N, K):
-    n = lib().gf_packed_bytes(wdtype, N, K)
+def packed_bytes(wdtype, N, K, G=32):
+    n = lib().gf_packed_bytes_w4g(N, K, G) if wdtype == W_INT4G32 else lib().gf_packed_bytes(wdtype, N, K)
     if n < 0:
-        raise GfError("bad shape for dtype %d: %dx%d" % (wdtype, N, K))
+        raise GfError("bad shape for dtype %d: %dx%d (G=%d)" % (wdtype, N, K, G))
     return int(n)
 
 
@@ -105,7 +107,7 @@ def quantize_w8(W, stream=None):
 
 def quantize_w4g(W, G=32, stream=None):
     N, K = W.shape
-    packed = torch.empty(packed_bytes(W_INT4G32, N, K), dtype=torch.uint8, device=W.device)
+    packed = torch.empty(packed_bytes(W_INT4G32, N, K, G), dtype=torch.uint8, device=W.device)
     _check(lib().gf_quantize_w4g(_p(W), N, K, G, _p(packed), _s(stream)), "gf_quantize_w4g")
     return packed
 
@@ -126,8 +128,8 @@ def unpack_w8(packed, N, K, stream=None):
 def unpack_w4g(packed, N, K, G=32, stream=None):
     dev = packed.device
     q = torch.empty((N, K), dtype=torch.uint8, device=dev)
-    s = torch.empty((N, K // 32), dtype=torch.bfloat16, device=dev)
-    z = torch.empty((N, K // 32), dtype=torch.bfloat16, device=dev)
+    s = torch.empty((N, K // G), dtype=torch.bfloat16, device=dev)
+    z = torch.empty((N, K // G), dtype=torch.bfloat16, device=dev)
     _check(lib().gf_unpack_w4g(_p(packed), N, K, G, _p(q), _p(s), _p(z), _s(stream)), "gf_unpack_w4g")
     return q, s, z
 
@@ -192,7 +194,7 @@ class _Config(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("n_layers", ctypes.c_int), ("n_heads", ctypes.c_int),
                 ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
                 ("vocab", ctypes.c_int), ("n_experts", ctypes.c_int), ("eps", ctypes.c_float),
-                ("theta", ctypes.c_double)]
+                ("theta", ctypes.c_double), ("group_size", ctypes.c_int)]
 
 
 class _Weights(ctypes.Structure):
@@ -212,13 +214,13 @@ class Model:
     layer, a dict of bf16 device tensors wqkv, wo, wgu (gate/up rows
     interleaved), wd, g_attn, g_ffn -- for a mixture of experts wgu and wd are
     lists (one per expert) and `router` [n_experts][d] is added; `glob` holds
-    embed, g_final, lm_head."""
+    embed, g_final, lm_head.  cfg["group"] sets the int4 group size (32)."""
 
     def __init__(self, cfg, wdtype, glob, layers):
         self.cfg = cfg
         self.wdtype = DTYPE_NAMES.get(wdtype, wdtype)
         c = _Config(cfg["d"], cfg["n_layers"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["ffn"],
-                    cfg["vocab"], cfg.get("n_experts", 0), cfg["eps"], cfg["theta"])
+                    cfg["vocab"], cfg.get("n_experts", 0), cfg["eps"], cfg["theta"], cfg.get("group", 32))
         keep = []
         arrays = {}
         moe = cfg.get("n_experts", 0) > 0
@@ -260,6 +262,11 @@ class KV:
         h = ctypes.c_void_p()
         _check(lib().gf_kv_create(model.h, tmax, ctypes.byref(h)), "gf_kv_create")
         self.h = h
+
+    def reset(self, stream=None):
+        """Zeroes the cache and step counters (gf_kv_reset); the caller's
+        position tensor is theirs to set back to 0."""
+        _check(lib().gf_kv_reset(self.h, _s(stream)), "gf_kv_reset")
 
     def cache_ptrs(self):
         k, v = ctypes.c_void_p(), ctypes.c_void_p()

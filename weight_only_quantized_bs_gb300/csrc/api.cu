@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+
 #include "gf_internal.cuh"
 
 namespace gf {
@@ -57,11 +58,11 @@ extern "C" {
 
 const char* gf_last_error(void) { return g_msg; }
 
-int gf_version(void) { return 1; }
+int gf_version(void) { return 2; }
 
 long long gf_packed_bytes(int wdtype, int N, int K) {
   if (wdtype < 0 || wdtype > 2 || N <= 0 || K <= 0 || K % per_chunk(wdtype)) return -1;
-  return packed_bytes(wdtype, N, K);
+  return packed_bytes(wdtype, N, K, 32);
 }
 
 int gf_copy_ceiling(const void* src, void* dst, size_t bytes, gf_stream stream) {

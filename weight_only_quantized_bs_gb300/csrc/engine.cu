@@ -2,26 +2,32 @@
 //
 // One CTA per SM runs a program of phases (a single GEMV or attention for the
 // standalone calls; every layer of a decode step for gf_decode_step).  In
-// each CTA one producer thread streams the CTA's weight half-tiles (16 rows x
-// one K-block) and KV-cache rows from HBM into a ring of 16 shared-memory
-// slots with bulk asynchronous copies (cp.async.bulk, completion counted on
-// an mbarrier, L2 evict-first hint), running ahead across phase boundaries
-// because the weight stream does not depend on activations.  Each slot
-// belongs to one of eight consumer warps (stream index mod 8, so a ring entry
-// always serves the same warp), which dequantises the
-// int8 / int4 codes of its 16 rows in registers against an fp32 copy of the
-// input vector held in shared memory and releases the slot; the K-block
-// partial sums of a half-tile meet in shared memory, where the last warp to
-// arrive adds them in a fixed order and runs the epilogue.  Dependent phases
-// are separated by grid barriers (cooperative launch); every wait in the
-// kernel is bounded by a 2-second clock, after which the kernel records an
-// error code, drains its own copies in flight and returns.
+// each CTA one producer thread streams the CTA's weight slots and KV-cache
+// rows from HBM into a ring of 16 shared-memory slots, running ahead across
+// phase boundaries because the weight stream does not depend on activations.
+// A weight slot is 32 rows x 256 bytes of each row (plus, for int4, the
+// rows' scale/zero words), stored contiguously in the swizzled layout of
+// gf_internal.cuh and moved by one bulk asynchronous copy (the tensor-memory
+// accelerator's linear mode); a KV slot is 16 positions of K and of V, one
+// bulk copy each.  Completion is counted on an mbarrier per slot, and the
+// loads carry an L2 evict-first hint.  Slot X belongs to consumer warp
+// X mod 8 (two ring entries per warp), whose lane r owns row r of the slot:
+// it dequantises the int8 / int4 codes of its row in registers against the
+// fp32 input vector staged in shared memory (a broadcast read, the same for
+// all lanes) and keeps its row's partial sum, so that no cross-lane reduction
+// is needed.  A tile's partial sums from the warps that held its K-slots meet
+// in shared memory, where the last warp to arrive adds them in K order and
+// runs the epilogue.  Dependent phases are separated by grid barriers
+// (cooperative launch) or by per-head completion counters; every wait in the
+// kernel is bounded by a clock (2 s by default), after which the kernel
+// records an error code, drains its own copies in flight and returns.
 //
 // The decode step computed here is the batch-size-1 autoregressive step of
 // the gpt-fast README ("Benchmarks", "Quantization"): RMSNorm, q/k/v, RoPE,
 // KV append, single-query attention, o projection, residual, RMSNorm, SwiGLU,
 // residual, final RMSNorm, lm_head, greedy argmax.
 #include <math.h>
+#include <string.h>
 
 #include "gf_internal.cuh"
 
@@ -71,17 +77,13 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// one-dimensional bulk copy (KV rows, column-sliced down projection)
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
-}
-__device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
 }
 __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
@@ -99,8 +101,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-constexpr uint64_t WAIT_NS = 2000000000ull;
-
 // try_wait that may suspend the thread for up to 20 us; the hardware wakes it
 // as soon as the phase completes, so the hint adds no latency but keeps a
 // waiting warp from spinning on issue slots the compute warps need.
@@ -114,33 +114,37 @@ __device__ __forceinline__ bool mbar_test_sleep(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* b, uint32_t parity, int* err, int code) {
+// The limit of every bounded wait of a launch (Params::wait_ns, else 2 s).
+__device__ __forceinline__ uint64_t wait_limit(const Params& P) { return P.wait_ns ? P.wait_ns : 2000000000ull; }
+
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* b, uint32_t parity, int* err, int code, uint64_t lim) {
   const uint64_t t0 = gtimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test_sleep(b, parity)) return true;
     if ((it & 3) == 0) {
       if (ld_relaxed(err)) return false;
-      if (gtimer() - t0 > WAIT_NS) {
+      if (gtimer() - t0 > lim) {
         atomicCAS(err, 0, code);
         return false;
       }
     }
   }
 }
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int* err, int code) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int* err, int code, uint64_t lim) {
   if (mbar_test(b, parity)) return true;
-  return mbar_wait_slow(b, parity, err, code);
+  return mbar_wait_slow(b, parity, err, code, lim);
 }
 
-__device__ __noinline__ bool grid_wait(const unsigned* bar, unsigned target, int* err) {
+// Waits until *ctr >= target (acquire); bounded.
+__device__ __noinline__ bool counter_wait(const unsigned* ctr, unsigned target, int* err, int code, uint64_t lim) {
   const uint64_t t0 = gtimer();
   for (uint32_t it = 0;; ++it) {
-    if (ld_acquire(bar) >= target) return true;
+    if (ld_acquire(ctr) >= target) return true;
     __nanosleep(40);
     if ((it & 15) == 15) {
       if (ld_relaxed(err)) return false;
-      if (gtimer() - t0 > WAIT_NS) {
-        atomicCAS(err, 0, ERR_WAIT_GRID);
+      if (gtimer() - t0 > lim) {
+        atomicCAS(err, 0, code);
         return false;
       }
     }
@@ -151,26 +155,39 @@ __device__ __forceinline__ void grid_arrive(unsigned* bar) {
   atomicAdd(bar, 1u);
 }
 
+// Bounded wait of one lane on a shared-memory word reaching `want` (==) or
+// at least `want` (ge); false if it gave up.
+__device__ __noinline__ bool smem_wait(const int* w, int want, bool ge, int* err, uint64_t lim) {
+  volatile const int* p = w;
+  const uint64_t t0 = gtimer();
+  while (ge ? (*p < want) : (*p != want)) {
+    __nanosleep(32);
+    if (gtimer() - t0 > lim) {
+      atomicCAS(err, 0, ERR_WAIT_COMBINE);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 __device__ __forceinline__ uint16_t f2bf(float f) {
   uint32_t u = __float_as_uint(f);
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
 }
-__device__ __forceinline__ float rbf(float f) { return bf2f(f2bf(f)); }
 
 // ---------------------------------------------------------- shared state --
 struct Smem {
   uint8_t* ring;
-  float* xs;        // fp32 input vector, swizzled per chunk
-  float* xsum;      // sum of x over each 32-wide group (int4 zero offsets)
-  float* tb;        // [NTB][NCW][HROWS] partial row sums of half-tiles
+  float* xs;        // fp32 input vector (times the dequantisation powers)
+  float* xsum;      // sums of x over each int4 group / int8 chunk (times 2^-64)
+  float* tb;        // [NTB][NCW][TR] partial row sums of tiles
   int* tbc;         // [NTB] arrival counters
-  int* tbg;         // [NTB] half-tile allowed to use the buffer next
+  int* tbg;         // [NTB] tile allowed to use the buffer next
   uint64_t* full;   // [NSLOT]
   uint64_t* empty;  // [NSLOT]
   uint64_t* cbar;   // consumer-warps barrier
-  uint64_t* xbar;   // completion of the bulk copy of a phase's input vector
   float* red;       // [64] reduction scratch; [32..39] router logits, [40..41] expert weights
   int* bcast;       // [64] broadcast ints; [32..33] chosen experts, [34] phase they were chosen in,
                     // [48..55] verify: union of the rows' experts, [56] its size
@@ -178,7 +195,11 @@ struct Smem {
   Phase* phb;       // [2] the consumers' copies of the current and next phase descriptor
 };
 
-__device__ __forceinline__ Smem smem_layout(uint8_t* base) {
+__device__ __forceinline__ Smem smem_layout(uint8_t* raw) {
+  // slots start on 128-byte boundaries, so that a line's units map to banks
+  // as the swizzle assumes
+  const uint32_t a = smem_u32(raw);
+  uint8_t* base = raw + ((128u - (a & 127u)) & 127u);
   Smem s;
   s.ring = base + OFF_RING;
   s.xs = reinterpret_cast<float*>(base + OFF_X);
@@ -189,7 +210,6 @@ __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
   s.full = reinterpret_cast<uint64_t*>(base + OFF_BAR);
   s.empty = s.full + NSLOT;
   s.cbar = s.empty + NSLOT;
-  s.xbar = s.cbar + 1;
   s.red = reinterpret_cast<float*>(base + OFF_MISC);
   s.bcast = reinterpret_cast<int*>(base + OFF_MISC + 256);
   s.moew = reinterpret_cast<float*>(base + OFF_MISC + 512);
@@ -198,49 +218,9 @@ __device__ __forceinline__ Smem smem_layout(uint8_t* base) {
 }
 
 __device__ __forceinline__ int first_unit(int cta, int rot, int G) { return ((cta - rot) % G + G) % G; }
+__device__ __forceinline__ int units_of(int first, int n, int G) { return first < n ? (n - first + G - 1) / G : 0; }
 
 __device__ __forceinline__ const Phase& phase_at(const Params& P, int i) { return P.prog ? P.prog[i] : P.single; }
-
-// ============================================================ producer ====
-struct Prod {
-  uint32_t it;
-  uint64_t pol;
-  uint32_t blocked;
-};
-
-__device__ __forceinline__ bool prod_slot(const Smem& S, Prod& pr, int* err, uint8_t*& dst, uint64_t*& fb) {
-  const uint32_t slot = pr.it % NSLOT, use = pr.it / NSLOT;
-  if (use > 0) {
-    if (!mbar_probe(&S.empty[slot], (use - 1) & 1u)) ++pr.blocked;
-    if (!mbar_wait(&S.empty[slot], (use - 1) & 1u, err, ERR_WAIT_EMPTY)) return false;
-  }
-  dst = S.ring + slot * SLOT_BYTES;
-  fb = &S.full[slot];
-  ++pr.it;
-  return true;
-}
-
-// The producer needs the two experts of a MOE_GU phase before it can stream
-// their weights: consumer thread 0 publishes them in shared memory, tagged
-// with the phase index.  Bounded wait.
-__device__ bool wait_experts(const Smem& S, int* err, int pi) {
-  volatile int* seq = S.bcast + 34;
-  const uint64_t t0 = gtimer();
-  for (uint32_t it = 0;; ++it) {
-    if (*seq == pi + 1) {
-      __threadfence_block();
-      return true;
-    }
-    __nanosleep(64);
-    if ((it & 31) == 31) {
-      if (ld_relaxed(err)) return false;
-      if (gtimer() - t0 > WAIT_NS) {
-        atomicCAS(err, 0, ERR_WAIT_ROUTER);
-        return false;
-      }
-    }
-  }
-}
 
 // ------------------------------------------------ attention units -------
 // Units of an attention phase: for each query row m (one in a decode step,
@@ -276,42 +256,35 @@ __device__ int attn_units(const Phase& ph, const Params& P, int pos, int u, Attn
   return base;
 }
 
-// Segments of a GEMV phase: the matrices it covers (several experts for MoE).
-__device__ __forceinline__ int gemv_segments(const Phase& ph, const Params& P, const Smem& S, int& Ns,
-                                             const uint8_t** wseg, int* eseg) {
+// Segments of a GEMV phase: the matrices it covers (several experts for MoE),
+// as expert indices into the tall matrix of all experts.
+__device__ __forceinline__ int gemv_segments(const Phase& ph, const Params& P, const Smem& S, int& Ns, int* eseg) {
   volatile int* bc = S.bcast;
   if (ph.moe == MOE_NONE) {
     Ns = ph.N;
-    wseg[0] = ph.W;
     eseg[0] = 0;
     return 1;
   }
   if (verifying(P)) {  // verify: the union of the rows' experts
     const int n = bc[56];
     Ns = ph.N;
-    for (int k = 0; k < n; ++k) {
-      eseg[k] = bc[48 + k];
-      wseg[k] = ph.W + (size_t)eseg[k] * ph.expert_stride;
-    }
+    for (int k = 0; k < n; ++k) eseg[k] = bc[48 + k];
     return n;
   }
   if (ph.moe == MOE_GU) {
     Ns = ph.N / 2;
-    for (int k = 0; k < 2; ++k) {
-      eseg[k] = bc[32 + k];
-      wseg[k] = ph.W + (size_t)eseg[k] * ph.expert_stride;
-    }
+    eseg[0] = bc[32];
+    eseg[1] = bc[33];
     return 2;
   }
   Ns = ph.N;
   eseg[0] = bc[32 + ph.moe - MOE_DOWN0];
-  wseg[0] = ph.W + (size_t)eseg[0] * ph.expert_stride;
   return 1;
 }
 
 // Slot order of a multi-row (verify) GEMV phase: the CTA's tiles in groups of
-// up to VTG tiles of one segment; per group, K-block by K-block, the group's
-// tiles and their halves.  Consumers walk the same order.
+// up to VTG tiles of one segment; per group, K-slot by K-slot, the group's
+// tiles.  Consumers walk the same order.
 struct TileGroups {
   int first, G, ntiles, tps;
 };
@@ -326,16 +299,76 @@ __device__ __forceinline__ int group_end(const TileGroups& tg, int i0) {
   return i1;
 }
 
-__device__ bool wait_experts(const Smem& S, int* err, int pi);
+// ============================================================ producer ====
+// NPROD producer threads (lane 0 of the last NPROD warps) walk the same slot
+// stream; producer p issues the slots X with X % NPROD == p, which use the
+// ring entries of that residue only.  One thread can issue a bulk copy only
+// every few hundred nanoseconds, which alone would cap the stream below the
+// HBM rate; two issue in parallel.
+struct Prod {
+  uint32_t it;
+  uint64_t pol;
+  uint32_t blocked;
+  uint64_t lim;
+  uint32_t pid;
+};
+
+// Advances the stream by one slot.  1: this producer's slot (dst and fb set,
+// its copies to be issued); 0: another producer's slot; -1: a wait gave up.
+__device__ __forceinline__ int prod_slot(const Smem& S, Prod& pr, int* err, uint8_t*& dst, uint64_t*& fb) {
+  const uint32_t x = pr.it++;
+  if (x % NPROD != pr.pid) return 0;
+  const uint32_t slot = x % NSLOT, use = x / NSLOT;
+  if (use > 0) {
+    if (!mbar_probe(&S.empty[slot], (use - 1) & 1u)) ++pr.blocked;
+    if (!mbar_wait(&S.empty[slot], (use - 1) & 1u, err, ERR_WAIT_EMPTY, pr.lim)) return -1;
+  }
+  dst = S.ring + slot * SLOT_BYTES;
+  fb = &S.full[slot];
+  return 1;
+}
+
+// One GEMV slot: tile lt of segment (expert) e (tiles per expert tps), K-slot b.
+__device__ __forceinline__ bool produce_gemv_slot(const Phase& ph, const Params& P, const Smem& S, Prod& pr, int e,
+                                                  int tps, int lt, int b) {
+  const int dt = ph.dtype, nb = k_slots(dt, ph.K), sb = slot_bytes(dt, ph.G);
+  uint8_t* dst;
+  uint64_t* fb;
+  const int r = prod_slot(S, pr, P.err, dst, fb);
+  if (r <= 0) return r == 0;
+  mbar_expect_tx(fb, (uint32_t)sb);
+  bulk_g2s(dst, ph.W + (((size_t)e * tps + lt) * nb + b) * sb, (uint32_t)sb, fb, pr.pol);
+  return true;
+}
+
+// The producer needs the two experts of a MOE_GU phase before it can stream
+// their weights: consumer thread 0 publishes them in shared memory, tagged
+// with the phase index.  Bounded wait.
+__device__ bool wait_experts(const Smem& S, int* err, int pi, uint64_t lim) {
+  volatile int* seq = S.bcast + 34;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 0;; ++it) {
+    if (*seq == pi + 1) {
+      __threadfence_block();
+      return true;
+    }
+    __nanosleep(64);
+    if ((it & 31) == 31) {
+      if (ld_relaxed(err)) return false;
+      if (gtimer() - t0 > lim) {
+        atomicCAS(err, 0, ERR_WAIT_ROUTER);
+        return false;
+      }
+    }
+  }
+}
 
 __device__ bool produce_gemv_m(const Phase& ph, const Params& P, const Smem& S, Prod& pr, int cta, int pi) {
-  int* err = P.err;
-  if (ph.moe == MOE_GU && !wait_experts(S, err, pi)) return false;
-  const int dt = ph.dtype, C = ph.K / per_chunk(dt), nb = (C + KBLK - 1) / KBLK;
+  if (ph.moe == MOE_GU && !wait_experts(S, P.err, pi, pr.lim)) return false;
+  const int nb = k_slots(ph.dtype, ph.K);
   int Ns;
-  const uint8_t* wseg[8];
   int eseg[8];
-  const int nseg = gemv_segments(ph, P, S, Ns, wseg, eseg);
+  const int nseg = gemv_segments(ph, P, S, Ns, eseg);
   TileGroups tg;
   tg.tps = (Ns + TR - 1) / TR;
   tg.ntiles = nseg * tg.tps;
@@ -344,22 +377,9 @@ __device__ bool produce_gemv_m(const Phase& ph, const Params& P, const Smem& S, 
   for (int i0 = 0; tg.first + i0 * tg.G < tg.ntiles;) {
     const int i1 = group_end(tg, i0);
     for (int b = 0; b < nb; ++b) {
-      const int Lb = min(KBLK, C - b * KBLK);
       for (int i = i0; i < i1; ++i) {
-        const int t = tg.first + i * tg.G, seg = t / tg.tps, lt = t % tg.tps;
-        const int Rt = min(TR, Ns - lt * TR);
-        for (int h = 0; h * HROWS < Rt; ++h) {
-          const int r0 = h * HROWS, rh = min(HROWS, Rt - r0);
-          const uint8_t* blk = wseg[seg] + block_offset(dt, C, lt, Rt, b);
-          const uint32_t cb = (uint32_t)(rh * Lb * 16);
-          const uint32_t sb = dt == DT_INT4 ? (uint32_t)((rh * Lb * 4 + 15) / 16 * 16) : 0u;
-          uint8_t* dst;
-          uint64_t* fb;
-          if (!prod_slot(S, pr, err, dst, fb)) return false;
-          mbar_expect_tx(fb, cb + sb);
-          bulk_g2s(dst, blk + (size_t)r0 * Lb * 16, cb, fb, pr.pol);
-          if (sb) bulk_g2s(dst + SLOT_SZ_OFF, blk + (size_t)Rt * Lb * 16 + (size_t)r0 * Lb * 4, sb, fb, pr.pol);
-        }
+        const int t = tg.first + i * tg.G;
+        if (!produce_gemv_slot(ph, P, S, pr, eseg[t / tg.tps], tg.tps, t % tg.tps, b)) return false;
       }
     }
     i0 = i1;
@@ -368,13 +388,16 @@ __device__ bool produce_gemv_m(const Phase& ph, const Params& P, const Smem& S, 
 }
 
 // Slot order of a GEMV phase (producer and consumers walk it identically):
-// for each of the CTA's tiles t, for each half h of the tile's rows, the
-// K-blocks b in order.
-__device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
+// for each of the CTA's tiles t, the K-slots b in order.  PH_FFN: per tile its
+// gate/up K-slots, then the down pieces of the previous tile (NCW * P slots;
+// the piece at stream position X carries rows of warp X % NCW).
+__device__ void producer(const Params& P, const Smem& S, int cta, int pos, int pid) {
   Prod pr;
   pr.it = 0;
   pr.blocked = 0;
+  pr.pid = (uint32_t)pid;
   pr.pol = evict_first_policy();
+  pr.lim = wait_limit(P);
   int* err = P.err;
   const int G = P.nctas;
   bool ok = true;
@@ -383,100 +406,59 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
     if (ph.kind == PH_GEMV && verifying(P)) {
       ok = produce_gemv_m(ph, P, S, pr, cta, pi);
     } else if (ph.kind == PH_GEMV) {
-      const int dt = ph.dtype, C = ph.K / per_chunk(dt);
-      // a phase covers nseg matrices of Ns rows each (two experts for MOE_GU)
-      const int nseg = ph.moe == MOE_GU ? 2 : 1, Ns = ph.N / nseg;
-      const int tps = (Ns + TR - 1) / TR, ntiles = nseg * tps, nb = (C + KBLK - 1) / KBLK;
-      const uint8_t* wseg[2] = {ph.W, ph.W};
-      if (ph.moe != MOE_NONE) {
-        if (ph.moe == MOE_GU && !(ok = wait_experts(S, err, pi))) break;
-        volatile int* sel = S.bcast + 32;
-        if (ph.moe == MOE_GU) {
-          wseg[0] = ph.W + (size_t)sel[0] * ph.expert_stride;
-          wseg[1] = ph.W + (size_t)sel[1] * ph.expert_stride;
-        } else {
-          wseg[0] = ph.W + (size_t)sel[ph.moe - MOE_DOWN0] * ph.expert_stride;
-        }
-      }
-      for (int t = first_unit(cta, ph.rot, G); t < ntiles && ok; t += G) {
-        const int seg = t / tps, lt = t % tps;
-        const int Rt = min(TR, Ns - lt * TR);
-        for (int h = 0; h * HROWS < Rt && ok; ++h) {
-          const int r0 = h * HROWS, rh = min(HROWS, Rt - r0);
-          for (int b = 0; b < nb; ++b) {
-            const int Lb = min(KBLK, C - b * KBLK);
-            const uint8_t* blk = wseg[seg] + block_offset(dt, C, lt, Rt, b);
-            const uint32_t cb = (uint32_t)(rh * Lb * 16);
-            const uint32_t sb = dt == DT_INT4 ? (uint32_t)((rh * Lb * 4 + 15) / 16 * 16) : 0u;
-            uint8_t* dst;
-            uint64_t* fb;
-            if (!(ok = prod_slot(S, pr, err, dst, fb))) break;
-            mbar_expect_tx(fb, cb + sb);
-            bulk_g2s(dst, blk + (size_t)r0 * Lb * 16, cb, fb, pr.pol);
-            if (sb) bulk_g2s(dst + SLOT_SZ_OFF, blk + (size_t)Rt * Lb * 16 + (size_t)r0 * Lb * 4, sb, fb, pr.pol);
-          }
-        }
-      }
+      if (ph.moe == MOE_GU && !(ok = wait_experts(S, err, pi, pr.lim))) break;
+      const int nb = k_slots(ph.dtype, ph.K);
+      int Ns;
+      int eseg[8];
+      gemv_segments(ph, P, S, Ns, eseg);
+      const int nseg = ph.moe == MOE_GU ? 2 : 1;
+      const int tps = (Ns + TR - 1) / TR, ntiles = nseg * tps;
+      for (int t = first_unit(cta, ph.rot, G); t < ntiles && ok; t += G)
+        for (int b = 0; b < nb && ok; ++b) ok = produce_gemv_slot(ph, P, S, pr, eseg[t / tps], tps, t % tps, b);
     } else if (ph.kind == PH_FFN) {
-      // per gate/up tile: its two half-tiles' K-blocks, then the rows of the
-      // matching 16-column slice of the down projection
-      const int dt = ph.dtype, C = ph.K / per_chunk(dt), nb = (C + KBLK - 1) / KBLK;
+      const int dt = ph.dtype, nb = k_slots(dt, ph.K);
       const int tps = ph.N / TR, d = ph.N2;
-      int nsl, DR;
-      ffn_split(dt, d, nsl, DR);
-      // an empty slot: completed by the arrival alone
-      auto empty_slot = [&]() {
-        uint8_t* dst;
-        uint64_t* fb;
-        if ((ok = prod_slot(S, pr, err, dst, fb))) mbar_arrive(fb);
-      };
-      // the down slice of a tile follows the next tile's gate/up blocks, so
-      // that its SwiGLU outputs are ready when its rows arrive
+      const FfnSplit fs = ffn_split(dt, d);
+      const int ND = NCW * fs.P;
+      // the down slice of local tile t: ND pieces
       auto down_slice = [&](int t) {
-        for (int k = 0; k < nsl && ok; ++k) {
-          const int r0 = k * DR, nr = min(DR, d - r0);
-          if (nr <= 0) {
-            empty_slot();
-            continue;
-          }
-          const uint8_t* src;
-          const uint8_t* szs = nullptr;
-          uint32_t cb;
-          if (dt == DT_INT4) {
-            const uint8_t* g = ph.W2 + (size_t)(t >> 1) * d * 20;
-            src = g + (size_t)(t & 1) * d * 8 + (size_t)r0 * 8;
-            szs = g + (size_t)d * 16 + (size_t)r0 * 4;
-            cb = (uint32_t)nr * 8;
-          } else {
-            const int rb = dt == DT_INT8 ? 16 : 32;
-            src = ph.W2 + ((size_t)t * d + r0) * rb;
-            cb = (uint32_t)(nr * rb);
-          }
+        for (int m = 0; m < ND && ok; ++m) {
+          const int w = (int)(pr.it % NCW), k = m / NCW;
+          int r0, r1;
+          ffn_piece(fs, d, w, k, r0, r1);
           uint8_t* dst;
           uint64_t* fb;
-          if (!(ok = prod_slot(S, pr, err, dst, fb))) break;
-          mbar_expect_tx(fb, cb + (szs ? (uint32_t)nr * 4 : 0u));
-          bulk_g2s(dst, src, cb, fb, pr.pol);
-          if (szs) bulk_g2s(dst + (size_t)DR * 8, szs, (uint32_t)nr * 4, fb, pr.pol);
+          const int rs = prod_slot(S, pr, err, dst, fb);
+          if (rs < 0) {
+            ok = false;
+            break;
+          }
+          if (rs == 0) continue;
+          if (r0 >= r1) {  // an empty slot: completed by the arrival alone
+            mbar_arrive(fb);
+            continue;
+          }
+          const uint32_t nr = (uint32_t)(r1 - r0);
+          if (dt == DT_INT4) {
+            const uint8_t* g = ph.W2 + (size_t)(t >> 1) * d * 20;
+            mbar_expect_tx(fb, nr * 12u);
+            bulk_g2s(dst, g + (size_t)(t & 1) * d * 8 + (size_t)r0 * 8, nr * 8u, fb, pr.pol);
+            bulk_g2s(dst + (size_t)fs.PR * 8, g + (size_t)d * 16 + (size_t)r0 * 4, nr * 4u, fb, pr.pol);
+          } else if (dt == DT_INT8) {
+            mbar_expect_tx(fb, nr * 16u);
+            bulk_g2s(dst, ph.W2 + ((size_t)t * d + r0) * 16, nr * 16u, fb, pr.pol);
+          } else {
+            const uint8_t* g = ph.W2 + (size_t)t * d * 32;
+            mbar_expect_tx(fb, nr * 32u);
+            bulk_g2s(dst, g + (size_t)r0 * 16, nr * 16u, fb, pr.pol);
+            bulk_g2s(dst + (size_t)fs.PR * 16, g + (size_t)d * 16 + (size_t)r0 * 16, nr * 16u, fb, pr.pol);
+          }
         }
       };
       int prev = -1;
       for (int t = first_unit(cta, ph.rot, G); t < tps && ok; t += G) {
-        for (int h = 0; h < 2 && ok; ++h) {
-          for (int b = 0; b < nb && ok; ++b) {
-            const int Lb = min(KBLK, C - b * KBLK);
-            const uint8_t* blk = ph.W + block_offset(dt, C, t, TR, b);
-            const uint32_t cb = (uint32_t)(HROWS * Lb * 16);
-            const uint32_t sb = dt == DT_INT4 ? (uint32_t)(HROWS * Lb * 4) : 0u;
-            uint8_t* dst;
-            uint64_t* fb;
-            if (!(ok = prod_slot(S, pr, err, dst, fb))) break;
-            mbar_expect_tx(fb, cb + sb);
-            bulk_g2s(dst, blk + (size_t)h * HROWS * Lb * 16, cb, fb, pr.pol);
-            if (sb) bulk_g2s(dst + SLOT_SZ_OFF, blk + (size_t)TR * Lb * 16 + (size_t)h * HROWS * Lb * 4, sb, fb, pr.pol);
-          }
-        }
-        if (prev >= 0) down_slice(prev);
+        for (int b = 0; b < nb && ok; ++b) ok = produce_gemv_slot(ph, P, S, pr, 0, tps, t, b);
+        if (prev >= 0 && ok) down_slice(prev);
         prev = t;
       }
       if (prev >= 0 && ok) down_slice(prev);
@@ -488,34 +470,41 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
         attn_units(ph, P, pos, u, &au);
         const int hh = au.kvh;
         const int p0 = au.p0, p1 = au.p1, pe = min(p1, au.Ts);
-        for (int p = p0; p < pe; p += ATT_POS_PER_SLOT) {
-          const int np = min(ATT_POS_PER_SLOT, pe - p);
+        const int aps = att_slot_pos(ph.hd);
+        for (int p = p0; p < pe; p += aps) {
+          const int np = min(aps, pe - p);
           uint8_t* dst;
           uint64_t* fb;
-          if (!(ok = prod_slot(S, pr, err, dst, fb))) break;
+          const int rs = prod_slot(S, pr, err, dst, fb);
+          if (rs < 0) {
+            ok = false;
+            break;
+          }
+          if (rs == 0) continue;
           const size_t off = ((size_t)hh * ph.Tmax + p) * ph.hd;
           mbar_expect_tx(fb, 2u * np * rowb);
           bulk_g2s(dst, ph.kc + off, np * rowb, fb, pr.pol);
-          bulk_g2s(dst + ATT_POS_PER_SLOT * rowb, ph.vc + off, np * rowb, fb, pr.pol);
+          bulk_g2s(dst + aps * rowb, ph.vc + off, np * rowb, fb, pr.pol);
         }
       }
     }
-    if (P.trace) {
+    if (P.trace && pid == 0) {
       unsigned long long* tr = P.trace + ((size_t)pi * G + cta) * TRACE_W;
       tr[5] = gtimer();
       tr[7] = pr.blocked;
       pr.blocked = 0;
     }
   }
-  // Drain: never leave the CTA with bulk copies still writing its shared
-  // memory.  The last min(it, NSLOT) slots are the only ones that can be in
-  // flight; wait for each one's completion (bounded).
+  // Drain: never leave the CTA with copies still writing its shared memory.
+  // Of this producer's slots, only those among the last min(it, NSLOT) can be
+  // in flight; wait for each one's completion (bounded).
   const uint32_t n = pr.it < (uint32_t)NSLOT ? pr.it : (uint32_t)NSLOT;
   for (uint32_t k = 0; k < n; ++k) {
     const uint32_t i = pr.it - 1 - k, slot = i % NSLOT, use = i / NSLOT;
+    if (i % NPROD != pr.pid) continue;
     const uint64_t t0 = gtimer();
     while (!mbar_test_sleep(&S.full[slot], use & 1u)) {
-      if (gtimer() - t0 > WAIT_NS) {
+      if (gtimer() - t0 > pr.lim) {
         atomicCAS(err, 0, ERR_DRAIN);
         break;
       }
@@ -527,11 +516,11 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos) {
 struct Cons {
   uint32_t it;       // ring position of the phase's first slot
   uint32_t cphase;   // parity of the consumer barrier
-  uint32_t useq;     // half-tiles seen so far (combine-buffer index)
+  uint32_t useq;     // tiles seen so far (combine-buffer index)
   int warp, lane, ctid;
   uint32_t starved;  // slot waits that found the slot still in flight (warp 0)
   float rnorm;       // RMSNorm factor of the staged input (1 if none)
-  uint32_t xphase;   // parity of the input-copy barrier
+  uint64_t lim;      // limit of the bounded waits
 };
 
 // all consumer warps meet; false if the wait gave up
@@ -539,7 +528,7 @@ __device__ __forceinline__ bool cta_sync(const Smem& S, Cons& cs, int* err) {
   __syncwarp();
   mbar_arrive(S.cbar);
   int ok = 1;
-  if (cs.lane == 0) ok = mbar_wait(S.cbar, cs.cphase, err, ERR_WAIT_CTA);
+  if (cs.lane == 0) ok = mbar_wait(S.cbar, cs.cphase, err, ERR_WAIT_CTA, cs.lim);
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok && cs.lane) mbar_test(S.cbar, cs.cphase);  // acquire for this lane (phase already complete)
   cs.cphase ^= 1u;
@@ -551,7 +540,7 @@ __device__ __forceinline__ bool cta_sync(const Smem& S, Cons& cs, int* err) {
 __device__ __forceinline__ bool slot_acquire(const Smem& S, Cons& cs, uint32_t it, int* err, const uint8_t*& base) {
   const uint32_t slot = it % NSLOT, par = (it / NSLOT) & 1u;
   if (cs.warp == 0 && cs.lane == 0 && !mbar_probe(&S.full[slot], par)) ++cs.starved;
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(&S.full[slot], par, err, ERR_WAIT_FULL));
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&S.full[slot], par, err, ERR_WAIT_FULL, cs.lim));
   base = S.ring + slot * SLOT_BYTES;
   return ok;
 }
@@ -593,149 +582,102 @@ __device__ __forceinline__ float4 dq_inv(int dt, int u) {
   return make_float4(1.0f, 1.0f, 1.0f, 1.0f);
 }
 // ------------------------------------------------------ input staging ----
-__device__ __forceinline__ int swz(int g, int U) { return ((g * U) >> 3) & (U - 1); }
-
 __device__ __forceinline__ float4 bf4(uint2 h) {
   return make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xFFFF0000u), __uint_as_float(h.y << 16),
                      __uint_as_float(h.y & 0xFFFF0000u));
 }
 
-// Stores float4 number k4 of x (swizzled per chunk so that the 32 lanes of a
-// warp read their chunks without bank conflicts), multiplied by the powers of
-// two that the subnormal dequantisation of int4 / int8 codes expects, and the
-// chunk sums the epilogues need: for int4 the sum of x over each 32-wide group
-// (8 consecutive threads hold one group), for int8 128 times the sum over each
-// 16-wide chunk (4 threads), both times 2^-64.
-__device__ __forceinline__ void stage_store(const Smem& S, const Cons& cs, int dt, int U, int k4, bool ok, float4 a) {
-  const int g = k4 / U, u = k4 % U;
-  const float4 m = dq_mult(dt, u);
-  if (ok)
-    reinterpret_cast<float4*>(S.xs)[g * U + (u ^ swz(g, U))] = make_float4(a.x * m.x, a.y * m.y, a.z * m.z, a.w * m.w);
+// Stores float4 number k4 of x multiplied by the powers of two that the
+// subnormal dequantisation of int4 / int8 codes expects, and the sums the
+// epilogues need: for int4 the sum of x over each group of G (G / 4
+// consecutive lanes hold one group; k4 runs over whole warps of consecutive
+// float4), for int8 128 times the sum over each 16-wide chunk (4 lanes),
+// both times 2^-64.
+__device__ __forceinline__ void stage_store(const Smem& S, const Cons& cs, int dt, int G, int k4, bool ok, float4 a) {
+  const float4 m = dq_mult(dt, k4 & 7);
+  if (ok) reinterpret_cast<float4*>(S.xs)[k4] = make_float4(a.x * m.x, a.y * m.y, a.z * m.z, a.w * m.w);
   if (dt != DT_BF16) {
     float sg = a.x + a.y + a.z + a.w;
-    sg += __shfl_xor_sync(0xffffffffu, sg, 1);
-    sg += __shfl_xor_sync(0xffffffffu, sg, 2);
-    if (dt == DT_INT4) sg += __shfl_xor_sync(0xffffffffu, sg, 4);
-    if (ok && (cs.lane & (U - 1)) == 0) S.xsum[g] = sg * (dt == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
+    const int span = dt == DT_INT4 ? G / 4 : 4;  // lanes per group / chunk
+    for (int o = 1; o < span; o <<= 1) sg += __shfl_xor_sync(0xffffffffu, sg, o);
+    if (ok && (cs.lane & (span - 1)) == 0) S.xsum[(4 * k4) / (dt == DT_INT4 ? G : 16)] =
+        sg * (dt == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
   }
 }
 
-// Stages the phase's input vector into shared memory as fp32.  Thread t
-// handles float4 numbers t + 224 i; all of its loads are issued before any is
-// used, so staging costs about one L2 round trip.  For an RMSNorm input only
-// the gain is applied here: the factor 1/rms needs the whole vector, and as
-// the GEMV is linear it is applied to the outputs in the epilogue instead
-// (cs.rnorm, 1 for other inputs), which keeps the reduction off the path.
-__device__ bool stage_x_regs(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
-  constexpr int NT = NCW * 32, MAXIT = (KMAX / 4 + NT - 1) / NT;
-  const int K = ph.K, dt = ph.dtype, U = per_chunk(dt) / 4, K4 = K / 4;
+// Stages the phase's input vector into shared memory as fp32, zero from K up
+// to the end of the last K-slot (the slots' padding codes are zero, and the
+// products with them must be exactly zero).  For an
+// RMSNorm input only the gain is applied here: the factor 1/rms needs the
+// whole vector, and as the GEMV is linear it is applied to the outputs in
+// the epilogue instead (cs.rnorm, 1 for other inputs), which keeps the
+// reduction off the path.  fp32 inputs (X_F32, X_NORM) are fetched with
+// per-thread asynchronous copies into the x area (the gain into the top of
+// that area), then converted in place: gain, 1/rms partial sums, the
+// dequantisation powers and the group sums.  Warp w copies and converts the
+// runs of 32 float4 starting at 32 w + 256 i: its lanes' copies are complete
+// and visible to the warp after wait_all and __syncwarp.  The copies use the
+// load/store path, not the bulk-copy engine, whose queue holds the
+// producer's weight prefetches.  bf16 inputs (standalone GEMVs, the embedding
+// row) are loaded into registers first.
+__device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
+  const int K = ph.K, dt = ph.dtype, G = ph.G, K4 = K / 4;
+  const int KP4 = (int)round_up(K, slot_k(dt)) / 4;  // staged float4, with the zero tail
   const bool norm = ph.xsrc == X_NORM || ph.xsrc == X_EMBED_NORM;
-  const uint16_t* emb = ph.xsrc == X_EMBED_NORM ? P.embed + (size_t)(*P.token) * K : nullptr;
-  float4 a[MAXIT];
-  uint2 gk[MAXIT];
-  // one load loop per source, each load writing its own register, so that
-  // nothing waits for a load before the next is issued
-#pragma unroll
-  for (int t = 0; t < MAXIT; ++t) {
-    const int k4 = cs.ctid + t * NT;
-    gk[t] = make_uint2(0x3F803F80u, 0x3F803F80u);  // bf16 ones
-    if (norm && k4 < K4) gk[t] = reinterpret_cast<const uint2*>(ph.gain)[k4];
-  }
-  if (ph.xsrc == X_F32 || ph.xsrc == X_NORM) {
+  float4* xs4 = reinterpret_cast<float4*>(S.xs);
+  float ss = 0.0f;
+  if ((ph.xsrc == X_F32 || ph.xsrc == X_NORM) && ((uintptr_t)ph.xptr & 15) == 0 &&
+      (!norm || (KP4 * 16 + K * 2 <= KMAX * 4 && ((uintptr_t)ph.gain & 7) == 0))) {
+    uint2* gs = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(S.xs) + KMAX * 4 - K * 2);
     const float4* src = reinterpret_cast<const float4*>(ph.xptr);
-#pragma unroll
-    for (int t = 0; t < MAXIT; ++t) {
-      const int k4 = cs.ctid + t * NT;
-      a[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (k4 < K4) a[t] = __ldcg(src + k4);
+    const uint2* gsrc = reinterpret_cast<const uint2*>(ph.gain);
+#pragma unroll 1
+    for (int f = cs.warp * 32 + cs.lane; f < K4; f += NCW * 32) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(xs4 + f)), "l"(src + f) : "memory");
+      if (norm) asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(gs + f)), "l"(gsrc + f) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    cp_async_wait_all();
+    __syncwarp();
+#pragma unroll 1
+    for (int base = cs.warp * 32; base < KP4; base += NCW * 32) {  // warp-uniform trip count
+      const int f = base + cs.lane;
+      const bool in = f < K4;
+      float4 a = in ? xs4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (norm) {
+        ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+        const float4 g = bf4(in ? gs[f] : make_uint2(0u, 0u));
+        a = make_float4(a.x * g.x, a.y * g.y, a.z * g.z, a.w * g.w);
+      }
+      __syncwarp();  // every lane has read the run before any lane overwrites it
+      stage_store(S, cs, dt, G, f, f < KP4, a);
     }
   } else {
-    const uint2* src = emb ? reinterpret_cast<const uint2*>(emb) : reinterpret_cast<const uint2*>(ph.xptr);
-    uint2 h[MAXIT];
-#pragma unroll
-    for (int t = 0; t < MAXIT; ++t) {
-      const int k4 = cs.ctid + t * NT;
-      h[t] = make_uint2(0u, 0u);
-      if (k4 < K4) h[t] = __ldcg(src + k4);
-    }
-#pragma unroll
-    for (int t = 0; t < MAXIT; ++t) a[t] = bf4(h[t]);
-  }
-  // keep every load above the shared-memory stores below (the compiler
-  // cannot tell that they do not alias), so that all are in flight at once
-  asm volatile("" ::: "memory");
-  float ss = 0.0f;
-#pragma unroll
-  for (int t = 0; t < MAXIT; ++t) {
-    const int k4 = cs.ctid + t * NT;
-    if (t * NT < K4) {  // warp-uniform: the chunk sums shuffle within the warp
-      if (norm) {
-        ss += a[t].x * a[t].x + a[t].y * a[t].y + a[t].z * a[t].z + a[t].w * a[t].w;
-        if (emb && cta == 0 && k4 < K4) reinterpret_cast<float4*>(P.resid)[k4] = a[t];
-        const float4 g = bf4(gk[t]);
-        a[t] = make_float4(a[t].x * g.x, a[t].y * g.y, a[t].z * g.z, a[t].w * g.w);
+    // bf16 vector or embedding row (optionally normalised), or an unaligned
+    // fp32 vector: loads into registers, one run of 32 float4 per warp at a time
+    const uint16_t* emb = ph.xsrc == X_EMBED_NORM ? P.embed + (size_t)(*P.token) * K : nullptr;
+#pragma unroll 1
+    for (int base = cs.warp * 32; base < KP4; base += NCW * 32) {
+      const int f = base + cs.lane;
+      const bool in = f < K4;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (in) {
+        if (ph.xsrc == X_F32 || ph.xsrc == X_NORM) {
+          const float* x = reinterpret_cast<const float*>(ph.xptr) + 4 * f;
+          a = make_float4(__ldcg(x), __ldcg(x + 1), __ldcg(x + 2), __ldcg(x + 3));
+        } else {
+          const uint2* src = emb ? reinterpret_cast<const uint2*>(emb) : reinterpret_cast<const uint2*>(ph.xptr);
+          a = bf4(__ldcg(src + f));
+        }
       }
-      stage_store(S, cs, dt, U, k4, k4 < K4, a[t]);
+      if (norm) {
+        ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+        if (emb && cta == 0 && in) reinterpret_cast<float4*>(P.resid)[f] = a;
+        const float4 g = bf4(in ? reinterpret_cast<const uint2*>(ph.gain)[f] : make_uint2(0u, 0u));
+        a = make_float4(a.x * g.x, a.y * g.y, a.z * g.z, a.w * g.w);
+      }
+      stage_store(S, cs, dt, G, f, f < KP4, a);
     }
-  }
-  if (norm) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (cs.lane == 0) S.red[cs.warp] = ss;
-  }
-  if (!cta_sync(S, cs, P.err)) return false;
-  cs.rnorm = 1.0f;
-  if (norm) {
-    float tot = 0.0f;
-#pragma unroll
-    for (int w = 0; w < NCW; ++w) tot += S.red[w];
-    cs.rnorm = 1.0f / sqrtf(tot / (float)K + ph.eps);
-  }
-  return true;
-}
-
-// Stages an fp32 input vector (X_F32, or X_NORM with its bf16 gain) with
-// per-thread asynchronous copies into the x area (the gain into the top of
-// that area), then converts it in place with a short loop: gain, 1/rms
-// partial sums, the dequantisation multipliers, the per-chunk swizzle and the
-// chunk sums.  Warp w copies and converts the runs of 32 float4 starting at
-// 32 w + 224 i (whole chunks): its lanes' copies are complete and visible to
-// the warp after wait_all and __syncwarp, and all lanes load a run before any
-// lane stores into it, so the in-place permutation inside a chunk is safe.
-// The copies use the load/store path, not the bulk-copy engine, whose queue
-// holds the producer's weight prefetches.  Other inputs (bf16 vectors, the
-// embedding row) go through stage_x_regs.
-__device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
-  const int K = ph.K, dt = ph.dtype, U = per_chunk(dt) / 4, K4 = K / 4;
-  const bool norm = ph.xsrc == X_NORM;
-  const bool fast = (ph.xsrc == X_F32 || norm) && (!norm || (K * 6 <= KMAX * 4 && ((uintptr_t)ph.gain & 7) == 0)) &&
-                    ((uintptr_t)ph.xptr & 15) == 0;
-  if (!fast) return stage_x_regs(ph, P, S, cs, cta);
-  float4* xs4 = reinterpret_cast<float4*>(S.xs);
-  uint2* gs = reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(S.xs) + KMAX * 4 - K * 2);
-  const float4* src = reinterpret_cast<const float4*>(ph.xptr);
-  const uint2* gsrc = reinterpret_cast<const uint2*>(ph.gain);
-#pragma unroll 1
-  for (int f = cs.warp * 32 + cs.lane; f < K4; f += NCW * 32) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(xs4 + f)), "l"(src + f) : "memory");
-    if (norm) asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(gs + f)), "l"(gsrc + f) : "memory");
-  }
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  cp_async_wait_all();
-  __syncwarp();
-  float ss = 0.0f;
-#pragma unroll 1
-  for (int base = cs.warp * 32; base < K4; base += NCW * 32) {  // warp-uniform trip count
-    const int f = base + cs.lane;
-    const bool in = f < K4;
-    float4 a = in ? xs4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (norm) {
-      ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
-      const float4 g = bf4(in ? gs[f] : make_uint2(0u, 0u));
-      a = make_float4(a.x * g.x, a.y * g.y, a.z * g.z, a.w * g.w);
-    }
-    __syncwarp();  // every lane has read the run before any lane overwrites it
-    stage_store(S, cs, dt, U, f, in, a);
   }
   if (norm) {
 #pragma unroll
@@ -757,44 +699,139 @@ __device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& c
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 __device__ __forceinline__ float2 bits2(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
 
-// One 32-bit word of codes of one row against its staged inputs x (natural
-// k order, as pairs), accumulated into acc.
+// One 32-bit word of codes of one row against its staged inputs (natural k
+// order, as pairs), accumulated into acc.
 // int4: the word holds 8 consecutive codes in nibbles 0..7.
-__device__ __forceinline__ float2 word_int4(const uint32_t w, const float2* x, float2 acc) {
+__device__ __forceinline__ float2 word_int4(const uint32_t w, float4 xa, float4 xb, float2 acc) {
   const uint32_t h = w >> 8;
-  acc = ffma2(bits2(w & 0x0000000Fu, w & 0x000000F0u), x[0], acc);
-  acc = ffma2(bits2(w & 0x00000F00u, w & 0x0000F000u), x[1], acc);
-  acc = ffma2(bits2(w & 0x000F0000u, w & 0x00F00000u), x[2], acc);
-  acc = ffma2(bits2(h & 0x000F0000u, h & 0x00F00000u), x[3], acc);
+  acc = ffma2(bits2(w & 0x0000000Fu, w & 0x000000F0u), lo2(xa), acc);
+  acc = ffma2(bits2(w & 0x00000F00u, w & 0x0000F000u), hi2(xa), acc);
+  acc = ffma2(bits2(w & 0x000F0000u, w & 0x00F00000u), lo2(xb), acc);
+  acc = ffma2(bits2(h & 0x000F0000u, h & 0x00F00000u), hi2(xb), acc);
   return acc;
 }
 // int8: 4 consecutive codes, one byte each, stored as the offset code c + 128.
-__device__ __forceinline__ float2 word_int8(const uint32_t wq, const float2* x, float2 acc) {
-  const uint32_t w = wq, h = w >> 8;
-  acc = ffma2(bits2(w & 0x000000FFu, w & 0x0000FF00u), x[0], acc);
-  acc = ffma2(bits2(w & 0x00FF0000u, h & 0x00FF0000u), x[1], acc);
+__device__ __forceinline__ float2 word_int8(const uint32_t w, float4 x, float2 acc) {
+  const uint32_t h = w >> 8;
+  acc = ffma2(bits2(w & 0x000000FFu, w & 0x0000FF00u), lo2(x), acc);
+  acc = ffma2(bits2(w & 0x00FF0000u, h & 0x00FF0000u), hi2(x), acc);
   return acc;
 }
 // bf16: 2 consecutive weights (low half first).
-__device__ __forceinline__ float2 word_bf16(const uint32_t w, const float2* x, float2 acc) {
-  return ffma2(bits2(w << 16, w & 0xFFFF0000u), x[0], acc);
+__device__ __forceinline__ float2 word_bf16(const uint32_t w, float2 x, float2 acc) {
+  return ffma2(bits2(w << 16, w & 0xFFFF0000u), x, acc);
 }
 
-// Sums each of 16 per-lane values over the 32 lanes; afterwards lane l holds
-// the total of value l >> 1.
-__device__ __forceinline__ float warp_rows16(float v[16], int lane) {
+// Lane `lane`'s 16-byte chunk u of a GEMV slot (row lane: line
+// (u >> 3) * 32 + lane, swizzled).
+__device__ __forceinline__ uint4 slot_chunk(const uint8_t* base, int lane, int u) {
+  return *reinterpret_cast<const uint4*>(base + (u >> 3) * (TR * LINE) + lane * LINE + (((u & 7) ^ (lane & 7)) << 4));
+}
+// The int4 scale/zero word of group g of the slot for row `lane` (line 64 + g,
+// swizzled).
+__device__ __forceinline__ uint32_t slot_sz(const uint8_t* base, int lane, int g) {
+  return *reinterpret_cast<const uint32_t*>(base + CODE_BYTES + g * LINE + ((((lane >> 2) ^ (g & 7)) << 4) | ((lane & 3) << 2)));
+}
+__device__ __forceinline__ float sum4(float2 a, float2 b, float2 c, float2 d) {
+  return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
+}
+
+__device__ __forceinline__ float fold_sz(uint32_t sz, float dot, float xsum, float v) {
+  return fmaf(__uint_as_float(sz << 16), dot, fmaf(__uint_as_float(sz & 0xFFFF0000u), xsum, v));
+}
+
+// The work of one lane on one GEMV slot.  A warp's lanes are 8 row lanes x 4
+// K quarters: lane (rr = lane & 7, kq = lane >> 3) takes rows rr + 8 i
+// (i = 0..3) over the quarter's chunks 4 kq .. 4 kq + 3, so each input chunk
+// it reads from shared memory (x, the slot's inputs from its first K value)
+// serves four rows: a quarter of the input reads of one row per lane, and
+// sixteen independent accumulator chains.  Per row i: int4 v[i] += s *
+// (codes . x) + z * (sum of x) per group of G (a group never straddles a
+// quarter); int8 / bf16 acc[i][] collect the dot product (int8: bias, the
+// 128 * sum of x over the lane's chunks, is removed at the end).
+template <int DT>
+__device__ __forceinline__ void slot_dot(const uint8_t* base, int lane, int G, const float* x, const float* xs,
+                                         float* v, float2 (*acc)[2], float& bias) {
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  const float2 z2 = make_float2(0.f, 0.f);
+  const int rr = lane & 7, kq = lane >> 3;
+  if (DT == DT_INT4) {
+    const int cpg = G >> 5;
+    float ga[4] = {0.f, 0.f, 0.f, 0.f};  // the running group's code . x, per row
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const int u = kq * 4 + c;
+      const float4* xu = x4 + u * 8;
+      const float4 x0 = xu[0], x1 = xu[1], x2 = xu[2], x3 = xu[3], x4_ = xu[4], x5 = xu[5], x6 = xu[6], x7 = xu[7];
 #pragma unroll
-  for (int s = 16, n = 16; s >= 2; s >>= 1, n >>= 1) {
-    const bool hi = lane & s;
+      for (int i = 0; i < 4; ++i) {
+        const int r = rr + 8 * i;
+        const uint4 q = slot_chunk(base, r, u);
+        const float2 a0 = word_int4(q.x, x0, x1, z2), a1 = word_int4(q.y, x2, x3, z2);
+        const float2 a2 = word_int4(q.z, x4_, x5, z2), a3 = word_int4(q.w, x6, x7, z2);
+        const float sa = sum4(a0, a1, a2, a3);
+        if (cpg == 1) {
+          v[i] = fold_sz(slot_sz(base, r, u), sa, xs[u], v[i]);
+        } else {
+          ga[i] += sa;
+          if (((c + 1) & (cpg - 1)) == 0) {  // group end
+            const int g = u / cpg;
+            v[i] = fold_sz(slot_sz(base, r, g), ga[i], xs[g], v[i]);
+            ga[i] = 0.f;
+          }
+        }
+      }
+    }
+  } else if (DT == DT_INT8) {
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const int u = kq * 4 + c;
+      const float4* xu = x4 + u * 4;
+      const float4 x0 = xu[0], x1 = xu[1], x2 = xu[2], x3 = xu[3];
 #pragma unroll
-    for (int k = 0; k < n / 2; ++k) {
-      const float keep = hi ? v[k + n / 2] : v[k];
-      const float send = hi ? v[k] : v[k + n / 2];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+      for (int i = 0; i < 4; ++i) {
+        const uint4 q = slot_chunk(base, rr + 8 * i, u);
+        acc[i][0] = word_int8(q.x, x0, acc[i][0]);
+        acc[i][1] = word_int8(q.y, x1, acc[i][1]);
+        acc[i][0] = word_int8(q.z, x2, acc[i][0]);
+        acc[i][1] = word_int8(q.w, x3, acc[i][1]);
+      }
+      bias += xs[u];
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const int u = kq * 4 + c;
+      const float4 x0 = x4[u * 2], x1 = x4[u * 2 + 1];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 q = slot_chunk(base, rr + 8 * i, u);
+        acc[i][0] = word_bf16(q.x, lo2(x0), acc[i][0]);
+        acc[i][1] = word_bf16(q.y, hi2(x0), acc[i][1]);
+        acc[i][0] = word_bf16(q.z, lo2(x1), acc[i][0]);
+        acc[i][1] = word_bf16(q.w, hi2(x1), acc[i][1]);
+      }
     }
   }
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+// The row sums of a lane's four rows over the warp's K-slots of a tile, added
+// over the four K quarters; returns the total of row `lane` (lane l =
+// (rr, kq) holds row rr + 8 kq among its four).
+template <int DT>
+__device__ __forceinline__ float rows_total(const float* v, float2 (*acc)[2], float bias, int lane) {
+  float t[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    t[i] = DT == DT_INT4 ? v[i] : ((acc[i][0].x + acc[i][0].y) + (acc[i][1].x + acc[i][1].y)) - bias;
+    t[i] += __shfl_xor_sync(0xffffffffu, t[i], 8);
+    t[i] += __shfl_xor_sync(0xffffffffu, t[i], 16);
+  }
+  const int kq = lane >> 3;
+  return kq == 0 ? t[0] : kq == 1 ? t[1] : kq == 2 ? t[2] : t[3];
 }
 
 struct ArgMax {
@@ -808,8 +845,8 @@ __device__ __forceinline__ void amax_merge(ArgMax& a, float v, int i) {
   }
 }
 
-// Epilogue of one output row n (value y); lanes 0..15 call it together, each
-// with its own row of the half-tile; yp is the value of row n ^ 1.
+// Epilogue of one output row n (value y); every lane calls it, lane r for
+// row r of the tile; yp is the value of row n ^ 1 (its lane's partner).
 __device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, const Smem& S, int seg, int n, float y,
                                               float yp, int pos, float2 rp, ArgMax& am) {
   switch (ph.epi) {
@@ -866,159 +903,70 @@ __device__ __forceinline__ void gemv_epilogue(const Phase& ph, const Params& P, 
   }
 }
 
-// The work of one lane on one slot of Lb chunks per row: its chunk (number g
-// of the row) of every row of the slot.  One copy of this code serves every
-// slot width, which keeps the engine's hot code small.
-template <int DT>
-__device__ __forceinline__ void slot_rows(const uint8_t* base, int Lb, int lane, int g, const float4* xs4, const Smem& S,
-                                          float* v, float2* acc, float& bias) {
-  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
-  constexpr int U = E / 4;
-  const int L = Lb;
-  // The four words of the chunk go by in a run-time loop (a small loop body
-  // stays in the instruction cache); in step jw lane l reads word
-  // (jw + l / 8) % 4, so that the 32 lanes' 4-byte loads hit 32 banks.
-  const int sw = swz(g, U);
-  const uint32_t* wrow = reinterpret_cast<const uint32_t*>(base) + lane * 4;
-  float2 a[HROWS];  // int4: this chunk's sums; int8 / bf16: running sums
-#pragma unroll
-  for (int r = 0; r < HROWS; ++r) a[r] = DT == DT_INT4 ? make_float2(0.f, 0.f) : acc[r];
-#pragma unroll 1
-  for (int jw = 0; jw < 4; ++jw) {
-    const int ws = (jw + (lane >> 3)) & 3;
-    float2 xr[4];
-    if (DT == DT_INT4) {
-      const float4 xa = xs4[g * U + ((2 * ws) ^ sw)], xb = xs4[g * U + ((2 * ws + 1) ^ sw)];
-      xr[0] = make_float2(xa.x, xa.y);
-      xr[1] = make_float2(xa.z, xa.w);
-      xr[2] = make_float2(xb.x, xb.y);
-      xr[3] = make_float2(xb.z, xb.w);
-    } else if (DT == DT_INT8) {
-      const float4 xa = xs4[g * U + (ws ^ sw)];
-      xr[0] = make_float2(xa.x, xa.y);
-      xr[1] = make_float2(xa.z, xa.w);
-    } else {
-      const float4 xa = xs4[g * U + ((ws >> 1) ^ sw)];
-      xr[0] = (ws & 1) ? make_float2(xa.z, xa.w) : make_float2(xa.x, xa.y);
-    }
-#pragma unroll
-    for (int r = 0; r < HROWS; ++r) {
-      const uint32_t wv = wrow[r * L * 4 + ws];
-      if (DT == DT_INT4) a[r] = word_int4(wv, xr, a[r]);
-      else if (DT == DT_INT8) a[r] = word_int8(wv, xr, a[r]);
-      else a[r] = word_bf16(wv, xr, a[r]);
-    }
-  }
-  if (DT == DT_INT4) {
-    const float xg = S.xsum[g];
-    const uint32_t* szp = reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF) + lane;
-#pragma unroll
-    for (int r = 0; r < HROWS; ++r) {
-      const uint32_t sz = szp[r * L];
-      v[r] = fmaf(__uint_as_float(sz << 16), a[r].x + a[r].y, fmaf(__uint_as_float(sz & 0xFFFF0000u), xg, v[r]));
-    }
-  } else {
-    if (DT == DT_INT8) bias += S.xsum[g];
-#pragma unroll
-    for (int r = 0; r < HROWS; ++r) acc[r] = a[r];
-  }
+// kv group whose q/k/v rows tile lt (32 rows of the stacked q/k/v matrix) holds
+__device__ __forceinline__ int qkv_group(const Phase& ph, int lt) {
+  const int n0 = lt * TR, gq = ph.Hq / ph.Hkv;
+  if (n0 < ph.q_rows) return n0 / ph.hd / gq;
+  if (n0 < ph.q_rows + ph.kv_rows) return (n0 - ph.q_rows) / ph.hd;
+  return (n0 - ph.q_rows - ph.kv_rows) / ph.hd;
 }
 
-// Waits until combine buffer buf may take half-tile cs.useq (the last
-// combiner of half-tile useq - NTB hands it on).  Bounded.
-__device__ __forceinline__ bool tb_claim(const Smem& S, const Cons& cs, int buf, int* err) {
-  int ok = 1;
-  if (cs.lane == 0) {
-    volatile int* g = S.tbg + buf;
-    if (*g != (int)cs.useq) {
-      const uint64_t t0 = gtimer();
-      while (*g != (int)cs.useq) {
-        __nanosleep(32);
-        if (gtimer() - t0 > WAIT_NS) {
-          atomicCAS(err, 0, ERR_WAIT_COMBINE);
-          ok = 0;
-          break;
-        }
-      }
-    }
-    __threadfence_block();
-  }
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// One GEMV phase for this CTA.  Slot X of the stream (in producer order)
-// belongs to warp X % NCW.  A warp accumulates its K-blocks of a half-tile in
-// registers (16 rows per lane), reduces them over the lanes, and deposits the
-// 16 row sums in the half-tile's combine buffer; the last contributing warp
-// adds the deposits in warp order and runs the epilogue.
-// One half-tile (16 rows r0.. of tile lt of segment seg; its nb K-blocks are
-// the CTA's local slots j0 ..) for the calling warp: its K-blocks, the lane
-// reduction, the deposit, and for the last contributing warp the combine.
-// Returns -1 if a wait gave up, 1 for the combining warp (lanes r < 16 hold
-// in tot the row sum of row r0 + r, already multiplied by the row's output
-// factor, and in rp its RoPE pair), else 0.
+// One tile (32 rows lt*32.. of segment seg; its nb K-slots are the CTA's
+// local slots j0 ..) for the calling warp: its K-slots, the deposit, and for
+// the last contributing warp the combine.  Returns -1 if a wait gave up, 1
+// for the combining warp (lane r holds in tot the sum of row lt*32 + r,
+// already multiplied by the row's output factor, and in rp its RoPE pair),
+// else 0.
 template <int DT>
-__device__ __forceinline__ int gemv_half(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int seg, int lt,
-                                         int r0, int Rt, uint32_t j0, int pos, float& tot, float2& rp) {
-  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
-  const int C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
-  const int nseg = ph.moe == MOE_GU ? 2 : 1, Ns = ph.N / nseg;
+__device__ __forceinline__ int gemv_tile(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int seg, int Ns,
+                                         int lt, uint32_t j0, int pos, float& tot, float2& rp) {
+  const int nb = k_slots(DT, ph.K);
   const int lane = cs.lane, w = cs.warp;
-  const int own0 = (int)((cs.it + j0) % NCW);  // owner of K-block 0
-  const int bfirst = (w - own0 + NCW) % NCW;   // this warp's first K-block
-  const int ncontrib = nb < NCW ? nb : NCW;
+  const int own0 = (int)((cs.it + j0) % NCW);  // owner of K-slot 0
+  const int bfirst = (w - own0 + NCW) % NCW;   // this warp's first K-slot
   if (bfirst >= nb) return 0;
-  const float4* xs4 = reinterpret_cast<const float4*>(S.xs);
-  // int8 row scales of the segment's matrix (the chosen expert's, for MoE)
-  const uint16_t* s8 = ph.s8;
-  if (DT == DT_INT8 && ph.moe != MOE_NONE)
-    s8 += (size_t)S.bcast[32 + (ph.moe == MOE_GU ? seg : ph.moe - MOE_DOWN0)] * Ns;
+  const int ncontrib = nb < NCW ? nb : NCW;
+  const int n = lt * TR + lane;
   // the epilogue's own inputs, fetched now so that their latency is hidden
-  // behind the K-blocks: lane r < 16 for row r0 + r
+  // behind the K-slots
   float pf = cs.rnorm * (DT == DT_BF16 ? 1.0f : DQ_UP);  // RMSNorm, 2^64, int8 row scale
   rp = make_float2(1.f, 0.f);
-  {
-    const int n = lt * TR + r0 + lane;
-    if (lane < HROWS && r0 + lane < Rt) {
-      if (DT == DT_INT8) pf *= bf2f(s8[n]);
-      if (ph.epi == EPI_QKV && n < ph.q_rows + ph.kv_rows) {
-        const int nn = n < ph.q_rows ? n : n - ph.q_rows;
-        rp = P.rope[(size_t)pos * (ph.hd / 2) + (nn % ph.hd) / 2];
-      }
+  if (n < Ns) {
+    if (DT == DT_INT8) {
+      const uint16_t* s8 = ph.s8;
+      if (ph.moe != MOE_NONE) s8 += (size_t)S.bcast[32 + (ph.moe == MOE_GU ? seg : ph.moe - MOE_DOWN0)] * Ns;
+      pf *= bf2f(s8[n]);
+    }
+    if (ph.epi == EPI_QKV && n < ph.q_rows + ph.kv_rows) {
+      const int nn = n < ph.q_rows ? n : n - ph.q_rows;
+      rp = P.rope[(size_t)pos * (ph.hd / 2) + (nn % ph.hd) / 2];
     }
   }
-  // int4: v[r] collects s * (codes . x) + z * (sum of x) per group, x 2^-64;
-  // int8 / bf16: acc[r] collects the row's dot product over the blocks
-  float v[HROWS];
-  float2 acc[HROWS];
+  float vr[4] = {0.f, 0.f, 0.f, 0.f}, bias = 0.0f;
+  float2 acc[4][2];
 #pragma unroll
-  for (int r = 0; r < HROWS; ++r) {
-    v[r] = 0.0f;
-    acc[r] = make_float2(0.f, 0.f);
-  }
-  float bias = 0.0f;  // int8: 128 * sum x * 2^-64 over this lane's chunks
+  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
   for (int b = bfirst; b < nb; b += NCW) {
     const uint32_t it = cs.it + j0 + (uint32_t)b;
     const uint8_t* base;
     if (!slot_acquire(S, cs, it, P.err, base)) return -1;
-    const int Lb = min(KBLK, C - b * KBLK);
-    // lane l takes chunk l of every row of the slot (rows past the tile read
-    // in-bounds stale bytes of the slot and are discarded)
-    if (lane < Lb) slot_rows<DT>(base, Lb, lane, b * KBLK + lane, xs4, S, v, acc, bias);
+    const int k0 = b * slot_k(DT);
+    slot_dot<DT>(base, lane, ph.G, S.xs + k0, S.xsum + (DT == DT_INT4 ? k0 / ph.G : k0 / 16), vr, acc, bias);
     slot_release(S, cs, it);
   }
-  if (DT != DT_INT4) {
-#pragma unroll
-    for (int r = 0; r < HROWS; ++r) v[r] = (acc[r].x + acc[r].y) - bias;
-  }
-  // deposit this warp's 16 row sums, then the last contributor combines
-  const float y = warp_rows16(v, lane);
+  const float v = rows_total<DT>(vr, acc, bias, lane);
+  // deposit this warp's 32 row sums, then the last contributor combines
   const int buf = (int)(cs.useq % NTB);
-  float* tb = S.tb + (size_t)buf * NCW * HROWS;
-  // the buffer's previous half-tile has been combined (bounded wait; in
-  // practice it was long ago)
-  if (!tb_claim(S, cs, buf, P.err)) return -1;
-  if ((lane & 1) == 0) tb[w * HROWS + (lane >> 1)] = y;
+  float* tb = S.tb + (size_t)buf * NCW * TR;
+  // the buffer's previous tile has been combined (bounded wait; in practice
+  // it was long ago)
+  int ok = 1;
+  if (lane == 0) {
+    ok = smem_wait(S.tbg + buf, (int)cs.useq, false, P.err, cs.lim);
+    __threadfence_block();
+  }
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return -1;
+  tb[w * TR + lane] = v;
   __syncwarp();
   int last = 0;
   if (lane == 0) {
@@ -1029,12 +977,7 @@ __device__ __forceinline__ int gemv_half(const Phase& ph, const Params& P, const
   if (!last) return 0;
   __threadfence_block();
   float t = 0.0f;
-  if (lane < HROWS) {
-    for (int ww = 0; ww < NCW; ++ww) {
-      const int bw = (ww - own0 + NCW) % NCW;
-      if (bw < nb) t += tb[ww * HROWS + lane];
-    }
-  }
+  for (int c = 0; c < ncontrib; ++c) t += tb[((own0 + c) % NCW) * TR + lane];  // K order
   __syncwarp();
   if (lane == 0) {
     S.tbc[buf] = 0;
@@ -1045,241 +988,184 @@ __device__ __forceinline__ int gemv_half(const Phase& ph, const Params& P, const
   return 1;
 }
 
-// One GEMV phase for this CTA: its tiles (round-robin over the CTAs), two
-// half-tiles each; the combining warp of a half-tile runs the epilogue.
+// One GEMV phase for this CTA: its tiles (round-robin over the CTAs); the
+// combining warp of a tile runs the epilogue.
 template <int DT>
 __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta, int pos, ArgMax& am) {
-  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
-  const int G = P.nctas;
-  const int C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
-  const int nseg = ph.moe == MOE_GU ? 2 : 1, Ns = ph.N / nseg;
+  const int G = P.nctas, nb = k_slots(DT, ph.K);
+  int Ns;
+  int eseg[8];
+  gemv_segments(ph, P, S, Ns, eseg);
+  const int nseg = ph.moe == MOE_GU ? 2 : 1;
   const int tps = (Ns + TR - 1) / TR, ntiles = nseg * tps;
   const int lane = cs.lane;
   uint32_t j = 0;  // slot index within the phase
-  for (int t = first_unit(cta, ph.rot, G); t < ntiles; t += G) {
+  for (int t = first_unit(cta, ph.rot, G); t < ntiles; t += G, ++cs.useq, j += (uint32_t)nb) {
     const int seg = t / tps, lt = t % tps;
-    const int Rt = min(TR, Ns - lt * TR);
-    for (int h = 0; h * HROWS < Rt; ++h, ++cs.useq, j += (uint32_t)nb) {
-      float tot;
-      float2 rp;
-      const int k = gemv_half<DT>(ph, P, S, cs, seg, lt, h * HROWS, Rt, j, pos, tot, rp);
-      if (k < 0) return false;
-      if (k == 0) continue;
-      const int r = h * HROWS + lane, n = lt * TR + r;
-      const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
-      if (lane < HROWS && r < Rt) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, rp, am);
+    float tot;
+    float2 rp;
+    const int k = gemv_tile<DT>(ph, P, S, cs, seg, Ns, lt, j, pos, tot, rp);
+    if (k < 0) return false;
+    if (k == 0) continue;
+    const int n = lt * TR + lane;
+    const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
+    if (n < Ns) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, rp, am);
+    if (ph.headc) {  // q/k/v rows of this tile are in memory: count them for its kv group
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(ph.headc + qkv_group(ph, lt), 1u);
     }
   }
   cs.it += j;
   return true;
 }
 
-// One row of a down slot (DR rows of 16 columns: the SwiGLU outputs of one
-// gate/up tile) against those outputs, staged as the subnormal
-// dequantisation reads them (xr; xz: their sum for the int4 zeros, or 128
-// times it for the int8 offset), without the 2^64 and int8 row scale that the
-// phase end applies.
+// One row of a down piece (16 columns: the SwiGLU outputs of one gate/up
+// tile), its codes (q0, q1: int4 in q0.x/y, int8 in q0, bf16 in q0 and q1)
+// and int4 scale/zero word, against those outputs,
+// staged as the subnormal dequantisation reads them (xr; xz: their sum for
+// the int4 zeros, or 128 times it for the int8 offset), without the 2^64 and
+// int8 row scale that the phase end applies.
 template <int DT>
-__device__ __forceinline__ float down_row(const uint8_t* base, int rl, int DR, const float2* xr, float xz) {
+__device__ __forceinline__ float down_row(uint4 q0, uint4 q1, uint32_t sz, const float4* xr, float xz) {
   if (DT == DT_INT4) {
-    const uint2 q = reinterpret_cast<const uint2*>(base)[rl];
-    const uint32_t sz = reinterpret_cast<const uint32_t*>(base + (size_t)DR * 8)[rl];
-    const float2 a0 = word_int4(q.x, xr, make_float2(0.f, 0.f));
-    const float2 a1 = word_int4(q.y, xr + 4, make_float2(0.f, 0.f));
+    const float2 a0 = word_int4(q0.x, xr[0], xr[1], make_float2(0.f, 0.f));
+    const float2 a1 = word_int4(q0.y, xr[2], xr[3], make_float2(0.f, 0.f));
     return fmaf(__uint_as_float(sz << 16), (a0.x + a1.x) + (a0.y + a1.y), __uint_as_float(sz & 0xFFFF0000u) * xz);
   } else if (DT == DT_INT8) {
-    const uint4 q = reinterpret_cast<const uint4*>(base)[rl];
-    float2 a0 = word_int8(q.x, xr, make_float2(0.f, 0.f));
-    float2 a1 = word_int8(q.z, xr + 4, make_float2(0.f, 0.f));
-    a0 = word_int8(q.y, xr + 2, a0);
-    a1 = word_int8(q.w, xr + 6, a1);
+    float2 a0 = word_int8(q0.x, xr[0], make_float2(0.f, 0.f));
+    float2 a1 = word_int8(q0.z, xr[2], make_float2(0.f, 0.f));
+    a0 = word_int8(q0.y, xr[1], a0);
+    a1 = word_int8(q0.w, xr[3], a1);
     return ((a0.x + a1.x) + (a0.y + a1.y)) - xz;
   } else {
-    const uint4 q0 = reinterpret_cast<const uint4*>(base)[2 * rl], q1 = reinterpret_cast<const uint4*>(base)[2 * rl + 1];
-    float2 a0 = word_bf16(q0.x, xr, make_float2(0.f, 0.f));
-    float2 a1 = word_bf16(q1.x, xr + 4, make_float2(0.f, 0.f));
-    a0 = word_bf16(q0.y, xr + 1, a0);
-    a1 = word_bf16(q1.y, xr + 5, a1);
-    a0 = word_bf16(q0.z, xr + 2, a0);
-    a1 = word_bf16(q1.z, xr + 6, a1);
-    a0 = word_bf16(q0.w, xr + 3, a0);
-    a1 = word_bf16(q1.w, xr + 7, a1);
+    float2 a0 = word_bf16(q0.x, lo2(xr[0]), make_float2(0.f, 0.f));
+    float2 a1 = word_bf16(q1.x, lo2(xr[2]), make_float2(0.f, 0.f));
+    a0 = word_bf16(q0.y, hi2(xr[0]), a0);
+    a1 = word_bf16(q1.y, hi2(xr[2]), a1);
+    a0 = word_bf16(q0.z, lo2(xr[1]), a0);
+    a1 = word_bf16(q1.z, lo2(xr[3]), a1);
+    a0 = word_bf16(q0.w, hi2(xr[1]), a0);
+    a1 = word_bf16(q1.w, hi2(xr[3]), a1);
     return (a0.x + a1.x) + (a0.y + a1.y);
   }
 }
 
+
 // A dense FFN in one phase (PH_FFN).  For each of this CTA's gate/up tiles
-// (round-robin): the two half-tiles as in a GEMV phase, whose combining warps
-// write silu(gate) * up of their 8 pairs into a shared buffer instead of
-// memory; then the tile's 16-column slice of the down projection, split into
-// slots of rows: lane l takes rows l, l + 32, ... of a slot, multiplies the
-// slot's codes by the 16 SwiGLU outputs (dequantised as in the GEMV) and adds
-// into the CTA's partial down outputs in shared memory.  At the end the CTA
-// adds its partial outputs to the residual (vector atomics): the down
-// projection needs no phase, no grid barrier and no staging of its own.
+// (round-robin): its K-slots as in a GEMV phase, whose combining warp writes
+// silu(gate) * up of the tile's 16 pairs into a shared buffer instead of
+// memory; then (one tile behind, so that those outputs are ready) the tile's
+// 16-column slice of the down projection, one piece per warp: warp w always
+// gets the rows w RW .., lane l rows l, l + 32, ..., and adds their products
+// with the 16 outputs into the CTA's partial down outputs in shared memory
+// (each row has one writer: no atomics, no ordering between warps).  At the
+// end the CTA adds its partial outputs to the residual (vector atomics): the
+// down projection needs no phase, no grid barrier and no staging of its own.
 template <int DT>
 __device__ bool ffn_phase(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta, int pos) {
-  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
-  const int G = P.nctas, C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
+  const int G = P.nctas, nb = k_slots(DT, ph.K);
   const int tps = ph.N / TR, d = ph.N2;
-  int nsl, DR;
-  ffn_split(DT, d, nsl, DR);
+  const FfnSplit fs = ffn_split(DT, d);
+  const int ND = NCW * fs.P;
   const int lane = cs.lane, w = cs.warp;
-  // The CTA's partial down outputs.  int8 / bf16 slots add in turn with plain
-  // adds (below), into two buffers where they fit (local tile kp into buffer
-  // kp % nbuf); int4 slots, whose tiles span fewer slots, use shared atomic
-  // adds into one buffer (measured faster on this path; the order of the adds
-  // then varies, the sum only by rounding).
-  constexpr bool ORDERED = DT != DT_INT4;
-  const int nbuf = ORDERED && ph.K + d + ffn_smem_floats(d) <= KMAX ? 2 : 1;
-  float* dacc = S.xs + ph.K;   // [nbuf][d]
-  float* hb = dacc + nbuf * d;  // [FFN_HN][16] SwiGLU outputs of the tiles in flight
-  int* hcnt = reinterpret_cast<int*>(hb + FFN_HN * 16);  // [FFN_HN] half-tiles finished per buffer
-  // dturn[b][k]: tiles of buffer b whose down slot k has been added; the
-  // buffer's next tile waits for it, so each row of a buffer is added to by
-  // one warp at a time, tile after tile (plain adds, a fixed order), while
-  // with two buffers consecutive tiles never wait for each other
-  int* dturn = hcnt + FFN_HN;  // [2][FFN_MAXSL]
-  for (int i = cs.ctid; i < nbuf * d; i += NCW * 32) dacc[i] = 0.0f;
-  if (cs.ctid < FFN_HN) hcnt[cs.ctid] = 0;
-  if (cs.ctid < 2 * FFN_MAXSL) dturn[cs.ctid] = 0;
+  float* hb = S.xs + round_up(ph.K, slot_k(DT));          // [FFN_HN][16] SwiGLU outputs of the tiles in flight
+  int* hcnt = reinterpret_cast<int*>(hb + FFN_HN * 16);   // [FFN_HN] rounds of each buffer written
+  int* dcnt = hcnt + FFN_HN;                              // [FFN_HN] down pieces of each buffer finished
+  float* dacc = reinterpret_cast<float*>(dcnt + FFN_HN);  // [d] this CTA's partial down outputs
+  for (int i = cs.ctid; i < d; i += NCW * 32) dacc[i] = 0.0f;
+  if (cs.ctid < 2 * FFN_HN) hcnt[cs.ctid] = 0;
   if (!cta_sync(S, cs, P.err)) return false;
-  uint32_t j = 0;
-  int kt = 0;  // this CTA's tiles so far
-  // the down slice of local tile kp (buffer e), slots j .. j + nsl - 1
-  auto down = [&](int kp) -> bool {
-    const int e = kp % FFN_HN, target = 2 * (kp / FFN_HN + 1);
-    for (int k = (w - (int)((cs.it + j) % NCW) + NCW) % NCW; k < nsl; k += NCW) {
-      // this tile's SwiGLU outputs (both half-tiles combined; bounded wait)
-      int ok = 1;
-      if (lane == 0) {
-        volatile int* c = hcnt + e;
-        if (*c < target) {
-          const uint64_t t0 = gtimer();
-          while (*c < target) {
-            __nanosleep(32);
-            if (gtimer() - t0 > WAIT_NS) {
-              atomicCAS(P.err, 0, ERR_WAIT_COMBINE);
-              ok = 0;
-              break;
-            }
-          }
-        }
-        __threadfence_block();
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-      float hv[16];
+  const int first = first_unit(cta, ph.rot, G), nt = units_of(first, tps, G);
+  const uint32_t X0 = cs.it;
+  // the down pieces of local tile i for this warp
+  auto down = [&](int i) -> bool {
+    const int e = i % FFN_HN;
+    const uint32_t pd = (i + 1 < nt) ? (uint32_t)((i + 2) * nb + i * ND) : (uint32_t)(nt * nb + i * ND);
+    const int m0 = (w - (int)((X0 + pd) % NCW) + NCW) % NCW;
+    // this tile's SwiGLU outputs (bounded wait)
+    int ok = 1;
+    if (lane == 0) {
+      ok = smem_wait(hcnt + e, i / FFN_HN + 1, true, P.err, cs.lim);
+      __threadfence_block();
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    // the outputs as the subnormal dequantisation reads them (natural k order)
+    float4 xr[4];
+    float hs = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 16; c += 4) {
-        const float4 t4 = reinterpret_cast<const float4*>(hb)[e * 4 + c / 4];
-        hv[c] = t4.x;
-        hv[c + 1] = t4.y;
-        hv[c + 2] = t4.z;
-        hv[c + 3] = t4.w;
-      }
-      // the inputs as the subnormal dequantisation reads them (natural k order)
-      float2 xr[8];
-      float hs = 0.0f;
-#pragma unroll
-      for (int c = 0; c < 16; c += 4) {
-        const float4 m = dq_mult(DT, DT == DT_INT4 ? (c >> 2) & 1 : 0);
-        xr[c / 2] = make_float2(hv[c] * m.x, hv[c + 1] * m.y);
-        xr[c / 2 + 1] = make_float2(hv[c + 2] * m.z, hv[c + 3] * m.w);
-        hs += (hv[c] + hv[c + 1]) + (hv[c + 2] + hv[c + 3]);
-      }
-      const float xz = DT == DT_INT4 ? hs * DQ_DOWN : DT == DT_INT8 ? 128.0f * hs * DQ_DOWN : 0.0f;
-      const uint32_t it = cs.it + j + (uint32_t)k;
+    for (int c = 0; c < 4; ++c) {
+      const float4 t4 = reinterpret_cast<const float4*>(hb)[e * 4 + c];
+      const float4 m = dq_mult(DT, DT == DT_INT4 ? c & 1 : 0);
+      xr[c] = make_float4(t4.x * m.x, t4.y * m.y, t4.z * m.z, t4.w * m.w);
+      hs += (t4.x + t4.y) + (t4.z + t4.w);
+    }
+    const float xz = DT == DT_INT4 ? hs * DQ_DOWN : DT == DT_INT8 ? 128.0f * hs * DQ_DOWN : 0.0f;
+    for (int k = 0; k < fs.P; ++k) {
+      const uint32_t it = X0 + pd + (uint32_t)(m0 + k * NCW);
       const uint8_t* base;
       if (!slot_acquire(S, cs, it, P.err, base)) return false;
-      // the buffer's previous tile has added its slot k (bounded wait)
-      const int bsel = kp % nbuf, turn = kp / nbuf;
-      float* acc = dacc + bsel * d;
-      int* tp = dturn + bsel * FFN_MAXSL + k;
-      if (ORDERED && lane == 0) {
-        volatile int* c = tp;
-        if (*c != turn) {
-          const uint64_t t0 = gtimer();
-          while (*c != turn) {
-            __nanosleep(32);
-            if (gtimer() - t0 > WAIT_NS) {
-              atomicCAS(P.err, 0, ERR_WAIT_COMBINE);
-              ok = 0;
-              break;
-            }
-          }
-        }
-        __threadfence_block();
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-      const int r0 = k * DR, nr = min(DR, d - r0);
-      if (!ORDERED) {
+      int r0, r1;
+      ffn_piece(fs, d, w, k, r0, r1);
+      const int nr = r1 - r0;
 #pragma unroll 4
-        for (int i = 0; i * 32 < nr; ++i) {
-          const int rl = lane + 32 * i;
-          if (rl < nr) atomicAdd(acc + r0 + rl, down_row<DT>(base, rl, DR, xr, xz));
+      for (int rl = lane; rl < nr; rl += 32) {
+        uint4 q0, q1 = make_uint4(0u, 0u, 0u, 0u);
+        uint32_t sz = 0u;
+        if (DT == DT_INT4) {
+          const uint2 t = reinterpret_cast<const uint2*>(base)[rl];
+          q0 = make_uint4(t.x, t.y, 0u, 0u);
+          sz = reinterpret_cast<const uint32_t*>(base + (size_t)fs.PR * 8)[rl];
+        } else {
+          q0 = reinterpret_cast<const uint4*>(base)[rl];
+          if (DT == DT_BF16) q1 = reinterpret_cast<const uint4*>(base + (size_t)fs.PR * 16)[rl];
         }
-      }
-      // groups of four rows per lane: their loads (codes, scales and the
-      // partial outputs, which no other warp touches now) go out first
-      for (int i0 = 0; ORDERED && i0 * 32 < nr; i0 += 4) {
-        float c[4], a0[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int rl = lane + 32 * (i0 + u);
-          c[u] = 0.f;
-          a0[u] = 0.f;
-          if (rl < nr) {
-            a0[u] = acc[r0 + rl];
-            c[u] = down_row<DT>(base, rl, DR, xr, xz);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int rl = lane + 32 * (i0 + u);
-          if (rl < nr) acc[r0 + rl] = a0[u] + c[u];
-        }
-      }
-      __syncwarp();
-      if (ORDERED && lane == 0) {
-        __threadfence_block();
-        *reinterpret_cast<volatile int*>(tp) = turn + 1;
+        dacc[r0 + rl] += down_row<DT>(q0, q1, sz, xr, xz);
       }
       slot_release(S, cs, it);
     }
-    j += (uint32_t)nsl;
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      atomicAdd(dcnt + e, 1);
+    }
     return true;
   };
-  for (int t = first_unit(cta, ph.rot, G); t < tps; t += G, ++kt) {
-    const int e = kt % FFN_HN;
-    for (int h = 0; h < 2; ++h, ++cs.useq, j += (uint32_t)nb) {
-      float tot;
-      float2 rp;
-      const int k = gemv_half<DT>(ph, P, S, cs, 0, t, h * HROWS, TR, j, pos, tot, rp);
-      if (k < 0) return false;
-      if (k == 0) continue;
+  for (int i = 0; i < nt; ++i, ++cs.useq) {
+    const int t = first + i * G;
+    const uint32_t pg = (uint32_t)(i * nb + (i > 0 ? (i - 1) * ND : 0));
+    float tot;
+    float2 rp;
+    const int k = gemv_tile<DT>(ph, P, S, cs, 0, ph.N, t, pg, pos, tot, rp);
+    if (k < 0) return false;
+    if (k == 1) {
+      const int e = i % FFN_HN;
+      // the buffer's previous round has been read by every warp (bounded)
+      int ok = 1;
+      if (lane == 0) {
+        ok = smem_wait(dcnt + e, NCW * (i / FFN_HN), true, P.err, cs.lim);
+        __threadfence_block();
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
       const float up = __shfl_xor_sync(0xffffffffu, tot, 1);
-      if (lane < HROWS && (lane & 1) == 0) hb[e * 16 + h * 8 + (lane >> 1)] = tot / (1.0f + expf(-tot)) * up;
+      if ((lane & 1) == 0) hb[e * 16 + (lane >> 1)] = tot / (1.0f + expf(-tot)) * up;
       __syncwarp();
       if (lane == 0) {
         __threadfence_block();
-        atomicAdd(hcnt + e, 1);
+        *reinterpret_cast<volatile int*>(hcnt + e) = i / FFN_HN + 1;
       }
     }
-    // the previous tile's down slice follows this tile's gate/up blocks
-    if (kt > 0 && !down(kt - 1)) return false;
+    // the previous tile's down slice follows this tile's gate/up slots
+    if (i > 0 && !down(i - 1)) return false;
   }
-  if (kt > 0 && !down(kt - 1)) return false;
-  cs.it += j;
+  if (nt > 0 && !down(nt - 1)) return false;
+  cs.it += (uint32_t)(nt * (nb + ND));
   // every warp's partial outputs are in dacc: add them to the residual
   if (!cta_sync(S, cs, P.err)) return false;
-  if (kt > 0) {
+  if (nt > 0) {
     float4* out = reinterpret_cast<float4*>(ph.out);
     for (int n4 = cs.ctid; n4 < d / 4; n4 += NCW * 32) {
       float4 v = reinterpret_cast<const float4*>(dacc)[n4];
-      if (nbuf == 2) {
-        const float4 v1 = reinterpret_cast<const float4*>(dacc + d)[n4];
-        v = make_float4(v.x + v1.x, v.y + v1.y, v.z + v1.z, v.w + v1.w);
-      }
       if (DT != DT_BF16) {
         float f[4] = {DQ_UP, DQ_UP, DQ_UP, DQ_UP};
         if (DT == DT_INT8) {
@@ -1299,8 +1185,8 @@ __device__ bool ffn_phase(const Phase& ph, const Params& P, const Smem& S, Cons&
 
 // ----------------------------------------------------------- attention ---
 // One unit = one query row x one kv head x one chunk of positions.  Each slot
-// (16 positions of K and V) belongs to the warp given by its stream index.
-// A warp takes the 16 positions of a block at once: lane l holds dims
+// (16 positions of K and V) belongs to the warp given by its stream index.  A
+// warp takes the positions of a slot at once: lane l holds dims
 // l*DPL .. l*DPL+DPL-1 (DPL = HD/32) of every position; it forms the 16
 // partial dot products of its dims, a reduce-scatter over the lanes leaves
 // lane l with the score of position l/2, and the block updates the warp's
@@ -1309,6 +1195,21 @@ __device__ bool ffn_phase(const Phase& ph, const Params& P, const Smem& S, Cons&
 // from its lane.  The warps merge in shared memory; a head split over several
 // chunks merges its chunks' (m, l, o) in the CTA that finishes last
 // (log-sum-exp combine).
+// Sums each of 16 per-lane values over the 32 lanes; afterwards lane l holds
+// the total of value l >> 1.
+__device__ __forceinline__ float warp_rows16(float v[16], int lane) {
+#pragma unroll
+  for (int s = 16, n = 16; s >= 2; s >>= 1, n >>= 1) {
+    const bool hi = lane & s;
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float keep = hi ? v[k + n / 2] : v[k];
+      const float send = hi ? v[k] : v[k + n / 2];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
 // Rows of one block, this lane's dims (bf16 pairs): NP positions of K or V.
 template <int HD, int NP>
 struct AttnRows {
@@ -1401,7 +1302,7 @@ __device__ __forceinline__ void attn_values(const AttnRows<HD, NP>& vr, int gq, 
   }
 }
 
-template <int HD>
+template <int HD, bool VER>
 __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, const AttnUnit& au, int pos,
                           uint32_t& j) {
   constexpr int DPL = HD / 32;
@@ -1412,7 +1313,18 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   const size_t qrow = (size_t)au.m * ph.Hq * HD;  // this unit's query / output row
   float* qs = S.xs;                       // [gq][HD], pre-scaled by 1/sqrt(HD)
   float* sc = S.xs + MAX_GQ * HD;         // [NCW][gq][HD + 2]
-  const int nslots = pe > p0 ? (pe - p0 + ATT_POS_PER_SLOT - 1) / ATT_POS_PER_SLOT : 0;
+  constexpr int APS = att_slot_pos(HD);  // positions of K and V in a slot
+  const int nslots = pe > p0 ? (pe - p0 + APS - 1) / APS : 0;
+  // the q/k/v rows of this kv group written during this launch (by the
+  // q/k/v tiles of every CTA, in the same phase): bounded wait on the group's
+  // tile count
+  if (ph.headc) {
+    int ok = 1;
+    if (cs.ctid == 0)
+      ok = counter_wait(ph.headc + kvh, (unsigned)((gq + 2) * (HD / TR)), P.err, ERR_WAIT_HEAD, cs.lim);
+    S.bcast[1] = ok;
+    if (!cta_sync(S, cs, P.err) || !S.bcast[1]) return false;
+  }
   // positions not streamed (rows written during this launch, at most 8) go
   // to the warp after the last slot's owner, which loads them right away
   const int pg = max(pe, p0);
@@ -1420,7 +1332,7 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   const bool has_g = (w == gw) && pg < p1;
   // rows written during this launch: a verify pass's own rows (at most
   // MAX_M) or a decode step's current row
-  constexpr int NPG = MAX_M;
+  constexpr int NPG = VER ? MAX_M : 1;
   AttnRows<HD, NPG> gk, gv;
   if (has_g) {
     const size_t off = ((size_t)kvh * ph.Tmax + pg) * HD;
@@ -1454,20 +1366,20 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   }
   for (int k = (w - (int)((cs.it + j) % NCW) + NCW) % NCW; k < nslots; k += NCW) {
     const uint32_t it = cs.it + j + (uint32_t)k;
-    const int np = min(ATT_POS_PER_SLOT, pe - (p0 + k * ATT_POS_PER_SLOT));
+    const int np = min(APS, pe - (p0 + k * APS));
     const uint8_t* base;
     if (!slot_acquire(S, cs, it, P.err, base)) return false;
     const uint16_t* kb = reinterpret_cast<const uint16_t*>(base);
     {
-      AttnRows<HD, ATT_POS_PER_SLOT> kr;
-      attn_rows<HD, ATT_POS_PER_SLOT, false>(kr, kb, np, lane);
-      attn_scores<HD, ATT_POS_PER_SLOT>(kr, np, gq, q, m, l, pr, cr, lane);
+      AttnRows<HD, APS> kr;
+      attn_rows<HD, APS, false>(kr, kb, np, lane);
+      attn_scores<HD, APS>(kr, np, gq, q, m, l, pr, cr, lane);
     }
     {
-      AttnRows<HD, ATT_POS_PER_SLOT> vr;
-      attn_rows<HD, ATT_POS_PER_SLOT, false>(vr, kb + ATT_POS_PER_SLOT * HD, np, lane);
+      AttnRows<HD, APS> vr;
+      attn_rows<HD, APS, false>(vr, kb + APS * HD, np, lane);
       slot_release(S, cs, it);  // the slot's rows are in registers
-      attn_values<HD, ATT_POS_PER_SLOT>(vr, gq, pr, cr, o);
+      attn_values<HD, APS>(vr, gq, pr, cr, o);
     }
   }
   j += (uint32_t)nslots;
@@ -1540,27 +1452,45 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   return true;
 }
 
+// Attention runs out of line, on copies of the consumer state, so that its
+// register needs (per-position rows, softmax state of up to four heads) do
+// not push the GEMV loops' values out to local memory.
+struct AttnRet {
+  uint32_t j, cphase, starved;
+  int ok;
+};
+template <int HD, bool VER>
+__device__ __noinline__ AttnRet attn_call(const Phase& ph, const Params& P, const Smem S, Cons cs, const AttnUnit au,
+                                          int pos, uint32_t j) {
+  AttnRet r;
+  r.ok = attn_unit<HD, VER>(ph, P, S, cs, au, pos, j);
+  r.j = j;
+  r.cphase = cs.cphase;
+  r.starved = cs.starved;
+  return r;
+}
+
 // ========================================================= verify pass ====
 // A speculative-verification pass (gpt-fast README, "Speculative sampling")
 // feeds M rows (the last accepted token and the drafts) at positions
 // pos..pos+M-1 through every layer with ONE stream of the weights.  GEMV
-// phases then work K-block by K-block over groups of up to VTG tiles: the
-// CTA stages the K-block's inputs of all M rows (fp32, swizzled per chunk),
-// each slot's owner warp dequantises its codes once and multiplies them with
-// the M rows, reduces over its lanes and adds the row sums into a shared
-// accumulator (each (row, m) has one writer per K-block, K-blocks in order:
-// deterministic); the group's epilogues then run per (row, m).
+// phases then work K-slot by K-slot over groups of up to VTG tiles: the CTA
+// stages the K-slot's inputs of all M rows (fp32, times the dequantisation
+// powers), each slot's owner warp dequantises its codes once (lane r: row r)
+// and multiplies them with the M rows, and adds its rows' M sums into a
+// shared accumulator (each (row, m) has one writer per K-slot, K-slots in
+// order: deterministic); the group's epilogues then run per (row, m).
 struct VS {
-  float* xk;    // [MAX_M][KBLK chunks][E] inputs of the current K-block
-  float* xgk;   // [MAX_M][KBLK] chunk sums of the inputs, as S.xsum
+  float* xk;    // [MAX_M][512] inputs of the current K-slot (256 used)
+  float* xgk;   // [MAX_M][32] sums of the inputs per int4 group / int8 chunk, as S.xsum
   float* acc;   // [VTG * TR][MAX_M] row sums of the tile group
   float* rfac;  // [MAX_M] RMSNorm factors
 };
 __device__ __forceinline__ VS vsmem(const Smem& S) {
   VS v;
   v.xk = S.xs;
-  v.xgk = v.xk + MAX_M * KBLK * 32;
-  v.acc = v.xgk + MAX_M * KBLK;
+  v.xgk = v.xk + MAX_M * 512;
+  v.acc = v.xgk + MAX_M * 32;
   v.rfac = v.acc + VTG * TR * MAX_M;
   return v;
 }
@@ -1708,19 +1638,16 @@ __device__ __forceinline__ void gemv_epilogue_m(const Phase& ph, const Params& P
 template <int DT>
 __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta, int pos, int pi,
                              ArgMax* am) {
-  constexpr int E = DT == DT_BF16 ? 8 : DT == DT_INT8 ? 16 : 32;
-  constexpr int U = E / 4;
-  constexpr int WP = E / 8;  // input pairs per 32-bit word of codes
+  constexpr int SK = slot_k(DT);  // K values per slot
   const VS V = vsmem(S);
-  const int M = P.M;
-  const int C = ph.K / E, nb = (C + KBLK - 1) / KBLK;
+  const int M = P.M, K = ph.K, Gq = ph.G;
+  const int nb = k_slots(DT, K);
   const int lane = cs.lane, w = cs.warp;
   if ((ph.xsrc == X_NORM || ph.xsrc == X_EMBED_NORM) && !verify_norm(ph, P, S, cs, cta)) return false;
   if (ph.moe == MOE_GU && !verify_route(ph, P, S, cs, pi)) return false;
   int Ns;
-  const uint8_t* wseg[8];
   int eseg[8];
-  const int nseg = gemv_segments(ph, P, S, Ns, wseg, eseg);
+  const int nseg = gemv_segments(ph, P, S, Ns, eseg);
   TileGroups tg;
   tg.tps = (Ns + TR - 1) / TR;
   tg.ntiles = nseg * tg.tps;
@@ -1733,130 +1660,103 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
     const int i1 = group_end(tg, i0);
     const int seg = (tg.first + i0 * tg.G) / tg.tps, e = eseg[seg];
     for (int b = 0; b < nb; ++b) {
-      const int Lb = min(KBLK, C - b * KBLK);
-      // stage the K-block's inputs of the M rows
-      const int per_m = KBLK * U;  // float4 per row
-      for (int q0 = 0; q0 < MAX_M * per_m; q0 += NCW * 32) {
-        const int q = q0 + cs.ctid, m = q / per_m, f4 = q % per_m, l = f4 / U, u = f4 % U;
-        const bool ok = m < M && l < Lb;
+      // stage the K-slot's inputs of the M rows, zero past K (whole warps of
+      // consecutive float4, so that group sums shuffle within a warp)
+      const int per_m = SK / 4;  // float4 per row
+      for (int q0 = 0; q0 < M * per_m; q0 += NCW * 32) {
+        const int q = q0 + cs.ctid, m = q / per_m, f4 = q % per_m;
+        const bool st = m < M, ok = st && b * per_m + f4 < K / 4;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ok) a = vin4(ph, P, V, m, e, (b * KBLK + l) * U + u);
-        const float4 mu = dq_mult(DT, u);
-        if (ok)
-          reinterpret_cast<float4*>(V.xk)[m * per_m + l * U + (u ^ swz(l, U))] =
-              make_float4(a.x * mu.x, a.y * mu.y, a.z * mu.z, a.w * mu.w);
-        if (DT != DT_BF16) {  // chunk sums as in stage_store
+        if (ok) a = vin4(ph, P, V, m, e, b * per_m + f4);
+        const float4 mu = dq_mult(DT, f4 & 7);
+        if (st) reinterpret_cast<float4*>(V.xk)[m * per_m + f4] = make_float4(a.x * mu.x, a.y * mu.y, a.z * mu.z, a.w * mu.w);
+        if (DT != DT_BF16) {  // group / chunk sums as in stage_store
           float sg = a.x + a.y + a.z + a.w;
-          sg += __shfl_xor_sync(0xffffffffu, sg, 1);
-          sg += __shfl_xor_sync(0xffffffffu, sg, 2);
-          if (DT == DT_INT4) sg += __shfl_xor_sync(0xffffffffu, sg, 4);
-          if (ok && (lane & (U - 1)) == 0) V.xgk[m * KBLK + l] = sg * (DT == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
+          const int span = DT == DT_INT4 ? Gq / 4 : 4;
+          for (int o = 1; o < span; o <<= 1) sg += __shfl_xor_sync(0xffffffffu, sg, o);
+          if (st && (lane & (span - 1)) == 0)
+            V.xgk[m * 32 + (4 * f4) / (DT == DT_INT4 ? Gq : 16)] = sg * (DT == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
         }
       }
       if (!cta_sync(S, cs, P.err)) return false;
-      for (int i = i0; i < i1; ++i) {
-        const int t = tg.first + i * tg.G, lt = t % tg.tps;
-        const int Rt = min(TR, Ns - lt * TR);
-        for (int h = 0; h * HROWS < Rt; ++h, ++j) {
-          const uint32_t it = cs.it + j;
-          if ((int)(it % NCW) != w) continue;
-          const uint8_t* base;
-          if (!slot_acquire(S, cs, it, P.err, base)) return false;
-          const bool lane_ok = lane < Lb;
-          const int sw = swz(lane, U);
-          const uint32_t* wbase = reinterpret_cast<const uint32_t*>(base) + lane * 4;
-#pragma unroll 1
-          for (int rb = 0; rb < HROWS; rb += 4) {
-            float2 a[4][MAX_M];
+      for (int i = i0; i < i1; ++i, ++j) {
+        const uint32_t it = cs.it + j;
+        if ((int)(it % NCW) != w) continue;
+        const uint8_t* base;
+        if (!slot_acquire(S, cs, it, P.err, base)) return false;
+        float2 a[MAX_M];
+        float v[MAX_M];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-              for (int m = 0; m < MAX_M; ++m) a[r][m] = make_float2(0.f, 0.f);
+        for (int m = 0; m < MAX_M; ++m) {
+          a[m] = make_float2(0.f, 0.f);
+          v[m] = 0.f;
+        }
+        const int cpg = DT == DT_INT4 ? Gq / 32 : 1;
 #pragma unroll 1
-            for (int jw0 = 0; jw0 < 4; ++jw0) {
-              const int jw = (jw0 + (lane >> 3)) & 3;  // per-lane word order: conflict-free loads
-              float2 xp[MAX_M][WP];
+        for (int u = 0; u < SLOT_CHUNKS; ++u) {
+          const uint4 qv = slot_chunk(base, lane, u);
+          const uint32_t wq[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+          for (int jw = 0; jw < 4; ++jw) {
+            const uint32_t wv = wq[jw];
+            if (DT == DT_INT4) {  // the subnormal reading of word_int4
+              const uint32_t hv = wv >> 8;
+              const float2 c0 = bits2(wv & 0x0000000Fu, wv & 0x000000F0u), c1 = bits2(wv & 0x00000F00u, wv & 0x0000F000u);
+              const float2 c2 = bits2(wv & 0x000F0000u, wv & 0x00F00000u), c3 = bits2(hv & 0x000F0000u, hv & 0x00F00000u);
 #pragma unroll
               for (int m = 0; m < MAX_M; ++m) {
                 if (m < M) {
-                  const float4* xm = xk4 + m * (KBLK * U) + lane * U;
-                  if (DT == DT_INT4) {
-                    const float4 xa = xm[(2 * jw) ^ sw], xb = xm[(2 * jw + 1) ^ sw];
-                    xp[m][0] = make_float2(xa.x, xa.y);
-                    xp[m][1 % WP] = make_float2(xa.z, xa.w);
-                    xp[m][2 % WP] = make_float2(xb.x, xb.y);
-                    xp[m][3 % WP] = make_float2(xb.z, xb.w);
-                  } else if (DT == DT_INT8) {
-                    const float4 xa = xm[jw ^ sw];
-                    xp[m][0] = make_float2(xa.x, xa.y);
-                    xp[m][1 % WP] = make_float2(xa.z, xa.w);
-                  } else {
-                    const float4 xa = xm[(jw >> 1) ^ sw];
-                    xp[m][0] = (jw & 1) ? make_float2(xa.z, xa.w) : make_float2(xa.x, xa.y);
-                  }
-                } else {
-#pragma unroll
-                  for (int i2 = 0; i2 < WP; ++i2) xp[m][i2] = make_float2(0.f, 0.f);
+                  const float4* xm = xk4 + m * (SK / 4) + u * 8 + 2 * jw;
+                  const float4 xa = xm[0], xb = xm[1];
+                  a[m] = ffma2(c0, lo2(xa), a[m]);
+                  a[m] = ffma2(c1, hi2(xa), a[m]);
+                  a[m] = ffma2(c2, lo2(xb), a[m]);
+                  a[m] = ffma2(c3, hi2(xb), a[m]);
                 }
               }
-#pragma unroll
-              for (int r = 0; r < 4; ++r) {
-                const uint32_t wv = wbase[(rb + r) * Lb * 4 + jw];
-                float2 qv[WP];
-                if (DT == DT_INT4) {  // the subnormal reading of word_int4
-                  const uint32_t hv = wv >> 8;
-                  qv[0] = bits2(wv & 0x0000000Fu, wv & 0x000000F0u);
-                  qv[1 % WP] = bits2(wv & 0x00000F00u, wv & 0x0000F000u);
-                  qv[2 % WP] = bits2(wv & 0x000F0000u, wv & 0x00F00000u);
-                  qv[3 % WP] = bits2(hv & 0x000F0000u, hv & 0x00F00000u);
-                } else if (DT == DT_INT8) {  // as word_int8
-                  const uint32_t w8 = wv, hv = w8 >> 8;
-                  qv[0] = bits2(w8 & 0x000000FFu, w8 & 0x0000FF00u);
-                  qv[1 % WP] = bits2(w8 & 0x00FF0000u, hv & 0x00FF0000u);
-                } else {
-                  qv[0] = bits2(wv << 16, wv & 0xFFFF0000u);
-                }
-#pragma unroll
-                for (int m = 0; m < MAX_M; ++m)
-#pragma unroll
-                  for (int i2 = 0; i2 < WP; ++i2) a[r][m] = ffma2(qv[i2], xp[m][i2], a[r][m]);
-              }
-            }
-            // per (row, m) contributions, then a reduce-scatter over the lanes:
-            // lane l ends with the total of row l >> 3 of the batch, input row l & 7
-            float v[32];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              uint32_t sz = 0u;
-              if (DT == DT_INT4) sz = reinterpret_cast<const uint32_t*>(base + SLOT_SZ_OFF)[(rb + r) * Lb + lane];
+            } else if (DT == DT_INT8) {  // as word_int8
+              const uint32_t hv = wv >> 8;
+              const float2 c0 = bits2(wv & 0x000000FFu, wv & 0x0000FF00u), c1 = bits2(wv & 0x00FF0000u, hv & 0x00FF0000u);
 #pragma unroll
               for (int m = 0; m < MAX_M; ++m) {
-                float c;
-                if (DT == DT_INT4) {
-                  c = fmaf(__uint_as_float(sz << 16), a[r][m].x + a[r][m].y,
-                           __uint_as_float(sz & 0xFFFF0000u) * V.xgk[m * KBLK + lane]);
-                } else if (DT == DT_INT8) {
-                  c = (a[r][m].x + a[r][m].y) - V.xgk[m * KBLK + lane];
-                } else {
-                  c = a[r][m].x + a[r][m].y;
+                if (m < M) {
+                  const float4 xa = xk4[m * (SK / 4) + u * 4 + jw];
+                  a[m] = ffma2(c0, lo2(xa), a[m]);
+                  a[m] = ffma2(c1, hi2(xa), a[m]);
                 }
-                v[r * 8 + m] = (lane_ok && m < M) ? c : 0.0f;
+              }
+            } else {
+              const float2 c0 = bits2(wv << 16, wv & 0xFFFF0000u);
+#pragma unroll
+              for (int m = 0; m < MAX_M; ++m) {
+                if (m < M) {
+                  const float4 xa = xk4[m * (SK / 4) + u * 2 + (jw >> 1)];
+                  a[m] = ffma2(c0, (jw & 1) ? hi2(xa) : lo2(xa), a[m]);
+                }
               }
             }
-#pragma unroll
-            for (int sft = 16, n = 32; sft >= 1; sft >>= 1, n >>= 1) {
-              const bool hi = lane & sft;
-#pragma unroll
-              for (int k = 0; k < n / 2; ++k) {
-                const float keep = hi ? v[k + n / 2] : v[k];
-                const float send = hi ? v[k] : v[k + n / 2];
-                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
-              }
-            }
-            const int rr = h * HROWS + rb + (lane >> 3), m = lane & 7;
-            if (m < M) V.acc[((i - i0) * TR + rr) * MAX_M + m] += v[0];
           }
-          slot_release(S, cs, it);
+          if (DT == DT_INT4) {
+            if ((u + 1) % cpg == 0) {  // group end: scale and zero
+              const int gi = u / cpg;
+              const uint32_t sz = slot_sz(base, lane, gi);
+#pragma unroll
+              for (int m = 0; m < MAX_M; ++m) {
+                v[m] = fmaf(__uint_as_float(sz << 16), a[m].x + a[m].y,
+                            fmaf(__uint_as_float(sz & 0xFFFF0000u), V.xgk[m * 32 + gi], v[m]));
+                a[m] = make_float2(0.f, 0.f);
+              }
+            }
+          } else if (DT == DT_INT8) {
+#pragma unroll
+            for (int m = 0; m < MAX_M; ++m) v[m] -= V.xgk[m * 32 + u];
+          }
+        }
+        slot_release(S, cs, it);
+        float* accr = V.acc + ((i - i0) * TR + lane) * MAX_M;
+#pragma unroll
+        for (int m = 0; m < MAX_M; ++m) {
+          if (m < M) accr[m] += DT == DT_INT4 ? v[m] : (a[m].x + a[m].y) + v[m];
         }
       }
       if (!cta_sync(S, cs, P.err)) return false;
@@ -1905,7 +1805,7 @@ __device__ bool verify_finish(const Params& P, const Smem& S, Cons& cs, int cta,
       amax_merge(a, v, i);
     }
     if (cs.lane == 0) {
-      S.red[cs.warp * 8 + m] = a.v;  // red has 64 floats: warps x rows <= 7 x 8
+      S.red[cs.warp * 8 + m] = a.v;  // red has 64 floats: warps x rows <= 8 x 8
       S.bcast[cs.warp * 8 + m] = a.i;
     }
   }
@@ -1947,14 +1847,13 @@ __device__ bool verify_finish(const Params& P, const Smem& S, Cons& cs, int cta,
 // (lower index first on ties), weights = softmax over those two.  Every CTA
 // computes the same logits in the same order, so all agree on the experts.
 __device__ bool route_experts(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int pi) {
-  const int K = ph.K, U = per_chunk(ph.dtype) / 4, K4 = K / 4;
+  const int K = ph.K, K4 = K / 4;
   const float4* xs4 = reinterpret_cast<const float4*>(S.xs);
   for (int e = cs.warp; e < ph.n_experts; e += NCW) {
     const uint2* wr = reinterpret_cast<const uint2*>(ph.router + (size_t)e * K);
     float acc = 0.0f;
     for (int k4 = cs.lane; k4 < K4; k4 += 32) {
-      const int g = k4 / U, u = k4 % U;
-      const float4 xm = xs4[g * U + (u ^ swz(g, U))], iv = dq_inv(ph.dtype, u);
+      const float4 xm = xs4[k4], iv = dq_inv(ph.dtype, k4 & 7);
       const float4 x = make_float4(xm.x * iv.x, xm.y * iv.y, xm.z * iv.z, xm.w * iv.w);
       const float4 wv = bf4(wr[k4]);
       acc = fmaf(x.x, wv.x, fmaf(x.y, wv.y, fmaf(x.z, wv.z, fmaf(x.w, wv.w, acc))));
@@ -2016,6 +1915,10 @@ __device__ bool argmax_finish(const Params& P, const Smem& S, Cons& cs, int cta,
 }
 
 // ============================================================== kernel ====
+// VER: the verification-pass instantiation (multi-row GEMV phases); the
+// decode instantiation carries the single-row GEMV and fused-FFN phases.
+// Splitting them keeps each kernel's register budget to its own code paths.
+template <bool VER>
 __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ Params P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const Smem S = smem_layout(smem_raw);
@@ -2026,7 +1929,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
       mbar_init(&S.empty[i], 1);
     }
     mbar_init(S.cbar, NCW * 32);
-    mbar_init(S.xbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < NTB) {
@@ -2047,7 +1949,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     if (tid == 0) atomicCAS(P.err, 0, ERR_BAD_TOKEN);
     return;
   }
-  if (verifying(P)) {
+  if (VER) {
     bool bad = P.M < 1 || P.M > MAX_M || pos + P.M > P.tmax;
     for (int m = 0; m < P.M; ++m) bad |= P.tokens[m] < 0 || P.tokens[m] >= P.vocab;
     if (bad) {
@@ -2056,8 +1958,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     }
   }
 
-  if (warp == NCW) {
-    if (lane == 0) producer(P, S, cta, pos);
+  if (warp >= NCW) {
+    if (lane == 0) producer(P, S, cta, pos, warp - NCW);
     return;
   }
 
@@ -2070,12 +1972,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   cs.ctid = tid;
   cs.starved = 0;
   cs.rnorm = 1.0f;
-  cs.xphase = 0;
+  cs.lim = wait_limit(P);
   const int G = P.nctas;
   ArgMax am = {-INFINITY, 0x7fffffff};
-  ArgMax amv[MAX_M];
+  ArgMax amv[VER ? MAX_M : 1];
 #pragma unroll
-  for (int m = 0; m < MAX_M; ++m) amv[m] = am;
+  for (int m = 0; m < (VER ? MAX_M : 1); ++m) amv[m] = am;
   bool any_logits = false;
 
   // The consumers read phase descriptors from shared memory: the copy of
@@ -2099,31 +2001,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     if (tr) tr[0] = gtimer();
     if (ph.wait_bar >= 0) {
       int ok = 1;
-      if (tid == 0) ok = grid_wait(P.bars + ph.wait_bar, (unsigned)G, P.err);
+      if (tid == 0) ok = counter_wait(P.bars + ph.wait_bar, (unsigned)G, P.err, ERR_WAIT_GRID, cs.lim);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) return;
       if (!cta_sync(S, cs, P.err)) return;
     }
     if (tr) tr[1] = gtimer();
-    if (ph.kind == PH_GEMV && verifying(P)) {
-      if (tr) tr[2] = gtimer();
+    if (ph.kind == PH_GEMV) {
       bool ok;
-      if (ph.dtype == DT_INT4) ok = gemv_phase_m<DT_INT4>(ph, P, S, cs, cta, pos, pi, amv);
-      else if (ph.dtype == DT_INT8) ok = gemv_phase_m<DT_INT8>(ph, P, S, cs, cta, pos, pi, amv);
-      else ok = gemv_phase_m<DT_BF16>(ph, P, S, cs, cta, pos, pi, amv);
+      if (VER) {
+        if (tr) tr[2] = gtimer();
+        if (ph.dtype == DT_INT4) ok = gemv_phase_m<DT_INT4>(ph, P, S, cs, cta, pos, pi, amv);
+        else if (ph.dtype == DT_INT8) ok = gemv_phase_m<DT_INT8>(ph, P, S, cs, cta, pos, pi, amv);
+        else ok = gemv_phase_m<DT_BF16>(ph, P, S, cs, cta, pos, pi, amv);
+      } else {
+        if (!stage_x(ph, P, S, cs, cta)) return;
+        if (ph.moe == MOE_GU && !route_experts(ph, P, S, cs, pi)) return;
+        if (tr) tr[2] = gtimer();
+        if (ph.dtype == DT_INT4) ok = gemv_phase<DT_INT4>(ph, P, S, cs, cta, pos, am);
+        else if (ph.dtype == DT_INT8) ok = gemv_phase<DT_INT8>(ph, P, S, cs, cta, pos, am);
+        else ok = gemv_phase<DT_BF16>(ph, P, S, cs, cta, pos, am);
+      }
       if (!ok) return;
       if (ph.epi == EPI_LOGITS) any_logits = true;
-    } else if (ph.kind == PH_GEMV) {
-      if (!stage_x(ph, P, S, cs, cta)) return;
-      if (ph.moe == MOE_GU && !route_experts(ph, P, S, cs, pi)) return;
-      if (tr) tr[2] = gtimer();
-      bool ok;
-      if (ph.dtype == DT_INT4) ok = gemv_phase<DT_INT4>(ph, P, S, cs, cta, pos, am);
-      else if (ph.dtype == DT_INT8) ok = gemv_phase<DT_INT8>(ph, P, S, cs, cta, pos, am);
-      else ok = gemv_phase<DT_BF16>(ph, P, S, cs, cta, pos, am);
-      if (!ok) return;
-      if (ph.epi == EPI_LOGITS) any_logits = true;
-    } else if (ph.kind == PH_FFN) {
+    } else if (ph.kind == PH_FFN && !VER) {
       if (!stage_x(ph, P, S, cs, cta)) return;
       if (tr) tr[2] = gtimer();
       bool ok;
@@ -2138,11 +2039,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
       for (int u = first_unit(cta, ph.rot, G); u < nunits; u += G) {
         AttnUnit au;
         attn_units(ph, P, pos, u, &au);
-        const bool ok = ph.hd == 128 ? attn_unit<128>(ph, P, S, cs, au, pos, j)
-                                     : attn_unit<64>(ph, P, S, cs, au, pos, j);
-        if (!ok) return;
+        const AttnRet r = ph.hd == 128 ? attn_call<128, VER>(ph, P, S, cs, au, pos, j)
+                                       : attn_call<64, VER>(ph, P, S, cs, au, pos, j);
+        j = r.j;
+        cs.cphase = r.cphase;
+        cs.starved = r.starved;
+        if (!r.ok) return;
       }
       cs.it += j;
+    } else {
+      if (tid == 0) atomicCAS(P.err, 0, ERR_BAD_PROGRAM);
+      return;
     }
     if (tr) {
       tr[3] = gtimer();
@@ -2156,24 +2063,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     if (tr) tr[4] = gtimer();
   }
   if (any_logits) {
-    if (verifying(P)) verify_finish(P, S, cs, cta, amv);
+    if (VER) verify_finish(P, S, cs, cta, amv);
     else argmax_finish(P, S, cs, cta, am);
   }
 }
 
 int launch_engine(const Params& p, int grid, bool cooperative, cudaStream_t s) {
-  static bool attr_set[64] = {false};
+  static bool attr_set[64][2] = {};
   int dev = 0;
   GF_CUDA(cudaGetDevice(&dev));
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    GF_CUDA(cudaFuncSetAttribute(k_engine, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    attr_set[dev] = true;
+  const bool ver = verifying(p);
+  const void* fn = ver ? (const void*)k_engine<true> : (const void*)k_engine<false>;
+  if (dev >= 0 && dev < 64 && !attr_set[dev][ver]) {
+    GF_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+    attr_set[dev][ver] = true;
   }
   if (cooperative) {
     void* args[] = {const_cast<Params*>(&p)};
-    GF_CUDA(cudaLaunchCooperativeKernel((const void*)k_engine, dim3(grid), dim3(NTHREADS), args, SMEM_BYTES, s));
+    GF_CUDA(cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NTHREADS), args, SMEM_BYTES, s));
   } else {
-    k_engine<<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
+    if (ver) k_engine<true><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
+    else k_engine<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
     GF_CUDA(cudaGetLastError());
   }
   return GF_OK;
@@ -2201,8 +2111,8 @@ static Params base_params() {
   return p;
 }
 
-static int gemv_common(const char* fn, int dt, const void* x, const void* Wp, const void* s8, int N, int K, void* y,
-                       int ydt, cudaStream_t stream) {
+static int gemv_common(const char* fn, int dt, const void* x, const void* Wp, const void* s8, int N, int K, int G,
+                       void* y, int ydt, cudaStream_t stream) {
   if (!x || !Wp || !y || N <= 0 || K <= 0 || K % per_chunk(dt) || (dt == DT_INT8 && !s8) ||
       (ydt != GF_Y_BF16 && ydt != GF_Y_F32)) {
     set_error("%s: bad arguments (N=%d, K=%d, ydtype=%d)", fn, N, K, ydt);
@@ -2222,6 +2132,7 @@ static int gemv_common(const char* fn, int dt, const void* x, const void* Wp, co
   ph.dtype = dt;
   ph.N = N;
   ph.K = K;
+  ph.G = G;
   ph.W = (const uint8_t*)Wp;
   ph.s8 = (const uint16_t*)s8;
   ph.xsrc = X_BF16;
@@ -2247,17 +2158,17 @@ using namespace gf;
 extern "C" {
 
 int gf_gemv_bf16(const void* x, const void* Wpacked, int N, int K, void* y, int ydtype, gf_stream stream) {
-  return gemv_common("gf_gemv_bf16", DT_BF16, x, Wpacked, nullptr, N, K, y, ydtype, (cudaStream_t)stream);
+  return gemv_common("gf_gemv_bf16", DT_BF16, x, Wpacked, nullptr, N, K, 32, y, ydtype, (cudaStream_t)stream);
 }
 int gf_gemv_w8(const void* x, const void* qpacked, const void* s, int N, int K, void* y, int ydtype, gf_stream stream) {
-  return gemv_common("gf_gemv_w8", DT_INT8, x, qpacked, s, N, K, y, ydtype, (cudaStream_t)stream);
+  return gemv_common("gf_gemv_w8", DT_INT8, x, qpacked, s, N, K, 32, y, ydtype, (cudaStream_t)stream);
 }
 int gf_gemv_w4g(const void* x, const void* qpacked, int N, int K, int G, void* y, int ydtype, gf_stream stream) {
-  if (G != 32) {
-    set_error("gf_gemv_w4g: only group size 32 is supported (got %d)", G);
+  if ((G != 32 && G != 64 && G != 128) || K % G) {
+    set_error("gf_gemv_w4g: group size must be 32, 64 or 128 and divide K (G=%d, K=%d)", G, K);
     return GF_EUNSUPPORTED;
   }
-  return gemv_common("gf_gemv_w4g", DT_INT4, x, qpacked, nullptr, N, K, y, ydtype, (cudaStream_t)stream);
+  return gemv_common("gf_gemv_w4g", DT_INT4, x, qpacked, nullptr, N, K, G, y, ydtype, (cudaStream_t)stream);
 }
 
 size_t gf_attn_workspace_bytes(int Hq, int Hkv, int hd) {

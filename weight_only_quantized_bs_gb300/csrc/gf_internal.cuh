@@ -1,7 +1,6 @@
-// gf_internal.cuh — shared definitions of the sm_103a engine: tile layout
-// arithmetic, PTX wrappers (mbarrier, bulk asynchronous copy, acquire/release
-// loads), the phase program executed by the persistent kernel, and host-side
-// error helpers.
+// gf_internal.cuh — shared definitions of the sm_103a engine: the weight
+// layout and slot geometry of the bulk copies, the phase program executed by
+// the persistent kernel, the shared-memory map, and host-side helpers.
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -11,83 +10,106 @@
 namespace gf {
 
 // ------------------------------------------------------------- layout ----
+// Device layout of a weight matrix: slots of 32 rows (one per lane of a
+// consumer warp) by 256 bytes of each row, stored one after another (tile t,
+// K-slot b at slot t * nb + b), each contiguous so that one bulk copy moves
+// it into a shared-memory ring entry.  A slot is 128-byte lines: line
+// h * 32 + r (h = 0, 1) holds bytes [256 b + 128 h, 256 b + 128 h + 128) of
+// row 32 t + r (zero past the row or the matrix), then for int4 lines 64 + g
+// hold the scale/zero words s | z << 16 of the 32 rows for group
+// 512 b / G + g.  Inside every line the 16-byte units are stored swizzled:
+// unit u of line L at unit u ^ (L & 7), so that the 32 lanes' 16-byte reads of
+// one unit of their rows (and their 4-byte reads of one scale line) hit all
+// 32 banks.
 constexpr int TR = GF_TILE_ROWS;  // rows per tile
-constexpr int KBLK = 32;          // chunks per K-block (one per lane)
 constexpr int KMAX = GF_KMAX;
 enum { DT_BF16 = 0, DT_INT8 = 1, DT_INT4 = 2 };
 
-__host__ __device__ inline int per_chunk(int dt) { return dt == DT_BF16 ? 8 : dt == DT_INT8 ? 16 : 32; }
-
-__host__ __device__ inline long long block_bytes(int dt, int Rt, int Lb) {
-  long long b = (long long)Rt * Lb * 16;
-  if (dt == DT_INT4) b += ((long long)Rt * Lb * 4 + 15) / 16 * 16;
-  return b;
+__host__ __device__ constexpr int per_chunk(int dt) { return dt == DT_BF16 ? 8 : dt == DT_INT8 ? 16 : 32; }
+// K values per slot (256 bytes of each row)
+__host__ __device__ constexpr int slot_k(int dt) { return dt == DT_BF16 ? 128 : dt == DT_INT8 ? 256 : 512; }
+constexpr int LINE = 128;                    // bytes of a line (the swizzle span)
+constexpr int CODE_BYTES = 2 * TR * LINE;    // code lines of a slot
+constexpr int SLOT_CHUNKS = 16;              // 16-byte chunks of each row in a slot
+__host__ __device__ inline long long round_up(long long a, long long m) { return (a + m - 1) / m * m; }
+__host__ __device__ inline int slot_bytes(int dt, int G) { return CODE_BYTES + (dt == DT_INT4 ? (512 / G) * LINE : 0); }
+__host__ __device__ inline int k_slots(int dt, int K) { return (K + slot_k(dt) - 1) / slot_k(dt); }
+__host__ __device__ inline long long packed_bytes(int dt, int N, int K, int G) {
+  return (long long)((N + TR - 1) / TR) * k_slots(dt, K) * slot_bytes(dt, G);
 }
-// Bytes of a full tile (TR rows, all K-blocks).  With TR a multiple of 4 the
-// int4 scale words need no padding, so this is TR times the row bytes.
-__host__ __device__ inline long long full_tile_bytes(int dt, int C) {
-  return (long long)TR * C * (dt == DT_INT4 ? 20 : 16);
+// byte of the packed buffer holding byte `kb` of row n's codes
+__host__ __device__ inline long long code_addr(int dt, int K, int G, int n, long long kb) {
+  const int nb = k_slots(dt, K), b = (int)(kb >> 8), r = n % TR, line = (int)((kb >> 7) & 1) * TR + r;
+  const int unit = (int)((kb >> 4) & 7) ^ (line & 7);
+  return ((long long)(n / TR) * nb + b) * slot_bytes(dt, G) + (long long)line * LINE + unit * 16 + (kb & 15);
 }
-__host__ __device__ inline long long packed_bytes(int dt, int N, int K) {
-  int C = K / per_chunk(dt);
-  long long total = (long long)(N / TR) * full_tile_bytes(dt, C);
-  if (N % TR) {
-    int Rt = N % TR;
-    for (int c0 = 0; c0 < C; c0 += KBLK) total += block_bytes(dt, Rt, C - c0 < KBLK ? C - c0 : KBLK);
-  }
-  return total;
-}
-// Byte offset of K-block b of the tile holding row-tile t (rows Rt), and of
-// chunk (r, l) inside it.
-__host__ __device__ inline long long block_offset(int dt, int C, int t, int Rt, int b) {
-  return (long long)t * full_tile_bytes(dt, C) + (long long)b * block_bytes(dt, Rt, KBLK);
+// byte of the packed buffer holding the int4 scale/zero word of (row n, group g)
+__host__ __device__ inline long long sz_addr(int K, int G, int n, int g) {
+  const int nb = k_slots(DT_INT4, K), gps = 512 / G, b = g / gps, gl = g % gps, r = n % TR;
+  const int unit = (r >> 2) ^ (gl & 7);  // line 64 + gl: (64 + gl) & 7 == gl & 7
+  return ((long long)(n / TR) * nb + b) * slot_bytes(DT_INT4, G) + CODE_BYTES + (long long)gl * LINE + unit * 16 +
+         (r & 3) * 4;
 }
 
 // ------------------------------------------------------- engine sizes ----
-constexpr int NCW = 7;                       // consumer warps per CTA
-constexpr int NTHREADS = (NCW + 1) * 32;     // + one producer warp
-constexpr int HROWS = 16;                    // rows of a slot: half a tile
-constexpr int SLOT_BYTES = 10240;            // codes of 16 rows x 32 chunks + int4 scale words
-constexpr int SLOT_SZ_OFF = 8192;            // int4 scale words inside a slot
+constexpr int NCW = 8;                       // consumer warps per CTA
+constexpr int NPROD = 2;                     // producer warps (lane 0 of each issues copies)
+constexpr int NTHREADS = (NCW + NPROD) * 32;
+constexpr int SLOT_BYTES = 10240;            // ring entry: a slot of any type
 // Slot X of the CTA's stream (counted over the whole program) belongs to
 // consumer warp X % NCW and uses ring entry X % NSLOT.  NSLOT is a multiple
-// of NCW, so every ring entry always belongs to the same warp: the previous
-// use of the entry a warp waits on is that warp's own, already consumed slot,
-// and the mbarrier phase parity it waits for is never ambiguous.
-constexpr int NSLOT = 14;
-// Half-tile combine buffers, used round-robin by half-tile number; a guard
-// word per buffer holds the number of the half-tile allowed to use it next.
-constexpr int NTB = 16;
-constexpr int OFF_RING = 0;
-constexpr int OFF_X = OFF_RING + NSLOT * SLOT_BYTES;     // fp32 x, swizzled
+// of NCW, so every ring entry always belongs to the same warp (two entries
+// per warp): the previous use of the entry a warp waits on is that warp's
+// own, already consumed slot, and the mbarrier parity it waits for is never
+// ambiguous.
+constexpr int NSLOT = 2 * NCW;
+constexpr int NTB = 4;                       // tile combine buffers (round-robin, guarded)
+constexpr int OFF_RING = 0;                  // 128-aligned: a slot's lines map to whole bank rows
+constexpr int OFF_X = OFF_RING + NSLOT * SLOT_BYTES;     // fp32 x (staged with the dequantisation powers)
 constexpr int OFF_XSUM = OFF_X + KMAX * 4;               // fp32 sums of x per chunk (int8) / group (int4)
-constexpr int OFF_TB = OFF_XSUM + (KMAX / 16) * 4 + 256;  // [NTB][NCW][HROWS] partial row sums
-constexpr int OFF_TBC = OFF_TB + NTB * NCW * HROWS * 4;  // [NTB] arrival counters, then [NTB] guards
+constexpr int OFF_TB = OFF_XSUM + (KMAX / 16) * 4;       // [NTB][NCW][TR] partial row sums
+constexpr int OFF_TBC = OFF_TB + NTB * NCW * TR * 4;     // [NTB] arrival counters, then [NTB] guards
 constexpr int OFF_BAR = OFF_TBC + 2 * NTB * 4;           // mbarriers
-constexpr int OFF_MISC = OFF_BAR + 320;
+constexpr int OFF_MISC = OFF_BAR + (2 * NSLOT + 2) * 8;
 constexpr int OFF_PHB = OFF_MISC + 1024;  // red[64] f32, bcast[64] i32, moew[64] f32, spare
 constexpr int PHB_BYTES = 256;            // one phase descriptor (two buffers)
-constexpr int SMEM_BYTES = OFF_PHB + 2 * PHB_BYTES;
-static_assert(OFF_PHB % 16 == 0, "phase descriptor buffers take 16-byte copies");
-static_assert(NSLOT % NCW == 0, "ring entries must map to a fixed warp");
-static_assert((2 * NSLOT + 1) * 8 <= 320, "mbarrier area");
+constexpr int SMEM_USED = OFF_PHB + 2 * PHB_BYTES;
+constexpr int SMEM_BYTES = SMEM_USED + 128;  // + slack to align the base to 128
+static_assert(SLOT_BYTES % 16 == 0 && SLOT_BYTES >= CODE_BYTES + 16 * LINE, "slot geometry");
+static_assert(OFF_BAR % 8 == 0 && OFF_PHB % 16 == 0, "shared-memory alignment");
+static_assert(NSLOT % NCW == 0 && NSLOT % NPROD == 0, "ring entries must map to a fixed warp and producer");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
-constexpr int ATT_POS_PER_SLOT = 16;
+constexpr int ATT_POS_PER_SLOT = 16;         // positions a warp scores at once (and a slot's most)
+// positions of K and V in one ring entry: 8 for head dim 128, 16 for 64
+__host__ __device__ constexpr int att_slot_pos(int hd) { return SLOT_BYTES / (4 * hd) >= 16 ? 16 : 8; }
 constexpr int FFN_HN = 8;                    // SwiGLU output buffers of a PH_FFN phase (tiles in flight)
-// Slots of a down slice in a PH_FFN phase: nsl slots of DR rows, as full as
-// the slot size allows (DR a multiple of 8, so every bulk copy is 16-byte
-// sized and aligned; the last slot may hold fewer rows), int4 scale words
-// right after a slot's DR rows of codes.
-constexpr int FFN_MAXSL = 32;                // most down slots per tile
-__host__ __device__ inline void ffn_split(int dt, int d, int& nsl, int& DR) {
-  const int rowb = dt == DT_INT4 ? 12 : dt == DT_INT8 ? 16 : 32;  // slot bytes per row
-  const int maxr = (SLOT_BYTES / rowb) / 8 * 8;
-  nsl = (d + maxr - 1) / maxr;
-  DR = ((d + nsl - 1) / nsl + 7) / 8 * 8;
+constexpr int FFN_MAX_D = 4096;              // widest model the fused FFN handles
+// Down projection of a PH_FFN phase: per gate/up tile, the 16 matching
+// columns of every output row (a column-sliced copy), split into NCW row
+// ranges of RW rows (warp w always owns rows w RW .. w RW + RW - 1, so its
+// partial outputs need no synchronisation), each streamed as P pieces of at
+// most PR rows (one slot each, as even as the slot size allows).  Row bytes
+// per slot: int4 8 code + 4 scale, int8 16, bf16 32.
+struct FfnSplit {
+  int RW, PR, P;
+};
+__host__ __device__ inline int ffn_row_bytes(int dt) { return dt == DT_INT4 ? 12 : dt == DT_INT8 ? 16 : 32; }
+__host__ __device__ inline FfnSplit ffn_split(int dt, int d) {
+  FfnSplit s;
+  s.RW = (int)round_up((d + NCW - 1) / NCW, 32);
+  const int maxr = SLOT_BYTES / ffn_row_bytes(dt) / 32 * 32;
+  s.P = (s.RW + maxr - 1) / maxr;
+  s.PR = (int)round_up((s.RW + s.P - 1) / s.P, 32);
+  return s;
 }
-// shared floats a PH_FFN phase needs above its input: partial outputs, SwiGLU
-// buffers and their counters, the down slots' turn counters
-__host__ __device__ constexpr int ffn_smem_floats(int d) { return d + FFN_HN * 16 + FFN_HN + 2 * FFN_MAXSL; }
+// rows [r0, r1) of piece k of warp w (empty when r0 >= r1)
+__host__ __device__ inline void ffn_piece(const FfnSplit& s, int d, int w, int k, int& r0, int& r1) {
+  r0 = w * s.RW + k * s.PR;
+  r1 = r0 + s.PR;
+  const int wend = (w + 1) * s.RW;
+  if (r1 > wend) r1 = wend;
+  if (r1 > d) r1 = d;
+}
 constexpr int MAX_GQ = 4;                    // q heads per kv head (GQA group)
 constexpr int MAX_M = 8;                     // rows of a verify pass
 constexpr int VTG = 4;                       // tiles per group of a multi-row GEMV phase
@@ -126,7 +148,8 @@ enum ErrCode {
   ERR_BAD_POS = 7,    // *d_pos outside [0, Tmax)
   ERR_BAD_TOKEN = 8,  // token id outside [0, vocab)
   ERR_WAIT_ROUTER = 9, // the producer gave up waiting for the expert choice
-  ERR_WAIT_COMBINE = 10 // a half-tile combine buffer was not handed on in time
+  ERR_WAIT_COMBINE = 10, // a tile combine buffer was not handed on in time
+  ERR_WAIT_HEAD = 11   // an attention unit gave up waiting for its head's q/k/v rows
 };
 
 struct alignas(16) Phase {
@@ -135,11 +158,13 @@ struct alignas(16) Phase {
   int signal_bar;  // grid barrier to arrive on after the phase (-1: none)
   int rot;         // unit rotation across CTAs
   // GEMV
-  int dtype, N, K;
+  int dtype, N, K, G;      // G: int4 group size
   int epi;
-  const uint8_t* W;        // packed weights
+  int pad0;
+  const uint8_t* W;        // packed matrix (experts back to back)
+  const void* pad1;
   const uint16_t* s8;      // int8 row scales
-  const uint8_t* W2;       // PH_FFN: column-sliced down projection [N2][N/2]
+  const uint8_t* W2;       // PH_FFN: column-sliced down projection
   const uint16_t* s8b;     // PH_FFN: its int8 row scales
   int N2;                  // PH_FFN: rows of the down projection (the model width)
   int xsrc;
@@ -157,11 +182,11 @@ struct alignas(16) Phase {
   int Hq, Hkv, hd, Tmax;
   float* part;             // [Hq][nch_max][hd + 2] partials
   unsigned* tick;          // [Hkv] combine tickets
+  unsigned* headc;         // [Hkv] q/k/v tiles of each kv group finished (nullptr: no wait)
   int stream_cur;          // 1: the row at pos is in memory before launch (standalone)
   // mixture of experts
   int moe;                 // MoeMode
   int n_experts;
-  long long expert_stride; // bytes between consecutive experts' packed matrices
   const uint16_t* router;  // [n_experts][K] bf16 (MOE_GU)
   // multi-row (verify) input addressing: row m, expert segment e of X_F32
   int x_mstride;           // floats between rows
@@ -208,6 +233,7 @@ struct Params {
   int vocab;
   int tmax;            // positions must lie in [0, tmax) (0: not checked)
   unsigned long long* trace;  // [nphases][nctas][TRACE_W] timestamps and counters (nullptr: off)
+  unsigned long long wait_ns;  // limit of every bounded wait (0: the default, 2 s)
   // speculative verification (tokens != nullptr): rows m = 0..M-1 are
   // tokens[m] at pos + m, 1 <= M <= MAX_M
   int M;               // rows of the pass (1 for a decode step)
@@ -228,7 +254,8 @@ __host__ __device__ __forceinline__ bool verifying(const Params& P) { return P.t
 // ------------------------------------------------------------ host side --
 void set_error(const char* fmt, ...);
 long long cols_bytes(int dt, int N, int K);
-int pack_cols(int dt, const void* packed, int N, int K, void* out, cudaStream_t s);
+int pack_cols(int dt, const void* packed, int N, int K, int G, void* out, cudaStream_t s);
+int quantize_rows(int dt, const void* W, int N, int K, int G, void* packed, void* s8, cudaStream_t s);
 int cuda_fail(cudaError_t e, const char* what);
 #define GF_CUDA(call)                                        \
   do {                                                       \

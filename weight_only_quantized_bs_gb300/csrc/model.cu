@@ -1,6 +1,7 @@
 // model.cu — host side of the decode step: library-owned quantised weights
-// (gf_model), the KV cache with its RoPE table and scratch (gf_kv), and the
-// phase program that the persistent engine runs once per token.
+// (gf_model), the KV cache with its RoPE table and
+// scratch (gf_kv), and the phase program that the persistent engine runs once
+// per token.
 #include <math.h>
 #include <string.h>
 
@@ -11,16 +12,18 @@
 struct gf_model {
   gf_model_config cfg;
   int wdtype;
+  int G;  // int4 group size
+  // One matrix in the device layout; the experts of a layer are packed one
+  // after another in one buffer (expert e at e * packed_bytes(N, K)).
   struct Mat {
-    uint8_t* W = nullptr;
+    uint8_t* packed = nullptr;
     uint16_t* s8 = nullptr;
-    int N = 0, K = 0;
+    int N = 0, K = 0, E = 1;
   };
-  std::vector<Mat> qkv, o, gu, dn;  // per layer (MoE: gu / dn hold all experts back to back)
+  std::vector<Mat> qkv, o, gu, dn;  // per layer
   std::vector<uint8_t*> dn_cols;    // dense: column-sliced copy of dn for the fused FFN phase
   bool ffn_fused = false;
   std::vector<uint16_t*> g_attn, g_ffn, router;
-  long long gu_stride = 0, dn_stride = 0;  // MoE: bytes between experts
   Mat lm;
   uint16_t* embed = nullptr;
   uint16_t* g_final = nullptr;
@@ -42,12 +45,13 @@ struct gf_kv {
   int nvphases = 0;
   float* amax_val = nullptr;
   int* amax_idx = nullptr;
-  unsigned* counters = nullptr;  // bars, then attention tickets, then the argmax ticket
+  unsigned* counters = nullptr;  // bars, attention tickets, q/k/v head counters, the argmax ticket
   size_t counter_bytes = 0;
-  unsigned *bars = nullptr, *ticks = nullptr, *amax_tick = nullptr;
+  unsigned *bars = nullptr, *ticks = nullptr, *headc = nullptr, *amax_tick = nullptr;
   gf::Phase* prog = nullptr;
   int nphases = 0;
   int sms = 0;
+  size_t cache_elems = 0;
   std::vector<void*> allocs;
 };
 
@@ -70,45 +74,37 @@ static void free_all(std::vector<void*>& list) {
   list.clear();
 }
 
-static int make_mat(gf_model* m, const void* src, int N, int K, gf_model::Mat& out) {
+// E matrices of N x K (E = 1: a single matrix) quantised into one buffer,
+// expert e from srcs[e].
+static int make_mat(gf_model* m, const void* const* srcs, int E, int N, int K, gf_model::Mat& out) {
   out.N = N;
   out.K = K;
-  const int dt = m->wdtype;
-  const long long bytes = packed_bytes(dt, N, K);
-  int rc = dev_alloc(m->allocs, (void**)&out.W, (size_t)bytes);
+  out.E = E;
+  const int dt = m->wdtype, G = m->G;
+  const long long pb = packed_bytes(dt, N, K, G);
+  int rc = dev_alloc(m->allocs, (void**)&out.packed, (size_t)(pb * E));
   if (rc) return rc;
-  m->weight_bytes += bytes;
-  if (dt == DT_INT8) {
-    if ((rc = dev_alloc(m->allocs, (void**)&out.s8, (size_t)N * 2))) return rc;
-    m->weight_bytes += (long long)N * 2;
-    return gf_quantize_w8(src, N, K, out.W, out.s8, nullptr);
-  }
-  if (dt == DT_INT4) return gf_quantize_w4g(src, N, K, 32, out.W, nullptr);
-  return gf_repack_bf16(src, N, K, out.W, nullptr);
-}
-
-// E experts of one layer quantised into one buffer, expert e at e * stride
-// (and int8 scales at e * N).
-static int make_experts(gf_model* m, const void* const* srcs, int E, int N, int K, gf_model::Mat& out,
-                        long long& stride) {
-  out.N = N;
-  out.K = K;
-  const int dt = m->wdtype;
-  stride = packed_bytes(dt, N, K);
-  int rc = dev_alloc(m->allocs, (void**)&out.W, (size_t)(stride * E));
-  if (rc) return rc;
-  if (dt == DT_INT8 && (rc = dev_alloc(m->allocs, (void**)&out.s8, (size_t)N * E * 2))) return rc;
+  if (dt == DT_INT8 && (rc = dev_alloc(m->allocs, (void**)&out.s8, (size_t)E * N * 2))) return rc;
+  GF_CUDA(cudaMemset(out.packed, 0, (size_t)(pb * E)));  // padding rows and K-slots read as zero
   for (int e = 0; e < E && !rc; ++e) {
     if (!srcs[e]) {
-      set_error("gf_model_create: null expert weight");
+      set_error("gf_model_create: null weight pointer");
       return GF_EINVAL;
     }
-    uint8_t* dst = out.W + (size_t)e * stride;
-    if (dt == DT_INT8) rc = gf_quantize_w8(srcs[e], N, K, dst, out.s8 + (size_t)e * N, nullptr);
-    else if (dt == DT_INT4) rc = gf_quantize_w4g(srcs[e], N, K, 32, dst, nullptr);
-    else rc = gf_repack_bf16(srcs[e], N, K, dst, nullptr);
+    rc = quantize_rows(dt, srcs[e], N, K, G, out.packed + (size_t)(pb * e), out.s8 ? out.s8 + (size_t)e * N : nullptr,
+                       nullptr);
   }
   return rc;
+}
+
+// bytes one token streams from a matrix (one expert of a tall one): the
+// method's codes and scales, not the layout's padding
+static long long mat_stream_bytes(const gf_model* m, const gf_model::Mat& a) {
+  const int dt = m->wdtype;
+  long long b = dt == DT_BF16 ? 2LL * a.N * a.K : dt == DT_INT8 ? (long long)a.N * a.K : (long long)a.N * a.K / 2;
+  if (dt == DT_INT8) b += 2LL * a.N;
+  if (dt == DT_INT4) b += 4LL * a.N * (a.K / m->G);
+  return b;
 }
 
 static int copy_vec(gf_model* m, const void* src, size_t elems, uint16_t** out) {
@@ -118,7 +114,7 @@ static int copy_vec(gf_model* m, const void* src, size_t elems, uint16_t** out) 
   return GF_OK;
 }
 
-static int check_cfg(const gf_model_config* c) {
+static int check_cfg(const gf_model_config* c, int wdtype) {
   if (!c || c->d <= 0 || c->n_layers <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->ffn <= 0 || c->vocab <= 0 ||
       c->n_heads % c->n_kv_heads || c->n_heads / c->n_kv_heads > MAX_GQ || (c->head_dim != 64 && c->head_dim != 128) ||
       c->d % 32 || c->ffn % 32 || c->d > KMAX || c->ffn > KMAX || c->n_heads * c->head_dim > KMAX ||
@@ -128,6 +124,12 @@ static int check_cfg(const gf_model_config* c) {
   }
   if (c->n_experts == 1 || c->n_experts < 0 || c->n_experts > 8) {
     set_error("gf_model_create: n_experts must be 0 (dense) or 2..8");
+    return GF_EUNSUPPORTED;
+  }
+  const int G = c->group_size ? c->group_size : 32;
+  if (wdtype == DT_INT4 && ((G != 32 && G != 64 && G != 128) || c->d % G || c->ffn % G ||
+                            (c->n_heads * c->head_dim) % G)) {
+    set_error("gf_model_create: int4 group size %d must be 32, 64 or 128 and divide d, ffn and the head width", G);
     return GF_EUNSUPPORTED;
   }
   return GF_OK;
@@ -140,7 +142,7 @@ using namespace gf;
 extern "C" {
 
 int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w, gf_model** out) {
-  int rc = check_cfg(cfg);
+  int rc = check_cfg(cfg, wdtype);
   if (rc) return rc;
   if (!w || !out || wdtype < 0 || wdtype > 2 || !w->embed || !w->g_final || !w->lm_head || !w->wqkv || !w->wo ||
       !w->wgu || !w->wd || !w->g_attn || !w->g_ffn || (cfg->n_experts && !w->router)) {
@@ -150,6 +152,7 @@ int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w,
   gf_model* m = new gf_model();
   m->cfg = *cfg;
   m->wdtype = wdtype;
+  m->G = cfg->group_size ? cfg->group_size : 32;
   const gf_model_config& c = *cfg;
   const int hd = c.head_dim, qkvN = (c.n_heads + 2 * c.n_kv_heads) * hd;
   m->qkv.resize(c.n_layers);
@@ -162,46 +165,45 @@ int gf_model_create(const gf_model_config* cfg, int wdtype, const gf_weights* w,
   m->dn_cols.resize(c.n_layers, nullptr);
   const int E = c.n_experts;
   // dense FFNs run as one phase when the partial down outputs fit in shared
-  // memory beside the staged input and a down slice takes few enough slots
-  int nsl = 0, DR = 0;
-  ffn_split(wdtype, c.d, nsl, DR);
-  m->ffn_fused = !E && c.d + ffn_smem_floats(c.d) <= KMAX && c.d % 16 == 0 && nsl <= FFN_MAXSL;
+  // memory beside the staged input
+  m->ffn_fused = !E && round_up(c.d, slot_k(wdtype)) + c.d + FFN_HN * 16 + 2 * FFN_HN <= KMAX && c.d % 16 == 0;
   for (int l = 0; l < c.n_layers && !rc; ++l) {
     if (!w->wqkv[l] || !w->wo[l] || !w->g_attn[l] || !w->g_ffn[l] || (E && !w->router[l])) {
       set_error("gf_model_create: null weight pointer in layer %d", l);
       rc = GF_EINVAL;
       break;
     }
-    if ((rc = make_mat(m, w->wqkv[l], qkvN, c.d, m->qkv[l]))) break;
-    if ((rc = make_mat(m, w->wo[l], c.d, c.n_heads * hd, m->o[l]))) break;
+    if ((rc = make_mat(m, &w->wqkv[l], 1, qkvN, c.d, m->qkv[l]))) break;
+    if ((rc = make_mat(m, &w->wo[l], 1, c.d, c.n_heads * hd, m->o[l]))) break;
+    m->weight_bytes += mat_stream_bytes(m, m->qkv[l]) + mat_stream_bytes(m, m->o[l]);
     if (E) {
-      const long long before = m->weight_bytes;
-      if ((rc = make_experts(m, w->wgu + (size_t)l * E, E, 2 * c.ffn, c.d, m->gu[l], m->gu_stride))) break;
-      if ((rc = make_experts(m, w->wd + (size_t)l * E, E, c.d, c.ffn, m->dn[l], m->dn_stride))) break;
+      if ((rc = make_mat(m, w->wgu + (size_t)l * E, E, 2 * c.ffn, c.d, m->gu[l]))) break;
+      if ((rc = make_mat(m, w->wd + (size_t)l * E, E, c.d, c.ffn, m->dn[l]))) break;
       if ((rc = copy_vec(m, w->router[l], (size_t)E * c.d, &m->router[l]))) break;
       // a token streams two experts and the router
-      m->weight_bytes = before + 2 * (m->gu_stride + m->dn_stride) + (long long)E * c.d * 2;
-      if (wdtype == DT_INT8) m->weight_bytes += 2LL * (2 * c.ffn + c.d) * 2;
+      m->weight_bytes += 2 * (mat_stream_bytes(m, m->gu[l]) + mat_stream_bytes(m, m->dn[l])) + (long long)E * c.d * 2;
     } else {
       if (!w->wgu[l] || !w->wd[l]) {
         set_error("gf_model_create: null weight pointer in layer %d", l);
         rc = GF_EINVAL;
         break;
       }
-      if ((rc = make_mat(m, w->wgu[l], 2 * c.ffn, c.d, m->gu[l]))) break;
-      if ((rc = make_mat(m, w->wd[l], c.d, c.ffn, m->dn[l]))) break;
+      if ((rc = make_mat(m, &w->wgu[l], 1, 2 * c.ffn, c.d, m->gu[l]))) break;
+      if ((rc = make_mat(m, &w->wd[l], 1, c.d, c.ffn, m->dn[l]))) break;
+      m->weight_bytes += mat_stream_bytes(m, m->gu[l]) + mat_stream_bytes(m, m->dn[l]);
       if (m->ffn_fused) {
         // the decode step streams this copy instead of dn (same bytes); the
         // verify pass keeps using dn
         if ((rc = dev_alloc(m->allocs, (void**)&m->dn_cols[l], (size_t)cols_bytes(wdtype, c.d, c.ffn)))) break;
-        if ((rc = pack_cols(wdtype, m->dn[l].W, c.d, c.ffn, m->dn_cols[l], nullptr))) break;
+        if ((rc = pack_cols(wdtype, m->dn[l].packed, c.d, c.ffn, m->G, m->dn_cols[l], nullptr))) break;
       }
     }
     if ((rc = copy_vec(m, w->g_attn[l], c.d, &m->g_attn[l]))) break;
     if ((rc = copy_vec(m, w->g_ffn[l], c.d, &m->g_ffn[l]))) break;
     m->weight_bytes += 2LL * c.d * 2;
   }
-  if (!rc) rc = make_mat(m, w->lm_head, c.vocab, c.d, m->lm);
+  if (!rc) rc = make_mat(m, &w->lm_head, 1, c.vocab, c.d, m->lm);
+  if (!rc) m->weight_bytes += mat_stream_bytes(m, m->lm);
   if (!rc) rc = copy_vec(m, w->embed, (size_t)c.vocab * c.d, &m->embed);
   if (!rc) rc = copy_vec(m, w->g_final, c.d, &m->g_final);
   if (!rc) {
@@ -241,13 +243,15 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
   const int G = kv->sms;
   int rc = GF_OK;
   const size_t cache_elems = (size_t)L * Hkv * Tmax * hd;
+  kv->cache_elems = cache_elems;
   const int nch_max = (G + Hkv - 1) / Hkv;
   const int E = c.n_experts;
   const int ppl = E ? 6 : m->ffn_fused ? 4 : 5;  // phases per layer
   const int nph = ppl * L + 1;
   const int nbars = nph;
   const size_t nticks = (size_t)L * MAX_M * Hkv;
-  kv->counter_bytes = (nbars + nticks + 1) * sizeof(unsigned);
+  const size_t nheadc = (size_t)L * Hkv;
+  kv->counter_bytes = (nbars + nticks + nheadc + 1) * sizeof(unsigned);
   do {
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->kc, cache_elems * 2))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->vc, cache_elems * 2))) break;
@@ -272,7 +276,8 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
   }
   kv->bars = kv->counters;
   kv->ticks = kv->counters + nbars;
-  kv->amax_tick = kv->ticks + nticks;
+  kv->headc = kv->ticks + nticks;
+  kv->amax_tick = kv->headc + nheadc;
   cudaError_t e = cudaMemset(kv->kc, 0, cache_elems * 2);
   if (e == cudaSuccess) e = cudaMemset(kv->vc, 0, cache_elems * 2);
   if (e == cudaSuccess) e = cudaMemset(kv->counters, 0, kv->counter_bytes);
@@ -286,16 +291,21 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     }
   if (e == cudaSuccess) e = cudaMemcpy(kv->rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice);
 
-  // the program: 5 phases per layer + lm_head, each waiting on its predecessor
+  // The program, per dense layer: q/k/v (with RoPE and the KV append) and
+  // attention in one stretch without a grid barrier (each attention unit waits
+  // for its kv group's q/k/v tiles), o, and the FFN; lm_head at the end.
   std::vector<Phase> ph(nph);
+  std::vector<char> chained(nph, 0);  // 1: follows its predecessor without a grid barrier
   memset(ph.data(), 0, ph.size() * sizeof(Phase));
   long long cum_units = 0;
+  const int Gq = m->G;
   auto gemv = [&](Phase& p, const gf_model::Mat& mat) {
     p.kind = PH_GEMV;
     p.dtype = m->wdtype;
     p.N = mat.N;
     p.K = mat.K;
-    p.W = mat.W;
+    p.G = Gq;
+    p.W = mat.packed;
     p.s8 = mat.s8;
     p.rot = (int)(cum_units % G);
     cum_units += (mat.N + TR - 1) / TR;
@@ -317,8 +327,12 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[0].kc = kcl;
     P[0].vc = vcl;
     P[0].hd = hd;
+    P[0].Hq = Hq;
+    P[0].Hkv = Hkv;
     P[0].Tmax = Tmax;
-    // attention over positions 0..pos
+    P[0].headc = kv->headc + (size_t)l * Hkv;
+    // attention over positions 0..pos (the units start on CTAs that hold
+    // fewer q/k/v tiles: the rotation continues after the q/k/v tiles)
     P[1].kind = PH_ATTN;
     P[1].qbuf = kv->qbuf;
     P[1].kc = kcl;
@@ -332,8 +346,10 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[1].Tmax = Tmax;
     P[1].part = kv->part;
     P[1].tick = kv->ticks + (size_t)l * MAX_M * Hkv;
+    P[1].headc = kv->headc + (size_t)l * Hkv;
     P[1].stream_cur = 0;
     P[1].rot = (int)(cum_units % G);
+    chained[ppl * l + 1] = 1;
     // o projection + residual
     gemv(P[2], m->o[l]);
     P[2].xsrc = X_F32;
@@ -375,7 +391,6 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
       gemv(P[3], two);
       P[3].moe = MOE_GU;
       P[3].n_experts = E;
-      P[3].expert_stride = m->gu_stride;
       P[3].router = m->router[l];
       P[3].xsrc = X_NORM;
       P[3].xptr = kv->resid;
@@ -389,7 +404,6 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
         gemv(D, m->dn[l]);
         D.moe = k == 0 ? MOE_DOWN0 : MOE_DOWN1;
         D.n_experts = E;
-        D.expert_stride = m->dn_stride;
         D.xsrc = X_F32;
         D.xptr = kv->h + (size_t)k * c.ffn;
         D.epi = EPI_MOE_RESID;
@@ -404,16 +418,19 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
   lm.gain = m->g_final;
   lm.eps = c.eps;
   lm.epi = EPI_LOGITS;
+  // grid barriers: phase i waits on barrier i - 1, which phase i - 1 signals,
+  // unless it is chained to its predecessor
   for (int i = 0; i < nph; ++i) {
-    ph[i].wait_bar = i == 0 ? -1 : i - 1;
-    ph[i].signal_bar = i == nph - 1 ? -1 : i;
+    ph[i].wait_bar = (i == 0 || chained[i]) ? -1 : i - 1;
+    ph[i].signal_bar = (i == nph - 1 || chained[i + 1]) ? -1 : i;
   }
   kv->nphases = nph;
   if (e == cudaSuccess) e = cudaMemcpy(kv->prog, ph.data(), ph.size() * sizeof(Phase), cudaMemcpyHostToDevice);
 
   // The verify program: the same layers over up to MAX_M rows, each GEMV
-  // phase reading its rows' inputs at a row stride; a MoE layer streams the
-  // union of the rows' experts (gate/up, then down) once.
+  // phase reading its rows' inputs at a row stride, every phase behind a grid
+  // barrier; a MoE layer streams the union of the rows' experts (gate/up,
+  // then down) once.
   const int nvph = 5 * L + 1;
   std::vector<Phase> vp(nvph);
   memset(vp.data(), 0, vp.size() * sizeof(Phase));
@@ -422,8 +439,10 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     Phase* P = &vp[5 * l];
     const Phase* D = &ph[ppl * l];
     P[0] = D[0];  // q/k/v: rows m at pos + m
+    P[0].headc = nullptr;
     P[0].out_mstride = 0;
     P[1] = D[1];  // attention of each row
+    P[1].headc = nullptr;
     P[2] = D[2];  // o
     P[2].x_mstride = Hq * hd;
     P[2].out_mstride = c.d;
@@ -471,6 +490,18 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     return rc;
   }
   *out = kv;
+  return GF_OK;
+}
+
+int gf_kv_reset(gf_kv* kv, gf_stream stream) {
+  if (!kv) {
+    set_error("gf_kv_reset: null handle");
+    return GF_EINVAL;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  GF_CUDA(cudaMemsetAsync(kv->kc, 0, kv->cache_elems * 2, s));
+  GF_CUDA(cudaMemsetAsync(kv->vc, 0, kv->cache_elems * 2, s));
+  GF_CUDA(cudaMemsetAsync(kv->counters, 0, kv->counter_bytes, s));
   return GF_OK;
 }
 

@@ -1,13 +1,16 @@
-// quant.cu — offline weight preparation: int8 and int4-G32 weight-only
-// quantisation written straight into the packed tile layout, bf16 repack, and
-// the inverse unpack kernels used for bit-exact layout checks.
+// quant.cu — offline weight preparation: int8 and int4 grouped weight-only
+// quantisation written straight into the device layout (slots of 32 rows x
+// 256 bytes, int4 scale/zero words after each slot's codes), the bf16 repack
+// into the same slots, the inverse unpack kernels used for bit-exact layout
+// checks, and the column-sliced copy of a down projection for the fused FFN.
 //
 // Quantisation follows the gpt-fast README, section "Quantization" (int8
-// weight-only; int4 weight-only with --groupsize 32), read as: int8 symmetric
-// per output row, s = bf16(max|w| / 127); int4 per row and 32-wide K group,
-// z = min, s = bf16((max - min) / 15), codes 0..15.  Every quotient is an
-// IEEE fp32 division and every rounding to an integer is rint (ties to even),
-// so the codes are bit-identical to any IEEE implementation of the same steps.
+// weight-only; int4 weight-only with --groupsize 32 / 64 / 128), read as: int8
+// symmetric per output row, s = bf16(max|w| / 127); int4 per row and G-wide K
+// group, z = min, s = bf16((max - min) / 15), codes 0..15.  Every quotient is
+// an IEEE fp32 division and every rounding to an integer is rint (ties to
+// even), so the codes are bit-identical to any IEEE implementation of the
+// same steps.
 #include "gf_internal.cuh"
 
 namespace gf {
@@ -19,25 +22,10 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   return (uint16_t)(u >> 16);
 }
 
-struct ChunkAddr {
-  long long code, sz;
-};
-__device__ __forceinline__ ChunkAddr chunk_addr(int dt, int N, int C, int n, int c) {
-  int t = n / TR, r = n % TR;
-  int Rt = min(TR, N - t * TR);
-  int b = c / KBLK, l = c % KBLK;
-  int Lb = min(KBLK, C - b * KBLK);
-  long long base = block_offset(dt, C, t, Rt, b);
-  ChunkAddr a;
-  a.code = base + (long long)(r * Lb + l) * 16;
-  a.sz = base + (long long)Rt * Lb * 16 + (long long)(r * Lb + l) * 4;
-  return a;
-}
-
 __device__ __forceinline__ int warp_id_global() { return (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); }
 __device__ __forceinline__ int warps_total() { return (int)((gridDim.x * blockDim.x) >> 5); }
 
-// int8: one warp per output row.
+// int8: one warp per output row; codes [N][K] stored as q + 128.
 __global__ void __launch_bounds__(256) k_quant_w8(const uint16_t* __restrict__ W, int N, int K,
                                                   uint8_t* __restrict__ P, uint16_t* __restrict__ S) {
   const int lane = threadIdx.x & 31, C = K / 16;
@@ -71,84 +59,75 @@ __global__ void __launch_bounds__(256) k_quant_w8(const uint16_t* __restrict__ W
         }
         words[j] = word;
       }
-      ChunkAddr a = chunk_addr(DT_INT8, N, C, n, c);
-      *reinterpret_cast<uint4*>(P + a.code) = make_uint4(words[0], words[1], words[2], words[3]);
+      *reinterpret_cast<uint4*>(P + code_addr(DT_INT8, K, 32, n, (long long)c * 16)) =
+          make_uint4(words[0], words[1], words[2], words[3]);
     }
   }
 }
 
-// int4 G=32: one warp per output row, one lane per group.
-__global__ void __launch_bounds__(256) k_quant_w4g(const uint16_t* __restrict__ W, int N, int K,
+// bf16: 16-byte chunks moved into their slots.
+__global__ void __launch_bounds__(256) k_repack_bf16(const uint16_t* __restrict__ W, int N, int K,
+                                                     uint8_t* __restrict__ P) {
+  const int lane = threadIdx.x & 31, C = K / 8;
+  for (int n = warp_id_global(); n < N; n += warps_total())
+    for (int c = lane; c < C; c += 32)
+      *reinterpret_cast<uint4*>(P + code_addr(DT_BF16, K, 32, n, (long long)c * 16)) =
+          *reinterpret_cast<const uint4*>(W + (size_t)n * K + c * 8);
+}
+
+// int4, group G (a multiple of 32): one warp per output row, one lane per
+// group.  Codes two per byte (code 2i low nibble of byte i of the row) and
+// the scale/zero word of each (row, group), in their slots.
+__global__ void __launch_bounds__(256) k_quant_w4g(const uint16_t* __restrict__ W, int N, int K, int G,
                                                    uint8_t* __restrict__ P) {
-  const int lane = threadIdx.x & 31, C = K / 32;
+  const int lane = threadIdx.x & 31, ng = K / G;
   for (int n = warp_id_global(); n < N; n += warps_total()) {
     const uint16_t* row = W + (size_t)n * K;
-    for (int c = lane; c < C; c += 32) {
-      float w[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(row + c * 32 + q * 8);
-        const uint32_t h[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          w[q * 8 + 2 * i] = __uint_as_float(h[i] << 16);
-          w[q * 8 + 2 * i + 1] = __uint_as_float(h[i] & 0xFFFF0000u);
-        }
-      }
+    for (int g = lane; g < ng; g += 32) {
+      const uint16_t* w = row + (size_t)g * G;
       // running min / max in index order, strict comparisons (so a signed
       // zero is kept exactly as the first one met)
-      float mn = w[0], mx = w[0];
-#pragma unroll
-      for (int i = 1; i < 32; ++i) {
-        if (w[i] < mn) mn = w[i];
-        if (w[i] > mx) mx = w[i];
+      float mn = bf2f(w[0]), mx = mn;
+      for (int i = 1; i < G; ++i) {
+        const float v = bf2f(w[i]);
+        if (v < mn) mn = v;
+        if (v > mx) mx = v;
       }
       const float range = mx - mn;
       const uint16_t sb = f2bf(range / 15.0f);
       const float sv = bf2f(sb);
       const uint16_t zb = f2bf(mn);
-      uint32_t words[4];
+      for (int c = 0; c < G; c += 32) {
+        uint32_t words[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t word = 0;
+        for (int j = 0; j < 4; ++j) {
+          uint32_t word = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          int code = 0;
-          if (sv != 0.0f) {
-            code = (int)rintf((w[8 * j + i] - mn) / sv);
-            code = max(0, min(15, code));
+          for (int i = 0; i < 8; ++i) {
+            int code = 0;
+            if (sv != 0.0f) {
+              code = (int)rintf((bf2f(w[c + 8 * j + i]) - mn) / sv);
+              code = max(0, min(15, code));
+            }
+            word |= (uint32_t)code << (4 * i);
           }
-          word |= (uint32_t)code << (4 * i);
+          words[j] = word;
         }
-        words[j] = word;
+        *reinterpret_cast<uint4*>(P + code_addr(DT_INT4, K, G, n, ((long long)g * G + c) / 2)) =
+            make_uint4(words[0], words[1], words[2], words[3]);
       }
-      ChunkAddr a = chunk_addr(DT_INT4, N, C, n, c);
-      *reinterpret_cast<uint4*>(P + a.code) = make_uint4(words[0], words[1], words[2], words[3]);
-      *reinterpret_cast<uint32_t*>(P + a.sz) = (uint32_t)sb | ((uint32_t)zb << 16);
+      *reinterpret_cast<uint32_t*>(P + sz_addr(K, G, n, g)) = (uint32_t)sb | ((uint32_t)zb << 16);
     }
   }
 }
 
-__global__ void __launch_bounds__(256) k_repack_bf16(const uint16_t* __restrict__ W, int N, int K,
-                                                     uint8_t* __restrict__ P) {
-  const int lane = threadIdx.x & 31, C = K / 8;
-  for (int n = warp_id_global(); n < N; n += warps_total()) {
-    for (int c = lane; c < C; c += 32) {
-      ChunkAddr a = chunk_addr(DT_BF16, N, C, n, c);
-      *reinterpret_cast<uint4*>(P + a.code) = *reinterpret_cast<const uint4*>(W + (size_t)n * K + c * 8);
-    }
-  }
-}
-
-// packed -> logical (for layout checks)
-__global__ void __launch_bounds__(256) k_unpack(int dt, const uint8_t* __restrict__ P, int N, int K,
-                                                void* __restrict__ Q, uint16_t* __restrict__ S,
-                                                uint16_t* __restrict__ Z) {
+// device layout -> logical (for layout checks)
+__global__ void __launch_bounds__(256) k_unpack(int dt, const uint8_t* __restrict__ P, int N, int K, int G,
+                                                void* __restrict__ Q, uint16_t* __restrict__ S, uint16_t* __restrict__ Z) {
   const int lane = threadIdx.x & 31, E = per_chunk(dt), C = K / E;
   for (int n = warp_id_global(); n < N; n += warps_total()) {
     for (int c = lane; c < C; c += 32) {
-      ChunkAddr a = chunk_addr(dt, N, C, n, c);
-      const uint4 v = *reinterpret_cast<const uint4*>(P + a.code);
+      const uint4 v = *reinterpret_cast<const uint4*>(P + code_addr(dt, K, G, n, (long long)c * 16));
       const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
       if (dt == DT_BF16) {
         *reinterpret_cast<uint4*>((uint16_t*)Q + (size_t)n * K + c * 8) = v;
@@ -160,9 +139,13 @@ __global__ void __launch_bounds__(256) k_unpack(int dt, const uint8_t* __restric
         for (int j = 0; j < 4; ++j) {
           for (int i = 0; i < 8; ++i) q[8 * j + i] = (uint8_t)((wv[j] >> (4 * i)) & 15u);
         }
-        const uint32_t sz = *reinterpret_cast<const uint32_t*>(P + a.sz);
-        S[(size_t)n * C + c] = (uint16_t)sz;
-        Z[(size_t)n * C + c] = (uint16_t)(sz >> 16);
+      }
+    }
+    if (dt == DT_INT4) {
+      for (int g = lane; g < K / G; g += 32) {
+        const uint32_t sz = *reinterpret_cast<const uint32_t*>(P + sz_addr(K, G, n, g));
+        S[(size_t)n * (K / G) + g] = (uint16_t)sz;
+        Z[(size_t)n * (K / G) + g] = (uint16_t)(sz >> 16);
       }
     }
   }
@@ -180,38 +163,57 @@ static int check_w(const char* fn, int dt, const void* W, int N, int K) {
   return GF_OK;
 }
 
+static bool group_ok(int G, int K) { return (G == 32 || G == 64 || G == 128) && K % G == 0; }
+
 static int grid_for_rows(int N) {
   int sms = device_sms();
   int blocks = (N + 7) / 8;
   return blocks < sms * 16 ? blocks : sms * 16;
 }
 
-// Column-sliced copy of a packed matrix, for a down projection fused behind
-// its gate/up GEMV: slice j holds columns 16j .. 16j+15 of every row, rows
-// consecutive (int4: 8 bytes = 16 codes a row, the two slices of a 32-wide
-// group followed by that group's scale/zero words, one per row; int8: 16
-// bytes a row; bf16: 32 bytes a row).  One thread per (row, slice).
-__global__ void __launch_bounds__(256) k_pack_cols(int dt, const uint8_t* __restrict__ P, int N, int K,
+// Quantises (or repacks) W [N][K] into `packed` (packed_bytes bytes, already
+// zeroed: the padding of ragged tiles and K-slots must read as zero); int8
+// row scales into s8.
+int quantize_rows(int dt, const void* W, int N, int K, int G, void* packed, void* s8, cudaStream_t s) {
+  if (dt == DT_BF16) {
+    k_repack_bf16<<<grid_for_rows(N), 256, 0, s>>>((const uint16_t*)W, N, K, (uint8_t*)packed);
+  } else if (dt == DT_INT8) {
+    k_quant_w8<<<grid_for_rows(N), 256, 0, s>>>((const uint16_t*)W, N, K, (uint8_t*)packed, (uint16_t*)s8);
+  } else {
+    k_quant_w4g<<<grid_for_rows(N), 256, 0, s>>>((const uint16_t*)W, N, K, G, (uint8_t*)packed);
+  }
+  GF_CUDA(cudaGetLastError());
+  return GF_OK;
+}
+
+// Column-sliced copy of a matrix in the device layout, for a down projection
+// fused behind its gate/up GEMV.  int4: per group of 32 columns, the rows'
+// 8 code bytes of columns 0..15, then of columns 16..31, then the rows'
+// scale/zero words (of the group that holds those columns); int8: per 16
+// columns, the rows' 16 code bytes; bf16: per 16 columns, the rows' first 8
+// values (16 bytes), then their last 8.  One thread per (row, 16 columns).
+__global__ void __launch_bounds__(256) k_pack_cols(int dt, const uint8_t* __restrict__ P, int N, int K, int G,
                                                    uint8_t* __restrict__ out) {
-  const int C = K / per_chunk(dt), nsl = K / 16;
+  const int nsl = K / 16;
   const long long total = (long long)N * nsl;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
     const int n = (int)(i % N), j = (int)(i / N);
     if (dt == DT_INT4) {
-      const ChunkAddr a = chunk_addr(DT_INT4, N, C, n, j >> 1);
-      const uint2 w = *reinterpret_cast<const uint2*>(P + a.code + (j & 1) * 8);
+      const uint2 w = *reinterpret_cast<const uint2*>(P + code_addr(DT_INT4, K, G, n, (long long)j * 8));
       uint8_t* g = out + (size_t)(j >> 1) * N * 20;
       *reinterpret_cast<uint2*>(g + (size_t)(j & 1) * N * 8 + (size_t)n * 8) = w;
-      if ((j & 1) == 0) *reinterpret_cast<uint32_t*>(g + (size_t)N * 16 + (size_t)n * 4) =
-          *reinterpret_cast<const uint32_t*>(P + a.sz);
+      if ((j & 1) == 0)
+        *reinterpret_cast<uint32_t*>(g + (size_t)N * 16 + (size_t)n * 4) =
+            *reinterpret_cast<const uint32_t*>(P + sz_addr(K, G, n, 16 * j / G));
     } else if (dt == DT_INT8) {
-      const ChunkAddr a = chunk_addr(DT_INT8, N, C, n, j);
-      *reinterpret_cast<uint4*>(out + ((size_t)j * N + n) * 16) = *reinterpret_cast<const uint4*>(P + a.code);
+      *reinterpret_cast<uint4*>(out + ((size_t)j * N + n) * 16) =
+          *reinterpret_cast<const uint4*>(P + code_addr(DT_INT8, K, 32, n, (long long)j * 16));
     } else {
-      const ChunkAddr a0 = chunk_addr(DT_BF16, N, C, n, 2 * j), a1 = chunk_addr(DT_BF16, N, C, n, 2 * j + 1);
-      uint4* o = reinterpret_cast<uint4*>(out + ((size_t)j * N + n) * 32);
-      o[0] = *reinterpret_cast<const uint4*>(P + a0.code);
-      o[1] = *reinterpret_cast<const uint4*>(P + a1.code);
+      uint8_t* o = out + (size_t)j * N * 32;
+      *reinterpret_cast<uint4*>(o + (size_t)n * 16) =
+          *reinterpret_cast<const uint4*>(P + code_addr(DT_BF16, K, 32, n, (long long)j * 32));
+      *reinterpret_cast<uint4*>(o + (size_t)N * 16 + (size_t)n * 16) =
+          *reinterpret_cast<const uint4*>(P + code_addr(DT_BF16, K, 32, n, (long long)j * 32 + 16));
     }
   }
 }
@@ -220,14 +222,14 @@ long long cols_bytes(int dt, int N, int K) {
   return dt == DT_INT4 ? (long long)(K / 32) * N * 20 : (long long)(K / 16) * N * (dt == DT_INT8 ? 16 : 32);
 }
 
-int pack_cols(int dt, const void* packed, int N, int K, void* out, cudaStream_t s) {
+int pack_cols(int dt, const void* packed, int N, int K, int G, void* out, cudaStream_t s) {
   if (K % 32 || N <= 0) {
     set_error("column-sliced copy: K must be a multiple of 32 (got %d)", K);
     return GF_EINVAL;
   }
   const long long total = (long long)N * (K / 16);
   const int blocks = (int)((total + 255) / 256 < 65535 ? (total + 255) / 256 : 65535);
-  k_pack_cols<<<blocks, 256, 0, s>>>(dt, (const uint8_t*)packed, N, K, (uint8_t*)out);
+  k_pack_cols<<<blocks, 256, 0, s>>>(dt, (const uint8_t*)packed, N, K, G, (uint8_t*)out);
   GF_CUDA(cudaGetLastError());
   return GF_OK;
 }
@@ -238,28 +240,31 @@ using namespace gf;
 
 extern "C" {
 
+long long gf_packed_bytes_w4g(int N, int K, int G) {
+  if (N <= 0 || K <= 0 || K % 32 || !group_ok(G, K)) return -1;
+  return packed_bytes(DT_INT4, N, K, G);
+}
+
 int gf_quantize_w8(const void* W, int N, int K, void* packed, void* s, gf_stream stream) {
   int rc = check_w("gf_quantize_w8", DT_INT8, W, N, K);
   if (rc) return rc;
   if (!packed || !s) { set_error("gf_quantize_w8: null output"); return GF_EINVAL; }
   if (!aligned16(packed) || !aligned16(s)) { set_error("gf_quantize_w8: outputs must be 16-byte aligned"); return GF_EALIGN; }
-  k_quant_w8<<<grid_for_rows(N), 256, 0, (cudaStream_t)stream>>>((const uint16_t*)W, N, K, (uint8_t*)packed,
-                                                                   (uint16_t*)s);
-  GF_CUDA(cudaGetLastError());
-  return GF_OK;
+  GF_CUDA(cudaMemsetAsync(packed, 0, (size_t)packed_bytes(DT_INT8, N, K, 32), (cudaStream_t)stream));
+  return quantize_rows(DT_INT8, W, N, K, 32, packed, s, (cudaStream_t)stream);
 }
 
 int gf_quantize_w4g(const void* W, int N, int K, int G, void* packed, gf_stream stream) {
-  if (G != 32) { set_error("gf_quantize_w4g: only group size 32 is supported (got %d)", G); return GF_EUNSUPPORTED; }
   int rc = check_w("gf_quantize_w4g", DT_INT4, W, N, K);
   if (rc) return rc;
+  if (!group_ok(G, K)) {
+    set_error("gf_quantize_w4g: group size must be 32, 64 or 128 and divide K (G=%d, K=%d)", G, K);
+    return GF_EUNSUPPORTED;
+  }
   if (!packed) { set_error("gf_quantize_w4g: null output"); return GF_EINVAL; }
   if (!aligned16(packed)) { set_error("gf_quantize_w4g: output must be 16-byte aligned"); return GF_EALIGN; }
-  // scale-word padding of a ragged tile must read as zero
-  if (N % TR) GF_CUDA(cudaMemsetAsync(packed, 0, (size_t)packed_bytes(DT_INT4, N, K), (cudaStream_t)stream));
-  k_quant_w4g<<<grid_for_rows(N), 256, 0, (cudaStream_t)stream>>>((const uint16_t*)W, N, K, (uint8_t*)packed);
-  GF_CUDA(cudaGetLastError());
-  return GF_OK;
+  GF_CUDA(cudaMemsetAsync(packed, 0, (size_t)packed_bytes(DT_INT4, N, K, G), (cudaStream_t)stream));
+  return quantize_rows(DT_INT4, W, N, K, G, packed, nullptr, (cudaStream_t)stream);
 }
 
 int gf_repack_bf16(const void* W, int N, int K, void* packed, gf_stream stream) {
@@ -267,32 +272,34 @@ int gf_repack_bf16(const void* W, int N, int K, void* packed, gf_stream stream) 
   if (rc) return rc;
   if (!packed) { set_error("gf_repack_bf16: null output"); return GF_EINVAL; }
   if (!aligned16(packed)) { set_error("gf_repack_bf16: output must be 16-byte aligned"); return GF_EALIGN; }
-  k_repack_bf16<<<grid_for_rows(N), 256, 0, (cudaStream_t)stream>>>((const uint16_t*)W, N, K, (uint8_t*)packed);
-  GF_CUDA(cudaGetLastError());
-  return GF_OK;
+  GF_CUDA(cudaMemsetAsync(packed, 0, (size_t)packed_bytes(DT_BF16, N, K, 32), (cudaStream_t)stream));
+  return quantize_rows(DT_BF16, W, N, K, 32, packed, nullptr, (cudaStream_t)stream);
 }
 
-static int unpack_common(const char* fn, int dt, const void* packed, int N, int K, void* q, void* s, void* z,
+static int unpack_common(const char* fn, int dt, const void* packed, int N, int K, int G, void* q, void* s, void* z,
                          gf_stream stream) {
   int rc = check_w(fn, dt, packed, N, K);
   if (rc) return rc;
   if (!q || (dt == DT_INT4 && (!s || !z))) { set_error("%s: null output", fn); return GF_EINVAL; }
   if (!aligned16(q)) { set_error("%s: outputs must be 16-byte aligned", fn); return GF_EALIGN; }
-  k_unpack<<<grid_for_rows(N), 256, 0, (cudaStream_t)stream>>>(dt, (const uint8_t*)packed, N, K, q, (uint16_t*)s,
+  k_unpack<<<grid_for_rows(N), 256, 0, (cudaStream_t)stream>>>(dt, (const uint8_t*)packed, N, K, G, q, (uint16_t*)s,
                                                                  (uint16_t*)z);
   GF_CUDA(cudaGetLastError());
   return GF_OK;
 }
 
 int gf_unpack_w8(const void* packed, int N, int K, void* q, gf_stream stream) {
-  return unpack_common("gf_unpack_w8", DT_INT8, packed, N, K, q, nullptr, nullptr, stream);
+  return unpack_common("gf_unpack_w8", DT_INT8, packed, N, K, 32, q, nullptr, nullptr, stream);
 }
 int gf_unpack_w4g(const void* packed, int N, int K, int G, void* q, void* s, void* z, gf_stream stream) {
-  if (G != 32) { set_error("gf_unpack_w4g: only group size 32 is supported"); return GF_EUNSUPPORTED; }
-  return unpack_common("gf_unpack_w4g", DT_INT4, packed, N, K, q, s, z, stream);
+  if (!group_ok(G, K)) {
+    set_error("gf_unpack_w4g: group size must be 32, 64 or 128 and divide K (G=%d, K=%d)", G, K);
+    return GF_EUNSUPPORTED;
+  }
+  return unpack_common("gf_unpack_w4g", DT_INT4, packed, N, K, G, q, s, z, stream);
 }
 int gf_unpack_bf16(const void* packed, int N, int K, void* W, gf_stream stream) {
-  return unpack_common("gf_unpack_bf16", DT_BF16, packed, N, K, W, nullptr, nullptr, stream);
+  return unpack_common("gf_unpack_bf16", DT_BF16, packed, N, K, 32, W, nullptr, nullptr, stream);
 }
 
 }  // extern "C"
