@@ -192,6 +192,7 @@ struct Smem {
   int* bcast;       // [64] broadcast ints; [32..33] chosen experts, [34] phase they were chosen in,
                     // [48..55] verify: union of the rows' experts, [56] its size
   float* moew;      // [MAX_M][8] verify: weight of expert e for row m (0 if not chosen)
+  int* ffnc;        // [2][FFN_HN] PH_FFN: SwiGLU buffer rounds written, down pieces finished (zero between phases)
   Phase* phb;       // [2] the consumers' copies of the current and next phase descriptor
 };
 
@@ -213,6 +214,7 @@ __device__ __forceinline__ Smem smem_layout(uint8_t* raw) {
   s.red = reinterpret_cast<float*>(base + OFF_MISC);
   s.bcast = reinterpret_cast<int*>(base + OFF_MISC + 256);
   s.moew = reinterpret_cast<float*>(base + OFF_MISC + 512);
+  s.ffnc = reinterpret_cast<int*>(base + OFF_MISC + 768);
   s.phb = reinterpret_cast<Phase*>(base + OFF_PHB);
   return s;
 }
@@ -415,6 +417,10 @@ __device__ void producer(const Params& P, const Smem& S, int cta, int pos, int p
       const int tps = (Ns + TR - 1) / TR, ntiles = nseg * tps;
       for (int t = first_unit(cta, ph.rot, G); t < ntiles && ok; t += G)
         for (int b = 0; b < nb && ok; ++b) ok = produce_gemv_slot(ph, P, S, pr, eseg[t / tps], tps, t % tps, b);
+    } else if (ph.kind == PH_OSPLIT) {
+      const int nb = k_slots(ph.dtype, ph.K), tps = (ph.N + TR - 1) / TR;
+      for (int u = first_unit(cta, ph.rot, G); u < tps * nb && ok; u += G)
+        ok = produce_gemv_slot(ph, P, S, pr, 0, tps, u / nb, u % nb);
     } else if (ph.kind == PH_FFN) {
       const int dt = ph.dtype, nb = k_slots(dt, ph.K);
       const int tps = ph.N / TR, d = ph.N2;
@@ -520,6 +526,7 @@ struct Cons {
   int warp, lane, ctid;
   uint32_t starved;  // slot waits that found the slot still in flight (warp 0)
   float rnorm;       // RMSNorm factor of the staged input (1 if none)
+  bool wnorm;        // staged per warp: the RMSNorm factor is formed at the combine from S.red
   uint64_t lim;      // limit of the bounded waits
 };
 
@@ -605,6 +612,61 @@ __device__ __forceinline__ void stage_store(const Smem& S, const Cons& cs, int d
   }
 }
 
+// Per-warp staging.  When the K-slots of a phase's tiles are a multiple of
+// the warp count, slot (tile, b) always belongs to warp (phase start + b) mod
+// NCW, so each warp stages only the input slices of its own K-slots (zero past
+// K): no CTA-wide barrier before the GEMV starts.  For an RMSNorm input each
+// warp leaves the sum of squares of its slices in S.red[warp]; the combining
+// warp of a tile forms 1/rms from all of them (every warp contributes to
+// every tile, so all are written by then).  Used for every non-MoE GEMV and
+// fused-FFN phase of the decode step whose K-slots divide evenly.
+__device__ __forceinline__ bool warp_stageable(const Phase& ph) {
+  return ph.moe == MOE_NONE && k_slots(ph.dtype, ph.K) % NCW == 0 && ph.xsrc != X_NONE;
+}
+__device__ void stage_x_warp(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
+  const int K = ph.K, dt = ph.dtype, G = ph.G, K4 = K / 4, SK4 = slot_k(dt) / 4, nb = k_slots(dt, K);
+  const bool norm = ph.xsrc == X_NORM || ph.xsrc == X_EMBED_NORM;
+  const uint16_t* emb = ph.xsrc == X_EMBED_NORM ? P.embed + (size_t)(*P.token) * K : nullptr;
+  float4* xs4 = reinterpret_cast<float4*>(S.xs);
+  float ss = 0.f;
+  for (int b = (cs.warp - (int)(cs.it % NCW) + NCW) % NCW; b < nb; b += NCW) {
+    for (int f = b * SK4 + cs.lane; f < (b + 1) * SK4; f += 32) {  // whole warps of consecutive float4
+      const bool in = f < K4;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (in) {
+        if (ph.xsrc == X_F32 || ph.xsrc == X_NORM) {
+          a = __ldcg(reinterpret_cast<const float4*>(ph.xptr) + f);
+        } else {
+          const uint2* src = emb ? reinterpret_cast<const uint2*>(emb) : reinterpret_cast<const uint2*>(ph.xptr);
+          a = bf4(__ldcg(src + f));
+        }
+      }
+      if (norm) {
+        ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+        if (emb && cta == 0 && in) reinterpret_cast<float4*>(P.resid)[f] = a;
+        const float4 g = bf4(in ? reinterpret_cast<const uint2*>(ph.gain)[f] : make_uint2(0u, 0u));
+        a = make_float4(a.x * g.x, a.y * g.y, a.z * g.z, a.w * g.w);
+      }
+      stage_store(S, cs, dt, G, f, true, a);
+    }
+  }
+  cs.rnorm = 1.0f;
+  cs.wnorm = norm;
+  if (norm) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (cs.lane == 0) S.red[cs.warp] = ss;
+  }
+  __syncwarp();
+}
+// 1 / rms of a warp-staged RMSNorm input (after every warp staged its part)
+__device__ __forceinline__ float warp_rnorm(const Phase& ph, const Smem& S) {
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < NCW; ++w) tot += S.red[w];
+  return 1.0f / sqrtf(tot / (float)ph.K + ph.eps);
+}
+
 // Stages the phase's input vector into shared memory as fp32, zero from K up
 // to the end of the last K-slot (the slots' padding codes are zero, and the
 // products with them must be exactly zero).  For an
@@ -686,6 +748,7 @@ __device__ bool stage_x(const Phase& ph, const Params& P, const Smem& S, Cons& c
   }
   if (!cta_sync(S, cs, P.err)) return false;
   cs.rnorm = 1.0f;
+  cs.wnorm = false;
   if (norm) {
     float tot = 0.0f;
 #pragma unroll
@@ -984,7 +1047,7 @@ __device__ __forceinline__ int gemv_tile(const Phase& ph, const Params& P, const
     __threadfence_block();
     *reinterpret_cast<volatile int*>(S.tbg + buf) = (int)(cs.useq + NTB);  // hand the buffer on
   }
-  tot = t * pf;
+  tot = t * pf * (cs.wnorm ? warp_rnorm(ph, S) : 1.0f);
   return 1;
 }
 
@@ -1010,13 +1073,73 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
     const int n = lt * TR + lane;
     const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
     if (n < Ns) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, rp, am);
-    if (ph.headc) {  // q/k/v rows of this tile are in memory: count them for its kv group
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) atomicAdd(ph.headc + qkv_group(ph, lt), 1u);
-    }
   }
   cs.it += j;
+  return true;
+}
+
+// The o projection split by K-slot (PH_OSPLIT).  The CTA's units (tile,
+// K-slot), round-robin over the CTAs, are one slot each, so each runs on one
+// warp alone: it waits (bounded) until the attention of every kv group with a
+// head in the K-slot has published its outputs, stages those SK inputs (fp32
+// attention outputs, times the dequantisation powers, with their group sums)
+// in its own shared-memory area, runs the slot, and adds the 32 partial row
+// sums to the residual.  The FFN behind it waits for all of them at its grid
+// barrier.
+template <int DT>
+__device__ bool osplit_phase(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
+  constexpr int SK = slot_k(DT), PL = SK / 32;  // inputs per slot, per lane
+  const int G = P.nctas, nb = k_slots(DT, ph.K), tps = (ph.N + TR - 1) / TR;
+  const int first = first_unit(cta, ph.rot, G), nu = units_of(first, tps * nb, G);
+  const int lane = cs.lane, w = cs.warp, gq = ph.Hq / ph.Hkv;
+  float* xw = S.xs + w * (512 + 32);  // this warp's inputs
+  float* xsw = xw + 512;              // and their group / chunk sums
+  const float* attn = reinterpret_cast<const float*>(ph.xptr);
+  for (int k = 0; k < nu; ++k) {
+    const uint32_t it = cs.it + (uint32_t)k;
+    if ((int)(it % NCW) != w) continue;
+    const int u = first + k * G, lt = u / nb, b = u % nb;
+    int ok = 1;
+    if (lane == 0) {
+      const int h0 = b * SK / ph.hd, h1 = min((b * SK + SK - 1) / ph.hd, ph.Hq - 1);
+      for (int g = h0 / gq; g <= h1 / gq && ok; ++g) ok = counter_wait(ph.attd + g, 1u, P.err, ERR_WAIT_HEAD, cs.lim);
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    // inputs b*SK .. b*SK + SK - 1: lane l holds PL consecutive ones
+    float sg = 0.f;
+#pragma unroll
+    for (int q = 0; q < PL / 4; ++q) {
+      const int f4 = lane * (PL / 4) + q, k4 = (b * SK) / 4 + f4;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (4 * k4 < ph.K) a = __ldcg(reinterpret_cast<const float4*>(attn) + k4);
+      const float4 mu = dq_mult(DT, f4 & 7);
+      reinterpret_cast<float4*>(xw)[f4] = make_float4(a.x * mu.x, a.y * mu.y, a.z * mu.z, a.w * mu.w);
+      sg += (a.x + a.y) + (a.z + a.w);
+    }
+    if (DT != DT_BF16) {  // sums per int4 group / int8 chunk of 16
+      const int span = DT == DT_INT4 ? ph.G / PL : 16 / PL;  // lanes per group / chunk
+      for (int o = 1; o < span; o <<= 1) sg += __shfl_xor_sync(0xffffffffu, sg, o);
+      if ((lane & (span - 1)) == 0) xsw[lane / span] = sg * (DT == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
+    }
+    __syncwarp();
+    const uint8_t* base;
+    if (!slot_acquire(S, cs, it, P.err, base)) return false;
+    float vr[4] = {0.f, 0.f, 0.f, 0.f}, bias = 0.f;
+    float2 acc[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
+    slot_dot<DT>(base, lane, ph.G, xw, xsw, vr, acc, bias);
+    slot_release(S, cs, it);
+    const float v = rows_total<DT>(vr, acc, bias, lane);
+    const int n = lt * TR + lane;
+    if (n < ph.N) {
+      float f = DT == DT_BF16 ? 1.0f : DQ_UP;
+      if (DT == DT_INT8) f *= bf2f(ph.s8[n]);
+      atomicAdd(reinterpret_cast<float*>(ph.out) + n, v * f);
+    }
+    __syncwarp();  // the warp's inputs are read before the next unit restages them
+  }
+  cs.it += (uint32_t)nu;
   return true;
 }
 
@@ -1070,12 +1193,12 @@ __device__ bool ffn_phase(const Phase& ph, const Params& P, const Smem& S, Cons&
   const int ND = NCW * fs.P;
   const int lane = cs.lane, w = cs.warp;
   float* hb = S.xs + round_up(ph.K, slot_k(DT));          // [FFN_HN][16] SwiGLU outputs of the tiles in flight
-  int* hcnt = reinterpret_cast<int*>(hb + FFN_HN * 16);   // [FFN_HN] rounds of each buffer written
+  int* hcnt = S.ffnc;                                     // [FFN_HN] rounds of each buffer written
   int* dcnt = hcnt + FFN_HN;                              // [FFN_HN] down pieces of each buffer finished
-  float* dacc = reinterpret_cast<float*>(dcnt + FFN_HN);  // [d] this CTA's partial down outputs
-  for (int i = cs.ctid; i < d; i += NCW * 32) dacc[i] = 0.0f;
-  if (cs.ctid < 2 * FFN_HN) hcnt[cs.ctid] = 0;
-  if (!cta_sync(S, cs, P.err)) return false;
+  float* dacc = hb + FFN_HN * 16;                         // [d] this CTA's partial down outputs
+  // each warp zeroes the rows it owns (the counters are zero between phases)
+  for (int i = w * fs.RW + lane; i < min((w + 1) * fs.RW, d); i += 32) dacc[i] = 0.0f;
+  __syncwarp();
   const int first = first_unit(cta, ph.rot, G), nt = units_of(first, tps, G);
   const uint32_t X0 = cs.it;
   // the down pieces of local tile i for this warp
@@ -1162,6 +1285,7 @@ __device__ bool ffn_phase(const Phase& ph, const Params& P, const Smem& S, Cons&
   cs.it += (uint32_t)(nt * (nb + ND));
   // every warp's partial outputs are in dacc: add them to the residual
   if (!cta_sync(S, cs, P.err)) return false;
+  if (cs.ctid < 2 * FFN_HN) S.ffnc[cs.ctid] = 0;  // for the next FFN phase
   if (nt > 0) {
     float4* out = reinterpret_cast<float4*>(ph.out);
     for (int n4 = cs.ctid; n4 < d / 4; n4 += NCW * 32) {
@@ -1302,6 +1426,16 @@ __device__ __forceinline__ void attn_values(const AttnRows<HD, NP>& vr, int gq, 
   }
 }
 
+// The outputs of kv group kvh's heads are written (by this CTA's threads):
+// publish that for the o projection units waiting on the group (PH_OSPLIT).
+__device__ __forceinline__ bool attn_done(const Phase& ph, const Smem& S, Cons& cs, const Params& P, int kvh) {
+  if (!ph.attd) return true;
+  __threadfence();
+  if (!cta_sync(S, cs, P.err)) return false;
+  if (cs.ctid == 0) atomicAdd(ph.attd + kvh, 1u);
+  return true;
+}
+
 template <int HD, bool VER>
 __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, const AttnUnit& au, int pos,
                           uint32_t& j) {
@@ -1422,7 +1556,7 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
       }
     }
   }
-  if (nch == 1) return true;
+  if (nch == 1) return attn_done(ph, S, cs, P, kvh);
   __threadfence();
   if (!cta_sync(S, cs, P.err)) return false;
   unsigned* tick = ph.tick + (size_t)au.m * ph.Hkv + kvh;
@@ -1448,6 +1582,7 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
       else reinterpret_cast<uint16_t*>(ph.attn_out)[qrow + (size_t)hq * HD + d] = f2bf(O / L);
     }
     if (cs.ctid == 0) *tick = 0u;
+    return attn_done(ph, S, cs, P, kvh);
   }
   return true;
 }
@@ -1915,10 +2050,13 @@ __device__ bool argmax_finish(const Params& P, const Smem& S, Cons& cs, int cta,
 }
 
 // ============================================================== kernel ====
-// VER: the verification-pass instantiation (multi-row GEMV phases); the
-// decode instantiation carries the single-row GEMV and fused-FFN phases.
-// Splitting them keeps each kernel's register budget to its own code paths.
-template <bool VER>
+// One instantiation per weight type DT and pass kind: VER, the verification
+// pass (multi-row GEMV phases); otherwise the decode step (single-row GEMV,
+// fused FFN, split o projection).  Splitting them keeps each kernel's
+// register budget to its own code paths and its code small: the code that
+// runs once per phase (staging, attention, epilogues) otherwise misses the
+// instruction cache every time.
+template <int DT, bool VER>
 __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ Params P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const Smem S = smem_layout(smem_raw);
@@ -1936,6 +2074,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     S.tbg[tid] = tid;
   }
   if (tid == 0) S.bcast[34] = 0;
+  if (tid < 2 * FFN_HN) S.ffnc[tid] = 0;
   __syncthreads();
   const int pos = P.d_pos ? *P.d_pos : P.pos_const;
   // Reject a position or token that would index outside the cache, the RoPE
@@ -1972,6 +2111,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   cs.ctid = tid;
   cs.starved = 0;
   cs.rnorm = 1.0f;
+  cs.wnorm = false;
   cs.lim = wait_limit(P);
   const int G = P.nctas;
   ArgMax am = {-INFINITY, 0x7fffffff};
@@ -2009,29 +2149,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     if (tr) tr[1] = gtimer();
     if (ph.kind == PH_GEMV) {
       bool ok;
+      if (ph.dtype != DT) {
+        if (tid == 0) atomicCAS(P.err, 0, ERR_BAD_PROGRAM);
+        return;
+      }
       if (VER) {
         if (tr) tr[2] = gtimer();
-        if (ph.dtype == DT_INT4) ok = gemv_phase_m<DT_INT4>(ph, P, S, cs, cta, pos, pi, amv);
-        else if (ph.dtype == DT_INT8) ok = gemv_phase_m<DT_INT8>(ph, P, S, cs, cta, pos, pi, amv);
-        else ok = gemv_phase_m<DT_BF16>(ph, P, S, cs, cta, pos, pi, amv);
+        ok = gemv_phase_m<DT>(ph, P, S, cs, cta, pos, pi, amv);
       } else {
-        if (!stage_x(ph, P, S, cs, cta)) return;
+        if (warp_stageable(ph)) stage_x_warp(ph, P, S, cs, cta);
+        else if (!stage_x(ph, P, S, cs, cta)) return;
         if (ph.moe == MOE_GU && !route_experts(ph, P, S, cs, pi)) return;
         if (tr) tr[2] = gtimer();
-        if (ph.dtype == DT_INT4) ok = gemv_phase<DT_INT4>(ph, P, S, cs, cta, pos, am);
-        else if (ph.dtype == DT_INT8) ok = gemv_phase<DT_INT8>(ph, P, S, cs, cta, pos, am);
-        else ok = gemv_phase<DT_BF16>(ph, P, S, cs, cta, pos, am);
+        ok = gemv_phase<DT>(ph, P, S, cs, cta, pos, am);
       }
       if (!ok) return;
       if (ph.epi == EPI_LOGITS) any_logits = true;
-    } else if (ph.kind == PH_FFN && !VER) {
-      if (!stage_x(ph, P, S, cs, cta)) return;
+    } else if (ph.kind == PH_OSPLIT && !VER && ph.dtype == DT) {
+      if (tr) tr[2] = tr[1];
+      if (!osplit_phase<DT>(ph, P, S, cs, cta)) return;
+    } else if (ph.kind == PH_FFN && !VER && ph.dtype == DT) {
+      if (warp_stageable(ph)) stage_x_warp(ph, P, S, cs, cta);
+      else if (!stage_x(ph, P, S, cs, cta)) return;
       if (tr) tr[2] = gtimer();
-      bool ok;
-      if (ph.dtype == DT_INT4) ok = ffn_phase<DT_INT4>(ph, P, S, cs, cta, pos);
-      else if (ph.dtype == DT_INT8) ok = ffn_phase<DT_INT8>(ph, P, S, cs, cta, pos);
-      else ok = ffn_phase<DT_BF16>(ph, P, S, cs, cta, pos);
-      if (!ok) return;
+      if (!ffn_phase<DT>(ph, P, S, cs, cta, pos)) return;
     } else if (ph.kind == PH_ATTN) {
       if (tr) tr[2] = tr[1];
       const int nunits = attn_units(ph, P, pos, -1, nullptr);
@@ -2057,9 +2198,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     }
     cs.starved = 0;
     if (tid < PH16) cp_async_wait_all();  // the next phase's descriptor has landed
+    // Past the barrier below, lanes of warp 0 may start the next phase and
+    // overwrite this descriptor's buffer with the one after it: what is read
+    // of it later is read before, or by all of warp 0 before a __syncwarp.
+    const int sbar = ph.signal_bar;
+    const bool qkv_signal = ph.headc != nullptr && ph.kind == PH_GEMV;
     // every warp of this CTA has finished the phase (its global writes made)
     if (!cta_sync(S, cs, P.err)) return;
-    if (ph.signal_bar >= 0 && tid == 0) grid_arrive(P.bars + ph.signal_bar);
+    if (qkv_signal && warp == 0) {
+      // the q/k/v rows of this CTA's tiles are in memory: count them for their
+      // kv groups, one lane per local tile, each after a fence
+      __threadfence();
+      const int tps = (ph.N + TR - 1) / TR;
+      for (int t = first_unit(cta, ph.rot, G) + lane * G; t < tps; t += 32 * G)
+        atomicAdd(ph.headc + qkv_group(ph, t), 1u);
+      __syncwarp();
+    }
+    if (sbar >= 0 && tid == 0) grid_arrive(P.bars + sbar);
     if (tr) tr[4] = gtimer();
   }
   if (any_logits) {
@@ -2068,24 +2223,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
   }
 }
 
+// The kernel instantiation of a launch: weight type p.dtype, decode or verify.
+static const void* engine_fn(int dt, bool ver) {
+  static const void* fns[3][2] = {{(const void*)k_engine<DT_BF16, false>, (const void*)k_engine<DT_BF16, true>},
+                                  {(const void*)k_engine<DT_INT8, false>, (const void*)k_engine<DT_INT8, true>},
+                                  {(const void*)k_engine<DT_INT4, false>, (const void*)k_engine<DT_INT4, true>}};
+  return fns[dt][ver];
+}
+
 int launch_engine(const Params& p, int grid, bool cooperative, cudaStream_t s) {
-  static bool attr_set[64][2] = {};
+  static bool attr_set[64][3][2] = {};
   int dev = 0;
   GF_CUDA(cudaGetDevice(&dev));
   const bool ver = verifying(p);
-  const void* fn = ver ? (const void*)k_engine<true> : (const void*)k_engine<false>;
-  if (dev >= 0 && dev < 64 && !attr_set[dev][ver]) {
+  if (p.dtype < 0 || p.dtype > 2) {
+    set_error("engine launch: bad weight type %d", p.dtype);
+    return GF_EINVAL;
+  }
+  const void* fn = engine_fn(p.dtype, ver);
+  if (dev >= 0 && dev < 64 && !attr_set[dev][p.dtype][ver]) {
     GF_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    attr_set[dev][ver] = true;
+    attr_set[dev][p.dtype][ver] = true;
   }
-  if (cooperative) {
-    void* args[] = {const_cast<Params*>(&p)};
-    GF_CUDA(cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NTHREADS), args, SMEM_BYTES, s));
-  } else {
-    if (ver) k_engine<true><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
-    else k_engine<false><<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
-    GF_CUDA(cudaGetLastError());
-  }
+  void* args[] = {const_cast<Params*>(&p)};
+  if (cooperative) GF_CUDA(cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NTHREADS), args, SMEM_BYTES, s));
+  else GF_CUDA(cudaLaunchKernel(fn, dim3(grid), dim3(NTHREADS), args, SMEM_BYTES, s));
   return GF_OK;
 }
 
@@ -2127,6 +2289,7 @@ static int gemv_common(const char* fn, int dt, const void* x, const void* Wp, co
     return GF_EALIGN;
   }
   Params p = base_params();
+  p.dtype = dt;
   Phase& ph = p.single;
   ph.kind = PH_GEMV;
   ph.dtype = dt;

@@ -118,7 +118,10 @@ constexpr int VTG = 4;                       // tiles per group of a multi-row G
 // PH_FFN: a dense FFN in one phase -- the gate/up GEMV (rows interleaved) and,
 // per gate/up tile, the matching 16-column slice of the down projection
 // (column-sliced copy W2), accumulated per CTA and added to the residual.
-enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1, PH_FFN = 2 };
+// PH_OSPLIT: the o projection split by K-slot: unit (tile, K-slot) waits for
+// the attention of the slot's heads, stages those heads' outputs, and adds its
+// 32 partial row sums to the residual -- no grid barrier after the attention.
+enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1, PH_FFN = 2, PH_OSPLIT = 3 };
 enum XSrc { X_NONE = 0, X_BF16 = 1, X_NORM = 2, X_EMBED_NORM = 3, X_F32 = 4 };
 enum Epi {
   EPI_STORE_BF16 = 0,
@@ -162,7 +165,7 @@ struct alignas(16) Phase {
   int epi;
   int pad0;
   const uint8_t* W;        // packed matrix (experts back to back)
-  const void* pad1;
+  unsigned* attd;          // [Hkv] attention of each kv group finished (PH_ATTN signals, PH_OSPLIT waits)
   const uint16_t* s8;      // int8 row scales
   const uint8_t* W2;       // PH_FFN: column-sliced down projection
   const uint16_t* s8b;     // PH_FFN: its int8 row scales
@@ -213,6 +216,7 @@ __host__ __device__ inline void attn_split(int T, int Hkv, int target, int& CH, 
 struct Params {
   const Phase* prog;   // device program (nullptr: use `single`)
   int nphases;
+  int dtype;           // weight type of the program's GEMV phases (selects the kernel)
   Phase single;
   const int* d_pos;    // current position (nullptr: use pos_const)
   int pos_const;

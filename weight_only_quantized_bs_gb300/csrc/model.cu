@@ -47,7 +47,7 @@ struct gf_kv {
   int* amax_idx = nullptr;
   unsigned* counters = nullptr;  // bars, attention tickets, q/k/v head counters, the argmax ticket
   size_t counter_bytes = 0;
-  unsigned *bars = nullptr, *ticks = nullptr, *headc = nullptr, *amax_tick = nullptr;
+  unsigned *bars = nullptr, *ticks = nullptr, *headc = nullptr, *attd = nullptr, *amax_tick = nullptr;
   gf::Phase* prog = nullptr;
   int nphases = 0;
   int sms = 0;
@@ -251,7 +251,7 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
   const int nbars = nph;
   const size_t nticks = (size_t)L * MAX_M * Hkv;
   const size_t nheadc = (size_t)L * Hkv;
-  kv->counter_bytes = (nbars + nticks + nheadc + 1) * sizeof(unsigned);
+  kv->counter_bytes = (nbars + nticks + 2 * nheadc + 1) * sizeof(unsigned);
   do {
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->kc, cache_elems * 2))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->vc, cache_elems * 2))) break;
@@ -277,7 +277,8 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
   kv->bars = kv->counters;
   kv->ticks = kv->counters + nbars;
   kv->headc = kv->ticks + nticks;
-  kv->amax_tick = kv->headc + nheadc;
+  kv->attd = kv->headc + nheadc;
+  kv->amax_tick = kv->attd + nheadc;
   cudaError_t e = cudaMemset(kv->kc, 0, cache_elems * 2);
   if (e == cudaSuccess) e = cudaMemset(kv->vc, 0, cache_elems * 2);
   if (e == cudaSuccess) e = cudaMemset(kv->counters, 0, kv->counter_bytes);
@@ -291,9 +292,10 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     }
   if (e == cudaSuccess) e = cudaMemcpy(kv->rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice);
 
-  // The program, per dense layer: q/k/v (with RoPE and the KV append) and
-  // attention in one stretch without a grid barrier (each attention unit waits
-  // for its kv group's q/k/v tiles), o, and the FFN; lm_head at the end.
+  // The program, per dense layer: q/k/v (with RoPE and the KV append),
+  // attention and the o projection in one stretch without a grid barrier (each
+  // attention unit waits for its kv group's q/k/v tiles, each o unit for the
+  // attention of its heads), then the FFN; lm_head at the end.
   std::vector<Phase> ph(nph);
   std::vector<char> chained(nph, 0);  // 1: follows its predecessor without a grid barrier
   memset(ph.data(), 0, ph.size() * sizeof(Phase));
@@ -347,15 +349,22 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[1].part = kv->part;
     P[1].tick = kv->ticks + (size_t)l * MAX_M * Hkv;
     P[1].headc = kv->headc + (size_t)l * Hkv;
+    P[1].attd = kv->attd + (size_t)l * Hkv;
     P[1].stream_cur = 0;
     P[1].rot = (int)(cum_units % G);
     chained[ppl * l + 1] = 1;
-    // o projection + residual
+    // o projection split by K-slot, each unit added to the residual
     gemv(P[2], m->o[l]);
+    P[2].kind = PH_OSPLIT;
     P[2].xsrc = X_F32;
     P[2].xptr = kv->attn;
-    P[2].epi = EPI_RESID;
     P[2].out = kv->resid;
+    P[2].attd = kv->attd + (size_t)l * Hkv;
+    P[2].Hq = Hq;
+    P[2].Hkv = Hkv;
+    P[2].hd = hd;
+    cum_units += (long long)((c.d + TR - 1) / TR) * (k_slots(m->wdtype, Hq * hd) - 1);  // units, not tiles
+    chained[ppl * l + 2] = 1;
     if (!E && m->ffn_fused) {
       // gate/up + SwiGLU + down + residual in one phase
       gemv(P[3], m->gu[l]);
@@ -443,7 +452,12 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     P[0].out_mstride = 0;
     P[1] = D[1];  // attention of each row
     P[1].headc = nullptr;
-    P[2] = D[2];  // o
+    P[1].attd = nullptr;
+    gemv(P[2], m->o[l]);  // o, all rows, behind a grid barrier
+    P[2].xsrc = X_F32;
+    P[2].xptr = kv->attn;
+    P[2].epi = EPI_RESID;
+    P[2].out = kv->resid;
     P[2].x_mstride = Hq * hd;
     P[2].out_mstride = c.d;
     if (!E) {
@@ -571,6 +585,7 @@ static int decode_launch(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t
   memset(&p, 0, sizeof p);
   p.prog = kv->prog;
   p.nphases = kv->nphases;
+  p.dtype = m->wdtype;
   p.d_pos = d_pos;
   p.nctas = kv->sms;
   p.unit_target = kv->sms;
@@ -613,6 +628,7 @@ int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t*
   memset(&p, 0, sizeof p);
   p.prog = kv->vprog;
   p.nphases = kv->nvphases;
+  p.dtype = m->wdtype;
   p.d_pos = d_pos;
   p.nctas = kv->sms;
   p.unit_target = kv->sms;
