@@ -115,6 +115,20 @@ int gf_gemv_w8(const void* x, const void* qpacked, const void* s, int N, int K, 
 int gf_gemv_w4g(const void* x, const void* qpacked, int N, int K, int G, void* y, int ydtype,
                 gf_stream stream);
 
+/* gf_gemv_bf16 behind a gate, to exercise the bounded device waits: every
+ * CTA of the launch first waits until the device word *d_gate (read with
+ * acquire semantics) is at least the launch's CTA count (min(ceil(N / 32),
+ * SMs); any value >= 65536 opens the gate), for at most wait_ns
+ * nanoseconds (0 < wait_ns <= 1e10) in place of the library's 2 s limit.
+ * A CTA that gives up records GF_DEVERR_WAIT_GRID in the device error word
+ * (gf_device_error), writes nothing to y, waits for its own copies in flight
+ * and returns; the launch completes and the context stays usable.  With the
+ * gate open the result is that of gf_gemv_bf16.  Nothing in the decode path
+ * calls this; it exists for tests of the wait limits and for callers that
+ * order a GEMV after a device-side event of their own. */
+int gf_gemv_bf16_gated(const void* x, const void* Wpacked, int N, int K, void* y, int ydtype,
+                       const unsigned* d_gate, unsigned long long wait_ns, gf_stream stream);
+
 /* Single-query attention of the decode step (the KV-cache attention the
  * gpt-fast model runs at every generated token): for each of Hq heads,
  * o_h = sum_t p_t v_t over positions t = 0..pos (inclusive), p = softmax of
@@ -138,11 +152,10 @@ int gf_decode_attn(const void* q, const void* kcache, const void* vcache, int Hq
  * library, held by every GPU that loads the library until the process exits.
  * Shapes needing more (Hq * ceil(SMs / Hkv) * (hd + 2) * 4 bytes, plus 4 per kv
  * head rounded up to 256)
- * return GF_EINVAL with the size in gf_last_error().  The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current and keeps it for the life of the process (a cudaDeviceReset
- * would move the array: do not call this again after one); make that first
- * call before any stream capture.  Every call shares the one array: calls
+ * return GF_EINVAL with the size in gf_last_error().  Every call looks up
+ * the array's device address in the current context (cudaGetSymbolAddress, a
+ * host call that allocates nothing), so the address stays right after a
+ * context is re-created.  Every call shares the one array: calls
  * that overlap on the same GPU (for example from two streams at once) race
  * and give wrong results; serialise them.  No cudaMalloc / cudaFree is made. */
 #define GF_NOALLOC_ATTN_SCRATCH (2 << 20)
@@ -246,9 +259,25 @@ int gf_decode_step_traced(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_
 int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t* d_pos,
                 int32_t* d_n_accepted, int32_t* d_next_token, float* d_logits, gf_stream stream);
 
-/* Reads and clears the device error word of the engine (0 = none; otherwise
- * a code naming the wait that gave up, or 7 / 8 for a position / token id
- * that a kernel refused).  Synchronises the device.  The word is shared by
+/* Codes of the device error word: the first failure a launch records. */
+enum {
+  GF_DEVERR_NONE = 0,
+  GF_DEVERR_WAIT_FULL = 1,      /* a consumer warp gave up waiting for a weight slot */
+  GF_DEVERR_WAIT_EMPTY = 2,     /* a producer gave up waiting for a free ring slot */
+  GF_DEVERR_WAIT_GRID = 3,      /* a CTA gave up waiting at a grid barrier or gate */
+  GF_DEVERR_WAIT_CTA = 4,       /* a warp gave up waiting at a CTA barrier */
+  GF_DEVERR_DRAIN = 5,          /* a producer gave up waiting for its last copies */
+  GF_DEVERR_BAD_PROGRAM = 6,    /* a phase the kernel does not run */
+  GF_DEVERR_BAD_POS = 7,        /* *d_pos outside the KV cache */
+  GF_DEVERR_BAD_TOKEN = 8,      /* a token id outside the vocabulary */
+  GF_DEVERR_WAIT_ROUTER = 9,    /* a producer gave up waiting for the expert choice */
+  GF_DEVERR_WAIT_COMBINE = 10,  /* a tile's combine buffer was not handed on in time */
+  GF_DEVERR_WAIT_HEAD = 11      /* a kernel gave up waiting for a head's q/k/v rows or output */
+};
+
+/* Reads and clears the device error word of the engine (GF_DEVERR_NONE, or
+ * the GF_DEVERR_* code of the first wait that gave up or input a kernel
+ * refused).  Synchronises the device.  The word is shared by
  * every call in the process.  The library keeps per-device state (the
  * addresses of its device variables, kernel attributes) for the life of the
  * process: do not use it again on a device after cudaDeviceReset. */

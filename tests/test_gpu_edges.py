@@ -227,3 +227,32 @@ def test_verify_rejects_rows_past_the_cache():
     assert gf.device_error() == 0 and 0 <= int(n_acc.item()) <= 3
     kv.close()
     m.close()
+
+
+# ------------------------------------------------------- bounded waits ----
+def test_gated_gemv_wait_runs_out_and_context_stays_usable():
+    """A grid wait that cannot end: the gated GEMV's CTAs wait for a gate word
+    that nothing sets, with a 1 ms limit in place of 2 s.  Every CTA gives up,
+    the launch completes, the device error word reads GF_DEVERR_WAIT_GRID and
+    nothing was written to y; then the same GEMV behind an open gate, and a
+    plain one, match the oracle on the same context."""
+    N, K = 4096, 4096  # 128 tiles: 128 CTAs, each with 32 slots behind the gate
+    dev = torch.device("cuda")
+    W, x = weights(N, K, 90), xvec(K, 91)
+    Wp = gf.repack_bf16(to_dev(W))
+    xd = to_dev(x)
+    ref = oracle.linear(oracle.BF16, W, None, None, oracle.bf16_to_double(x))
+    gate = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = torch.full((N,), 7.0, dtype=torch.float32, device=dev)
+    assert gf.device_error() == 0
+    gf.gemv_bf16_gated(xd, Wp, N, K, gate, 1_000_000, gf.Y_F32, out=y)
+    assert gf.device_error() == gf.DEVERR_WAIT_GRID
+    assert torch.all(y == 7.0).item()  # nothing past the gate ran
+    # the context is usable: the gate opened, then the ungated call
+    gate.fill_(1 << 20)
+    gf.gemv_bf16_gated(xd, Wp, N, K, gate, 1_000_000_000, gf.Y_F32, out=y)
+    assert gf.device_error() == 0
+    assert rel_err(as_f64(y), ref) <= 1e-4
+    y2 = gf.gemv_bf16(xd, Wp, N, K, gf.Y_F32)
+    assert gf.device_error() == 0
+    assert rel_err(as_f64(y2), ref) <= 1e-4

@@ -3,12 +3,13 @@ oracle on the same seeded inputs, in the launch configuration the benchmark
 times (one persistent launch per decode step on every SM):
 
 * Llama-2-7B-shaped (32 layers), bf16 / int8 / int4-G32: a 6-token
-  teacher-forced sequence, logits within 2e-2 * std at every step, identical
-  argmax outside near-ties;
+  teacher-forced sequence from position 0, and steps at positions 200..203
+  and 2040..2042 after seeded contexts, logits within 2e-2 * std at every
+  step and the oracle's argmax (ties within the measured error allowed);
 * Llama-3.1-8B-shaped (GQA, vocab 128256): one decode step after a context
-  of 8192 (int8) or 1024 (bf16) positions written straight into both KV
-  caches (bf16 N(0, 1) rows; the workload fixes the context length without a
-  prefill run);
+  of 128, 1024 or 8192 positions written straight into both KV caches (bf16
+  N(0, 1) rows; the workload fixes the context length without a prefill
+  run);
 * Mixtral-8x7B per-layer shapes (8 experts of ffn 14336, top-2), 2 of the 32
   layers so that the oracle finishes in about a minute: teacher-forced decode
   and a k = 5 speculative verification against the oracle's own verify.
@@ -22,6 +23,7 @@ import oracle
 from synth import models
 import weight_only_quantized_bs_gb300 as gf
 from weight_only_quantized_bs_gb300.weights import build_model
+from gpu_util import check_steps
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -63,35 +65,37 @@ def _decode(m, kv, cfg, tokens, pos0):
 
 def check_verify(vgot, vref, toks, n_acc, nxt, n_ref, nxt_ref):
     """Logits rows within tolerance; the device's acceptance is the greedy
-    prefix rule applied to its own rows; it equals the oracle's wherever the
-    oracle's top-2 gap on the rows that decide it exceeds twice the tolerance
-    (a random-init model has near-ties that either side may break)."""
+    prefix rule applied to its own rows; its argmax of every row that decides
+    the acceptance is the oracle's, or a tie within that row's measured logit
+    error, and where all of them are the oracle's the acceptance equals the
+    oracle's."""
     a = []
-    clear = True
+    same = True
     for i in range(vref.shape[0]):
+        err = float(np.abs(vgot[i] - vref[i]).max())
         tol = 2e-2 * vref[i].std()
-        assert np.abs(vgot[i] - vref[i]).max() <= tol, (i, np.abs(vgot[i] - vref[i]).max(), tol)
+        assert err <= tol, (i, err, tol)
         a.append(int(np.argmax(vgot[i])))
-        if i <= n_ref:
-            top2 = np.sort(vref[i])[-2:]
-            clear = clear and top2[1] - top2[0] > 2 * tol
+        best = int(np.argmax(vref[i]))
+        if a[i] != best:
+            assert vref[i][a[i]] >= vref[i][best] - 2 * err, i
+            if i <= n_ref:
+                same = False
     n = 0
     while n < len(toks) - 1 and a[n] == toks[n + 1]:
         n += 1
     assert (n_acc, nxt) == (n, a[n])
-    if clear:
+    if same:
         assert (n_acc, nxt) == (n_ref, nxt_ref)
 
 
 def _check(got, ams, ref):
-    for i in range(ref.shape[0]):
-        tol = 2e-2 * ref[i].std()
-        err = np.abs(got[i] - ref[i]).max()
-        assert err <= tol, (i, err, tol)
-        assert ams[i] == int(np.argmax(got[i]))
-        top2 = np.sort(ref[i])[-2:]
-        if top2[1] - top2[0] > 2 * tol:
-            assert ams[i] == int(np.argmax(ref[i])), i
+    """At full size the fp32 logits are ~1e-2 from the fp64 oracle's, and a
+    32000-way random-init argmax sometimes has a top-2 gap below twice that:
+    at most one such tie per run (each within the measured error)."""
+    n = check_steps(got, ams, ref)
+    print("argmax differs from the oracle's at %d of %d steps" % (n, ref.shape[0]))
+    assert n <= 1
 
 
 @pytest.mark.parametrize("dtype", ["int4", "int8", "bf16"])
@@ -108,7 +112,57 @@ def test_llama2_7b_teacher_forced(dtype):
     _check(got, ams, ref)
 
 
-@pytest.mark.parametrize("dtype,ctx", [("int8", 8192), ("bf16", 1024)])
+def _write_rows(kv, cfg, tmax, l, k, v, r0, r1):
+    """Rows [r0, r1) of layer l's K and V caches (bf16 [Hkv][tmax][hd]) from
+    the host arrays k, v ([Hkv][>= r1][hd]), one copy per head."""
+    Hkv, hd = cfg["n_kv_heads"], cfg["head_dim"]
+    kp, vp = kv.cache_ptrs()
+    dev = torch.device("cuda")
+    for src, base in ((k, kp), (v, vp)):
+        t = torch.from_numpy(np.ascontiguousarray(src[:, r0:r1, :]).view(np.int16)).to(dev)
+        for h in range(Hkv):
+            off = ((l * Hkv + h) * tmax + r0) * hd * 2
+            gf.copy_ceiling(t[h], _Raw(base + off), (r1 - r0) * hd * 2)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("dtype", ["int4", "int8", "bf16"])
+def test_llama2_7b_split_kv_positions(dtype):
+    """Llama-2-7B at positions the 200-token decode reaches and near the end
+    of a 2048-row cache, where attention splits across many CTAs: a seeded
+    context of 200 rows in every layer (both caches), 4 teacher-forced steps
+    at 200..203, then rows 204..2039 filled the same way and 3 steps at
+    2040..2042."""
+    cfg = models.config("llama2-7b")
+    wc = models.WeightCache(cfg, seed=34, keep=False)
+    tmax, L = 2048, cfg["n_layers"]
+    om = oracle.OracleModel(cfg, dtype, wc, tmax=tmax, keep=False)
+    m = build_model(cfg, dtype, wc)
+    kv = gf.KV(m, tmax)
+    draws = []
+    for l in range(L):
+        k, v = models.kv_prefill(cfg, 34, l, 2040)
+        draws.append((k, v))
+        om.K[l][:, :200, :] = oracle.bf16_to_double(k[:, :200, :])
+        om.V[l][:, :200, :] = oracle.bf16_to_double(v[:, :200, :])
+        _write_rows(kv, cfg, tmax, l, k, v, 0, 200)
+    toks = list(models.prompt(cfg, 34, 7))
+    ref = om.forward(toks[:4], 200)
+    got, ams = _decode(m, kv, cfg, toks[:4], 200)
+    _check(got, ams, ref)
+    for l, (k, v) in enumerate(draws):
+        om.K[l][:, 204:2040, :] = oracle.bf16_to_double(k[:, 204:2040, :])
+        om.V[l][:, 204:2040, :] = oracle.bf16_to_double(v[:, 204:2040, :])
+        _write_rows(kv, cfg, tmax, l, k, v, 204, 2040)
+    ref = om.forward(toks[4:], 2040)
+    got, ams = _decode(m, kv, cfg, toks[4:], 2040)
+    _check(got, ams, ref)
+    kv.close()
+    m.close()
+
+
+@pytest.mark.parametrize("dtype,ctx", [("int8", 8192), ("bf16", 8192), ("int8", 128), ("bf16", 1024)])
 def test_llama31_8b_long_context(dtype, ctx):
     cfg = models.config("llama3.1-8b")
     wc = models.WeightCache(cfg, seed=32, keep=False)

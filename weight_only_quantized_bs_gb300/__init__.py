@@ -16,6 +16,9 @@ LIB_PATH = os.path.join(HERE, "libgf.so")
 
 W_BF16, W_INT8, W_INT4G32 = 0, 1, 2
 Y_BF16, Y_F32 = 0, 1
+# device error word codes (gf_device_error)
+DEVERR_WAIT_GRID = 3
+DEVERR_BAD_POS, DEVERR_BAD_TOKEN = 7, 8
 TILE_ROWS = 32
 KMAX = 14336
 DTYPE_NAMES = {"bf16": W_BF16, "int8": W_INT8, "int4": W_INT4G32}
@@ -48,6 +51,7 @@ def lib():
             "gf_gemv_bf16": ([vp, vp, i32, i32, vp, i32, vp], i32),
             "gf_gemv_w8": ([vp, vp, vp, i32, i32, vp, i32, vp], i32),
             "gf_gemv_w4g": ([vp, vp, i32, i32, i32, vp, i32, vp], i32),
+            "gf_gemv_bf16_gated": ([vp, vp, i32, i32, vp, i32, vp, ctypes.c_ulonglong, vp], i32),
             "gf_attn_workspace_bytes": ([i32, i32, i32], sz),
             "gf_decode_attn": ([vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, sz, vp], i32),
             "gf_decode_attn_noalloc": ([vp, vp, vp, i32, i32, i32, i32, i32, vp, vp], i32),
@@ -162,6 +166,15 @@ def gemv_w8(x, qp, s, N, K, ydt=Y_BF16, out=None, stream=None):
 def gemv_w4g(x, qp, N, K, ydt=Y_BF16, out=None, G=32, stream=None):
     y = _yout(N, ydt, x.device, out)
     _check(lib().gf_gemv_w4g(_p(x), _p(qp), N, K, G, _p(y), ydt, _s(stream)), "gf_gemv_w4g")
+    return y
+
+
+def gemv_bf16_gated(x, Wp, N, K, gate, wait_ns, ydt=Y_BF16, out=None, stream=None):
+    """gf_gemv_bf16 whose CTAs first wait (at most wait_ns) for the int32
+    device word `gate` to reach the launch's CTA count."""
+    y = _yout(N, ydt, x.device, out)
+    _check(lib().gf_gemv_bf16_gated(_p(x), _p(Wp), N, K, _p(y), ydt, _p(gate), int(wait_ns), _s(stream)),
+           "gf_gemv_bf16_gated")
     return y
 
 

@@ -81,6 +81,14 @@ int gf_copy_ceiling(const void* src, void* dst, size_t bytes, gf_stream stream) 
   return GF_OK;
 }
 
+static_assert(GF_DEVERR_WAIT_FULL == ERR_WAIT_FULL && GF_DEVERR_WAIT_EMPTY == ERR_WAIT_EMPTY &&
+                  GF_DEVERR_WAIT_GRID == ERR_WAIT_GRID && GF_DEVERR_WAIT_CTA == ERR_WAIT_CTA &&
+                  GF_DEVERR_DRAIN == ERR_DRAIN && GF_DEVERR_BAD_PROGRAM == ERR_BAD_PROGRAM &&
+                  GF_DEVERR_BAD_POS == ERR_BAD_POS && GF_DEVERR_BAD_TOKEN == ERR_BAD_TOKEN &&
+                  GF_DEVERR_WAIT_ROUTER == ERR_WAIT_ROUTER && GF_DEVERR_WAIT_COMBINE == ERR_WAIT_COMBINE &&
+                  GF_DEVERR_WAIT_HEAD == ERR_WAIT_HEAD,
+              "public and internal device error codes agree");
+
 int gf_device_error(void) {
   GF_CUDA(cudaDeviceSynchronize());
   int* p = device_err_ptr();

@@ -5,7 +5,6 @@
 // allocator (cudaMalloc / cudaFree can synchronise the device).  Its scratch
 // (the per-chunk softmax partials and the combine tickets) lives in the
 // file-scope array below instead of a caller-provided workspace.
-#include <mutex>
 #include <string.h>
 
 #include "gf_internal.cuh"
@@ -16,23 +15,17 @@ namespace gf {
 static __device__ __align__(256) unsigned char g_attn_scratch[GF_NOALLOC_ATTN_SCRATCH];
 
 // Host code cannot use g_attn_scratch as a device address (in host code the
-// name is a stand-in).  The real address is looked up once per device, with
-// that device current, on the first call made there.
-static void* scratch_addr(int dev) {
-  static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  if (dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_attn_scratch);
-    if (e != cudaSuccess) {
-      set_error("gf_decode_attn_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
-      return nullptr;
-    }
-    addr[dev] = p;
+// name is a stand-in).  The real address is looked up on every call, in the
+// current context: a host call that allocates nothing, and stays right after
+// the context (and with it the module) has been re-created.
+static void* scratch_addr() {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_attn_scratch);
+  if (e != cudaSuccess) {
+    set_error("gf_decode_attn_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+    return nullptr;
   }
-  return addr[dev];
+  return p;
 }
 
 }  // namespace gf
@@ -67,9 +60,7 @@ int gf_decode_attn_noalloc(const void* q, const void* kcache, const void* vcache
               need, Hq, Hkv, hd, GF_NOALLOC_ATTN_SCRATCH);
     return GF_EINVAL;
   }
-  int dev = 0;
-  GF_CUDA(cudaGetDevice(&dev));
-  unsigned char* base = (unsigned char*)scratch_addr(dev);
+  unsigned char* base = (unsigned char*)scratch_addr();
   if (!base) return GF_ECUDA;
   int* err = device_err_ptr();
   if (!err) {

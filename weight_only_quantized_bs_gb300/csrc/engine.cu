@@ -626,28 +626,52 @@ __device__ __forceinline__ bool warp_stageable(const Phase& ph) {
 __device__ void stage_x_warp(const Phase& ph, const Params& P, const Smem& S, Cons& cs, int cta) {
   const int K = ph.K, dt = ph.dtype, G = ph.G, K4 = K / 4, SK4 = slot_k(dt) / 4, nb = k_slots(dt, K);
   const bool norm = ph.xsrc == X_NORM || ph.xsrc == X_EMBED_NORM;
+  const bool f32 = ph.xsrc == X_F32 || ph.xsrc == X_NORM;
   const uint16_t* emb = ph.xsrc == X_EMBED_NORM ? P.embed + (size_t)(*P.token) * K : nullptr;
-  float4* xs4 = reinterpret_cast<float4*>(S.xs);
+  const uint2* src16 = emb ? reinterpret_cast<const uint2*>(emb) : reinterpret_cast<const uint2*>(ph.xptr);
+  const float4* src32 = reinterpret_cast<const float4*>(ph.xptr);
+  const uint2* gain = reinterpret_cast<const uint2*>(ph.gain);
+  // this lane's float4: runs of 32 in the warp's K-slots b0, b0 + NCW, ...
+  const int b0 = (cs.warp - (int)(cs.it % NCW) + NCW) % NCW, per = SK4 / 32;
+  const int n = (nb - b0 + NCW - 1) / NCW * per;
   float ss = 0.f;
-  for (int b = (cs.warp - (int)(cs.it % NCW) + NCW) % NCW; b < nb; b += NCW) {
-    for (int f = b * SK4 + cs.lane; f < (b + 1) * SK4; f += 32) {  // whole warps of consecutive float4
-      const bool in = f < K4;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int BATCH = 4;  // loads in flight per lane before the first is used
+  for (int j0 = 0; j0 < n; j0 += BATCH) {  // warp-uniform trip count
+    float4 a[BATCH];
+    uint2 g[BATCH];
+    int fs[BATCH];
+#pragma unroll
+    for (int q = 0; q < BATCH; ++q) {
+      const int j = j0 + q;
+      fs[q] = ((b0 + (j / per) * NCW) * SK4) + (j % per) * 32 + cs.lane;
+      const bool in = j < n && fs[q] < K4;
+      a[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      g[q] = make_uint2(0u, 0u);
       if (in) {
-        if (ph.xsrc == X_F32 || ph.xsrc == X_NORM) {
-          a = __ldcg(reinterpret_cast<const float4*>(ph.xptr) + f);
+        if (f32) {
+          a[q] = __ldcg(src32 + fs[q]);
         } else {
-          const uint2* src = emb ? reinterpret_cast<const uint2*>(emb) : reinterpret_cast<const uint2*>(ph.xptr);
-          a = bf4(__ldcg(src + f));
+          const uint2 h = __ldcg(src16 + fs[q]);
+          a[q].x = __uint_as_float(h.x);
+          a[q].y = __uint_as_float(h.y);
         }
+        if (norm) g[q] = gain[fs[q]];
       }
+    }
+#pragma unroll
+    for (int q = 0; q < BATCH; ++q) {
+      if (j0 + q >= n) break;  // uniform
+      const int f = fs[q];
+      const bool in = f < K4;
+      float4 v = f32 ? a[q] : bf4(make_uint2(__float_as_uint(a[q].x), __float_as_uint(a[q].y)));
+      if (!in) v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (norm) {
-        ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
-        if (emb && cta == 0 && in) reinterpret_cast<float4*>(P.resid)[f] = a;
-        const float4 g = bf4(in ? reinterpret_cast<const uint2*>(ph.gain)[f] : make_uint2(0u, 0u));
-        a = make_float4(a.x * g.x, a.y * g.y, a.z * g.z, a.w * g.w);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        if (emb && cta == 0 && in) reinterpret_cast<float4*>(P.resid)[f] = v;
+        const float4 gg = bf4(g[q]);
+        v = make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w);
       }
-      stage_store(S, cs, dt, G, f, true, a);
+      stage_store(S, cs, dt, G, f, true, v);
     }
   }
   cs.rnorm = 1.0f;
@@ -2274,7 +2298,8 @@ static Params base_params() {
 }
 
 static int gemv_common(const char* fn, int dt, const void* x, const void* Wp, const void* s8, int N, int K, int G,
-                       void* y, int ydt, cudaStream_t stream) {
+                       void* y, int ydt, cudaStream_t stream, const unsigned* gate = nullptr,
+                       unsigned long long wait_ns = 0) {
   if (!x || !Wp || !y || N <= 0 || K <= 0 || K % per_chunk(dt) || (dt == DT_INT8 && !s8) ||
       (ydt != GF_Y_BF16 && ydt != GF_Y_F32)) {
     set_error("%s: bad arguments (N=%d, K=%d, ydtype=%d)", fn, N, K, ydt);
@@ -2311,6 +2336,11 @@ static int gemv_common(const char* fn, int dt, const void* x, const void* Wp, co
     set_error("%s: cannot resolve the device error word", fn);
     return GF_ECUDA;
   }
+  if (gate) {  // every CTA first waits for the gate word to reach the CTA count
+    ph.wait_bar = 0;
+    p.bars = const_cast<unsigned*>(gate);
+    p.wait_ns = wait_ns;
+  }
   return launch_engine(p, grid, false, stream);
 }
 
@@ -2332,6 +2362,16 @@ int gf_gemv_w4g(const void* x, const void* qpacked, int N, int K, int G, void* y
     return GF_EUNSUPPORTED;
   }
   return gemv_common("gf_gemv_w4g", DT_INT4, x, qpacked, nullptr, N, K, G, y, ydtype, (cudaStream_t)stream);
+}
+
+int gf_gemv_bf16_gated(const void* x, const void* Wpacked, int N, int K, void* y, int ydtype, const unsigned* d_gate,
+                       unsigned long long wait_ns, gf_stream stream) {
+  if (!d_gate || ((uintptr_t)d_gate & 3) || wait_ns == 0 || wait_ns > 10000000000ull) {
+    set_error("gf_gemv_bf16_gated: need a 4-byte aligned gate word and 0 < wait_ns <= 1e10");
+    return GF_EINVAL;
+  }
+  return gemv_common("gf_gemv_bf16_gated", DT_BF16, x, Wpacked, nullptr, N, K, 32, y, ydtype, (cudaStream_t)stream,
+                     d_gate, wait_ns);
 }
 
 size_t gf_attn_workspace_bytes(int Hq, int Hkv, int hd) {
