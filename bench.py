@@ -159,32 +159,72 @@ def measured_peaks():
 
 
 # ------------------------------------------------------ CPU baseline -----
-def oracle_sampler(cfg, dtype, seed, n_layers_sample):
-    """The oracle as it stands, on one host core.  Returns a function timing
-    one sample: a decode token at position 5 through `n_layers_sample` of the
-    model's layers plus the full lm_head; it returns the per-token seconds
-    scaled to all layers and the seconds the sample took.  Building and
-    quantising the sampled layers is not timed."""
-    import numpy as np
-    import oracle
-    from synth import models
-    wc = models.WeightCache(cfg, seed=seed, keep=False)
-    om = oracle.OracleModel(cfg, dtype, wc, tmax=8, keep=True)
-    for l in range(n_layers_sample):
-        om._layer(l)
-    x0 = oracle.bf16_to_double(wc.glob["embed"][[1]])
+class OracleStream:
+    """The oracle as it stands, on one host core, decoding a stream of tokens
+    at positions p0, p0 + 1, ... in stages: stage s of a token is layer s
+    (s < n_layers) or the final RMSNorm + lm_head (s == n_layers), in that
+    order, each on the previous stage's output, so that n_layers + 1
+    consecutive stages are one whole token.  The cache rows 0..p0-1 of every
+    layer hold seeded bf16 N(0, 1) K and V rows (the context the GPU arm has
+    reached at p0).  Building and quantising the layers (`layers_needed` of
+    them, in order) happens before any stage and is not timed."""
 
-    def sample():
-        x = x0
+    def __init__(self, cfg, dtype, seed, p0, layers_needed):
+        import oracle
+        from synth import models
+        self.cfg, self.p0 = cfg, p0
+        self.wc = models.WeightCache(cfg, seed=seed, keep=False)
+        self.om = oracle.OracleModel(cfg, dtype, self.wc, tmax=p0 + 64, keep=True)
+        for l in range(min(layers_needed, cfg["n_layers"])):
+            self.om._layer(l)
+            if p0 > 0:
+                k, v = models.kv_prefill(cfg, seed, l, p0)
+                self.om.K[l][:, :p0, :] = oracle.bf16_to_double(k)
+                self.om.V[l][:, :p0, :] = oracle.bf16_to_double(v)
+        self.tokens = models.prompt(cfg, seed, 64)
+        self.n_stages = cfg["n_layers"] + 1
+        self.i = 0
+        self.x = None
+
+    def stage(self):
+        """Runs the next stage; returns its seconds."""
+        import numpy as np
+        import oracle
+        cfg, om = self.cfg, self.om
+        j, s = divmod(self.i, self.n_stages)
+        pos = self.p0 + j
+        if s == 0:
+            self.x = oracle.bf16_to_double(om.embed[[int(self.tokens[j % len(self.tokens)])]])
         t0 = time.perf_counter()
-        for l in range(n_layers_sample):
-            x = om.layer_forward(l, x, 0)
-        t1 = time.perf_counter()
-        om.lm_head(np.stack([oracle.rmsnorm(x[0], wc.glob["g_final"], cfg["eps"])]))
-        t2 = time.perf_counter()
-        return (t1 - t0) / n_layers_sample * cfg["n_layers"] + (t2 - t1), t2 - t0
+        if s < cfg["n_layers"]:
+            self.x = om.layer_forward(s, self.x, pos)
+        else:
+            om.lm_head(np.stack([oracle.rmsnorm(self.x[0], self.wc.glob["g_final"], cfg["eps"])]))
+        dt = time.perf_counter() - t0
+        self.i += 1
+        return dt
 
-    return sample
+
+def bench_config(args, cfg, tmax, p_first, ctxs):
+    """The `config` object of both arms' JSON line (identical for one command)."""
+    c = {"workload": "%s-shaped greedy decode, %s weights" % (args.workload, args.dtype),
+         "shapes": args.workload, "n_layers": cfg["n_layers"],
+         "weights": args.dtype + ("-g32" if args.dtype == "int4" else ""),
+         "batch": 1, "prompt": 1 if ctxs else N_PROMPT, "tmax": tmax,
+         "positions": [p_first, p_first + args.steps],
+         "parallelism": "replicas" if args.gpus > 1 else "single",
+         "l2": "no flush: every step streams the whole model (GBs), far above the 129 MB L2"}
+    if ctxs:
+        c["contexts"] = ctxs
+    return c
+
+
+def bench_positions(args):
+    """(tmax, first timed position, contexts) of a command line."""
+    ctxs = [int(c) for c in args.ctx.split(",") if c]
+    tmax = 2048 if not ctxs else max(ctxs) + max(args.warmup, N_PROMPT) + args.steps + 8
+    p_first = ctxs[0] + args.warmup if ctxs else max(args.warmup, N_PROMPT)
+    return tmax, p_first, ctxs
 
 
 # ------------------------------------------------- byte accounting -----
@@ -298,10 +338,8 @@ def run_ours(args):
     cfg = models.config(args.workload)
     if args.layers:
         cfg["n_layers"] = args.layers
-    ctxs = [int(c) for c in args.ctx.split(",") if c]
-    tmax = 2048 if not ctxs else max(ctxs) + max(args.warmup, N_PROMPT) + args.steps + 8
-    dtypes = [args.dtype] if args.only_headline else [d for d in ("int4", "int8", "bf16")
-                                                       if args.workload == "llama2-7b" or d != "int4"]
+    tmax, p_first, ctxs = bench_positions(args)
+    dtypes = [args.dtype] if args.only_headline else ["int4", "int8", "bf16"]
     if args.dtype not in dtypes:
         dtypes.insert(0, args.dtype)
 
@@ -423,8 +461,6 @@ def run_ours(args):
     del layers, glob
 
     head = results[args.dtype]
-    # first timed position (the headline context, after the warm-up steps)
-    p_first = ctxs[0] + args.warmup if ctxs else max(args.warmup, N_PROMPT)
     out = {
         "metric": METRIC,
         "value": round(head["tok_s"], 2),
@@ -435,17 +471,14 @@ def run_ours(args):
         "ms_per_step": round(head["ms_per_token"], 4),
         "higher_is_better": True,
         "scaling": "weak",
-        "vs_baseline": (round(head["tok_s"] / world / PUBLISHED_TOKS[(args.workload, args.dtype)], 3)
-                        if (args.workload, args.dtype) in PUBLISHED_TOKS else None),
+        "vs_baseline": None,
+        "vs_published_a100": ({"ratio": round(head["tok_s"] / world / PUBLISHED_TOKS[(args.workload, args.dtype)], 3),
+                               "published_tok_s": PUBLISHED_TOKS[(args.workload, args.dtype)],
+                               "hardware": "1x A100-80GB at 330 W (gpt-fast README, Benchmarks); context only"}
+                              if (args.workload, args.dtype) in PUBLISHED_TOKS else None),
         "dtype": "f32",
         "data": "synthetic (seeded random-init weights, uniform random prompt)",
-        "config": {"workload": "%s-shaped greedy decode, %s weights" % (args.workload, args.dtype),
-                   "shapes": args.workload, "n_layers": cfg["n_layers"], "weights": args.dtype + ("-g32" if args.dtype == "int4" else ""),
-                   "batch": 1, "prompt": 1 if ctxs else N_PROMPT, "tmax": tmax,
-                   "positions": [p_first, p_first + args.steps],
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "no flush: the model's %d MB stream per step is far above L2" %
-                         int(head["weight_bytes"] / 1e6)},
+        "config": bench_config(args, cfg, tmax, p_first, ctxs),
         "achieved_gbs": round(head["gbs"], 1),
         "roofline": {"bound": "hbm", "achieved": round(head["gbs"], 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(head["gbs"] / hbm_peak, 4),
@@ -462,20 +495,22 @@ def run_ours(args):
         "clocks": clocks,
         "setup_s": round(gen_s, 1),
     }
-    if ctxs:
-        out["config"]["contexts"] = ctxs
     if rank == 0 and not args.no_cpu_baseline:
-        sample = oracle_sampler(cfg, args.dtype, args.seed, n_layers_sample=2)
-        ts, spent = [], 0.0
-        while spent < 10.0 and len(ts) < 50:  # about 10 s of CPU work
-            t, dt = sample()
-            ts.append(t)
-            spent += dt
-        per_tok = statistics.median(ts)
-        out["cpu_baseline"] = {"value": round(1.0 / per_tok, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                               "sample": "%d repetitions of one token through 2 of %d layers + full lm_head, "
-                                         "scaled to %d layers (median; %.1f s of CPU)"
-                                         % (len(ts), cfg["n_layers"], cfg["n_layers"], spent)}
+        # the token stream from the first timed position, stage by stage, for
+        # about 20 s of CPU (at most one whole token); only the layers the
+        # sample reaches are built
+        probe = OracleStream(cfg, args.dtype, args.seed, p_first, 1)
+        t1 = probe.stage()
+        n = max(1, min(cfg["n_layers"] + 1, int(20.0 / max(t1, 1e-3))))
+        del probe
+        st = OracleStream(cfg, args.dtype, args.seed, p_first, n)
+        spent = sum(st.stage() for _ in range(n))
+        out["cpu_baseline"] = {"value": round(n / st.n_stages / spent, 5), "unit": "tokens/s", "cores": 1,
+                               "kind": "oracle",
+                               "sample": "%d stages (of %d per token: %d layers + lm_head) of the token stream at "
+                                         "position %d, %.1f s on one core; value = stages / %d per second "
+                                         "(building and quantising the layers untimed)"
+                                         % (n, st.n_stages, cfg["n_layers"], p_first, spent, st.n_stages)}
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
@@ -556,33 +591,38 @@ def run_gemv(args):
 
 # ------------------------------------------------------ reference arm -----
 def run_reference(args):
+    """The oracle (this build's reference implementation) on the host: the
+    same command's workload as a stream of token stages (OracleStream), one
+    stage per step after `warmup` untimed stages.  value = the stages timed /
+    (n_layers + 1) per second: whole-token throughput measured on the stages
+    run (every stage of a token is one layer or the lm_head; a run of fewer
+    than n_layers + 1 steps measures part of a token's work)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import oracle  # noqa: F401  (the oracle is this tier's reference implementation)
     from synth import models
     cfg = models.config(args.workload)
-    sample = oracle_sampler(cfg, args.dtype, args.seed, n_layers_sample=1)
+    if args.layers:
+        cfg["n_layers"] = args.layers
+    tmax, p_first, ctxs = bench_positions(args)
+    st = OracleStream(cfg, args.dtype, args.seed, p_first, args.warmup + args.steps)
     for _ in range(args.warmup):
-        sample()
-    per = [sample()[0] for _ in range(args.steps)]
-    per_tok = statistics.median(per)
-    v = 1.0 / per_tok
+        st.stage()
+    t0 = time.perf_counter()
+    per = [st.stage() for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    v = args.steps / st.n_stages / wall
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "tokens/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_tok * 1e3, 1),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded random-init weights)",
-        "config": {"workload": "%s-shaped greedy decode, %s weights" % (args.workload, args.dtype),
-                   "shapes": args.workload, "n_layers": cfg["n_layers"],
-                   "weights": args.dtype + ("-g32" if args.dtype == "int4" else ""),
-                   "batch": 1, "prompt": N_PROMPT, "tmax": 2048,
-                   "positions": [N_PROMPT if args.warmup <= N_PROMPT else args.warmup,
-                                 max(args.warmup, N_PROMPT) + args.steps],
-                   "parallelism": "single", "l2": "not applicable (the oracle runs on the host)"},
+        "data": "synthetic (seeded random-init weights, uniform random prompt)",
+        "config": bench_config(args, cfg, tmax, p_first, ctxs),
         "cpu_baseline": {"value": round(v, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "each step: one token through 1 of %d layers + full lm_head, scaled "
-                                   "to %d layers (median over the steps)" % (cfg["n_layers"], cfg["n_layers"])},
+                         "sample": "%d stages (of %d per token: %d layers + lm_head) of the token stream "
+                                   "from position %d after %d untimed stages; stage times %.3f-%.3f s"
+                                   % (args.steps, st.n_stages, cfg["n_layers"], p_first, args.warmup,
+                                      min(per), max(per))},
         "e2e": {"value": round(v, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
