@@ -53,6 +53,12 @@ def parse():
                     choices=["llama2-7b", "llama3.1-8b", "mixtral-8x7b", "gemv-set", "gemv"])
     ap.add_argument("--ctx", default="", help="comma-separated context lengths written into the KV cache")
     ap.add_argument("--verify-k", type=int, default=0, help="also time verification passes of k drafts")
+    ap.add_argument("--speculate", type=int, default=0,
+                    help="also time speculative generation with k drafts per round (target --spec-target, "
+                         "draft --spec-draft copies of the same model) against plain greedy generation")
+    ap.add_argument("--spec-target", default="bf16", choices=["int4", "int8", "bf16"])
+    ap.add_argument("--spec-draft", default="int4", choices=["int4", "int8", "bf16"])
+    ap.add_argument("--spec-tokens", type=int, default=100)
     ap.add_argument("--only-headline", action="store_true", help="skip the other two weight dtypes")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
@@ -314,6 +320,42 @@ def measure_verify(gf, m, kv, cfg, prompt, k, rounds, seed, dev):
             "device_error": gf.device_error()}
 
 
+def measure_speculative(gf, cfg, glob, layers, prompt, args):
+    """Speculative generation (gf_generate_speculative: draft = the
+    --spec-draft copy of the same model proposing k tokens per round, target
+    = the --spec-target copy verifying them) against plain greedy generation
+    on the target (gf_generate), --spec-tokens tokens after the 5-token
+    prompt, each call timed end to end on the host (the calls synchronise
+    once per round / at the end) after one untimed call."""
+    import torch
+    k, n = args.speculate, args.spec_tokens
+    tm = gf.Model(cfg, args.spec_target, glob, layers)
+    dm = gf.Model(cfg, args.spec_draft, glob, layers)
+    tmax = N_PROMPT + n + k + 8
+    tkv, dkv = gf.KV(tm, tmax), gf.KV(dm, tmax)
+    p = [int(t) for t in prompt]
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        r = fn()
+        return r, time.perf_counter() - t0
+
+    plain, t_plain = timed(lambda: gf.generate(tm, tkv, p, n))
+    (toks, st), t_spec = timed(lambda: gf.generate_speculative(tm, tkv, dm, dkv, p, n, k))
+    err = gf.device_error()
+    for h in (tkv, dkv, tm, dm):
+        h.close()
+    # both calls include the prompt's N_PROMPT decode steps (and the draft's)
+    return {"k": k, "target": args.spec_target, "draft": args.spec_draft, "tokens": n,
+            "tok_s": round(n / t_spec, 2), "greedy_tok_s": round(n / t_plain, 2),
+            "speedup": round(t_plain / t_spec, 3),
+            "acceptance": round(st["accepted"] / max(st["drafted"], 1), 4), "rounds": st["rounds"],
+            "same_tokens_as_greedy": toks == plain, "device_error": err,
+            "timing": "host wall clock around each whole call (prompt included), after one untimed call"}
+
+
 # ------------------------------------------------------------ our arm -----
 def run_ours(args):
     import numpy as np
@@ -458,8 +500,8 @@ def run_ours(args):
         kv.close()
         m.close()
         torch.cuda.synchronize()
-    del layers, glob
 
+    spec = measure_speculative(gf, cfg, glob, layers, prompt, args) if args.speculate else None
     head = results[args.dtype]
     out = {
         "metric": METRIC,
@@ -495,6 +537,9 @@ def run_ours(args):
         "clocks": clocks,
         "setup_s": round(gen_s, 1),
     }
+    if spec is not None:
+        out["speculative"] = spec
+    del layers, glob
     if rank == 0 and not args.no_cpu_baseline:
         # the token stream from the first timed position, stage by stage, for
         # about 20 s of CPU (at most one whole token); only the layers the

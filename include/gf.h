@@ -259,6 +259,44 @@ int gf_decode_step_traced(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_
 int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t* d_pos,
                 int32_t* d_n_accepted, int32_t* d_next_token, float* d_logits, gf_stream stream);
 
+/* Greedy generation (gpt-fast README, "Generate text", at batch size 1): the
+ * n_prompt host tokens h_prompt are fed one per gf_decode_step from position
+ * 0 of kv (earlier contents are overwritten), then n_new tokens are
+ * generated, each the argmax of the step fed the one before; they are
+ * written to the host array h_out[n_new].  Token ids stay on the device
+ * between steps; the call returns after the last one (the stream is
+ * synchronised).  n_prompt >= 1, n_new >= 1, n_prompt + n_new <= Tmax.
+ * Allocates and frees n_prompt + n_new + 8 ints of device memory. */
+int gf_generate(gf_model* m, gf_kv* kv, const int32_t* h_prompt, int n_prompt, int n_new, int32_t* h_out,
+                gf_stream stream);
+
+/* Counters of a speculative generation: verify passes, draft tokens
+ * proposed (rounds * k), draft tokens the target accepted. */
+typedef struct {
+  int rounds;
+  int drafted;
+  int accepted;
+} gf_spec_stats;
+
+/* Speculative greedy generation (README, "Speculative sampling"; the draft is
+ * the int8 or int4 copy of the target in the README's example): the prompt
+ * is fed to both models as in gf_generate.  Then, per round, from the current
+ * token t at position p: the draft runs k gf_decode_step calls (t and its own
+ * argmaxes at p .. p + k - 1) proposing d_1..d_k; gf_verify_k on the target
+ * checks [t, d_1..d_k] at p .. p + k and accepts the longest prefix d_1..d_n
+ * equal to its own greedy choices, with next token a_n; d_1..d_n and a_n are
+ * emitted, the target's position advances to p + n + 1 and the draft's is
+ * set to the same (after one more draft step over d_k when n = k).  The
+ * emitted tokens equal gf_generate's on the target wherever the verify pass
+ * and the decode step take the same argmax.  h_out receives n_new tokens;
+ * *stats (if not NULL) the counters.  1 <= k <= 7, equal vocabularies,
+ * distinct KV handles, n_prompt + n_new + k + 1 <= both Tmax.  Synchronises
+ * the stream once per round (to read n); returns GF_EDEVICE if a verify pass
+ * reports an impossible count (a device error). */
+int gf_generate_speculative(gf_model* target, gf_kv* tkv, gf_model* draft, gf_kv* dkv, const int32_t* h_prompt,
+                            int n_prompt, int n_new, int k, int32_t* h_out, gf_spec_stats* stats,
+                            gf_stream stream);
+
 /* Codes of the device error word: the first failure a launch records. */
 enum {
   GF_DEVERR_NONE = 0,

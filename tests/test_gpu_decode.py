@@ -125,3 +125,13 @@ def test_kv_reset_then_decode_from_position_zero(dtype):
     assert check(np.stack(got), np.array(got_am), ref) == 0
     kv.close()
     m.close()
+
+
+@pytest.mark.parametrize("G", [64, 128])
+def test_decode_int4_group_sizes(G):
+    """int4 with groups of 64 and 128 along K through the whole decode step
+    (the fused FFN's column-sliced down copy takes each 16-wide slice's scale
+    and zero from its group)."""
+    cfg = models.config("tiny", ffn=384, group=G)
+    got, am, ref = run_teacher_forced(cfg, "int4", seed=17, n_prompt=5, n_gen=30, tmax=64)
+    assert check(got, am, ref) == 0

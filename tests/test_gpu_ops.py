@@ -54,6 +54,36 @@ def test_quantize_w4g_bit_exact(N, K):
     assert np.array_equal(bf16_host(s), s_ref) and np.array_equal(bf16_host(z), z_ref)
 
 
+# int4 group sizes other than 32 (K a multiple of G): ragged N, several
+# tiles, the 4096 x 4096 GEMV and the 11008-wide down projection
+SHAPES_G = [(45, 1152), (7, 3200), (100, 512), (4096, 4096), (128, 11008)]
+
+
+@pytest.mark.parametrize("G", [64, 128])
+@pytest.mark.parametrize("N,K", SHAPES_G)
+def test_quantize_w4g_group_sizes_bit_exact(G, N, K):
+    W = weights(N, K, 14)
+    W[0, :G] = W[0, 5]                      # a degenerate group
+    packed = gf.quantize_w4g(to_dev(W), G=G)
+    q_ref, s_ref, z_ref = oracle.quant_w4g(W, G)
+    assert s_ref.shape == (N, K // G)
+    assert np.array_equal(packed.cpu().numpy(), oracle.pack(oracle.INT4, N, K, q_ref, s_ref, z_ref, G=G))
+    q, s, z = gf.unpack_w4g(packed, N, K, G=G)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(bf16_host(s), s_ref) and np.array_equal(bf16_host(z), z_ref)
+
+
+@pytest.mark.parametrize("G", [64, 128])
+@pytest.mark.parametrize("N,K", SHAPES_G + [(12288, 4096), (4096, 14336)])
+def test_gemv_w4g_group_sizes(G, N, K):
+    W, x = weights(N, K, 15), xvec(K, 32)
+    qp = gf.quantize_w4g(to_dev(W), G=G)
+    y = as_f64(gf.gemv_w4g(to_dev(x), qp, N, K, gf.Y_F32, G=G))
+    q, sr, zr = oracle.quant_w4g(W, G)
+    ref = oracle.linear(oracle.INT4, q, sr, zr, oracle.bf16_to_double(x))
+    assert rel_err(y, ref) <= 1e-4
+
+
 @pytest.mark.parametrize("N,K", SHAPES_SMALL + [(4096, 4096)])
 def test_repack_bf16_bit_exact(N, K):
     W = weights(N, K, 13)

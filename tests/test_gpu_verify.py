@@ -97,3 +97,35 @@ def test_verify_k0_is_a_decode_step():
     assert int(n_acc.item()) == 0 and int(nxt.item()) == gen[0] and int(pos.item()) == len(prompt)
     kv.close()
     m.close()
+
+
+@pytest.mark.parametrize("name,target,draft,k", [("tiny", "bf16", "int4", 4), ("small", "int8", "int4", 3),
+                                                 ("tiny", "int8", "int8", 7)])
+def test_speculative_generation_equals_greedy(name, target, draft, k):
+    """gf_generate_speculative (a draft copy of the same seeded model in
+    another weight type proposes k tokens, the target verifies) emits exactly
+    the oracle's plain greedy decode of the target over 40 tokens, and so
+    does gf_generate on the target; with the draft equal to the target's own
+    weights almost every draft is accepted."""
+    cfg = models.config(name)
+    wc = models.WeightCache(cfg, seed=24)
+    prompt = [int(t) for t in models.prompt(cfg, 24, 5)]
+    n_new = 40
+    ref, _ = oracle.OracleModel(cfg, target, wc, tmax=64).greedy(prompt, n_new)
+    tm = build_model(cfg, target, wc)
+    dm = build_model(cfg, draft, wc)
+    tkv, dkv = gf.KV(tm, 64), gf.KV(dm, 64)
+    plain = gf.generate(tm, tkv, prompt, n_new)
+    assert plain == [int(t) for t in ref]
+    spec, st = gf.generate_speculative(tm, tkv, dm, dkv, prompt, n_new, k)
+    assert spec == [int(t) for t in ref]
+    assert st["drafted"] == st["rounds"] * k and 0 <= st["accepted"] <= st["drafted"]
+    # every round emits accepted + 1 tokens (the first also the prompt's next)
+    assert st["accepted"] + st["rounds"] + 1 >= n_new
+    if draft == target:
+        assert st["accepted"] >= 0.9 * st["drafted"]
+    for h in (tkv, dkv):
+        h.close()
+    tm.close()
+    dm.close()
+    assert gf.device_error() == 0

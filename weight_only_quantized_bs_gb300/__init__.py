@@ -61,6 +61,8 @@ def lib():
             "gf_kv_create": ([vp, i32, vp], i32),
             "gf_kv_destroy": ([vp], i32),
             "gf_kv_reset": ([vp, vp], i32),
+            "gf_generate": ([vp, vp, vp, i32, i32, vp, vp], i32),
+            "gf_generate_speculative": ([vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp], i32),
             "gf_kv_cache_ptrs": ([vp, vp, vp], i32),
             "gf_decode_step": ([vp, vp, vp, vp, vp, vp, vp], i32),
             "gf_verify_k": ([vp, vp, vp, i32, vp, vp, vp, vp, vp], i32),
@@ -323,3 +325,32 @@ def decode_step_traced(model, kv, d_token, d_pos, d_logits, d_argmax, d_trace, s
 def verify_k(model, kv, d_tokens, k, d_pos, d_n, d_next, d_logits=None, stream=None):
     _check(lib().gf_verify_k(model.h, kv.h, _p(d_tokens), k, _p(d_pos), _p(d_n), _p(d_next), _p(d_logits),
                              _s(stream)), "gf_verify_k")
+
+
+# -------------------------------------------------------- generation ------
+class SpecStats(ctypes.Structure):
+    _fields_ = [("rounds", ctypes.c_int), ("drafted", ctypes.c_int), ("accepted", ctypes.c_int)]
+
+
+def _host_ints(seq):
+    arr = (ctypes.c_int32 * len(seq))(*[int(t) for t in seq])
+    return arr
+
+
+def generate(model, kv, prompt, n_new, stream=None):
+    """Greedy generation through gf_generate: returns the n_new token ids."""
+    hp = _host_ints(prompt)
+    out = (ctypes.c_int32 * n_new)()
+    _check(lib().gf_generate(model.h, kv.h, hp, len(prompt), n_new, out, _s(stream)), "gf_generate")
+    return list(out)
+
+
+def generate_speculative(target, tkv, draft, dkv, prompt, n_new, k, stream=None):
+    """Speculative greedy generation through gf_generate_speculative: returns
+    (the n_new token ids, {rounds, drafted, accepted})."""
+    hp = _host_ints(prompt)
+    out = (ctypes.c_int32 * n_new)()
+    st = SpecStats()
+    _check(lib().gf_generate_speculative(target.h, tkv.h, draft.h, dkv.h, hp, len(prompt), n_new, k, out,
+                                         ctypes.byref(st), _s(stream)), "gf_generate_speculative")
+    return list(out), {"rounds": st.rounds, "drafted": st.drafted, "accepted": st.accepted}

@@ -656,3 +656,128 @@ int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t*
 }
 
 }  // extern "C"
+
+// ============================================================ generation ===
+// Host loops over the decode and verify launches: plain greedy generation
+// (gpt-fast README, "Generate text": a prompt, then greedy tokens at batch
+// size 1) and speculative generation (README, "Speculative sampling": a draft
+// model -- the int8 or int4 copy of the target -- proposes k tokens, the
+// target checks them in one pass and keeps the longest prefix equal to its
+// own greedy choices plus its next token).  The loops only order launches,
+// copy token ids and positions, and count; every step of the arithmetic runs
+// in the engine.
+namespace {
+
+struct DevInts {  // one small device array, freed on scope exit
+  int32_t* p = nullptr;
+  ~DevInts() {
+    if (p) cudaFree(p);
+  }
+};
+
+// Feeds the prompt one token per step from position 0; the argmax of the
+// last step is written to *d_first (the first generated token), the other
+// steps' to *d_junk.
+int feed_prompt(gf_model* m, gf_kv* kv, const int32_t* d_prompt, int n, int32_t* d_pos, int32_t* d_first,
+                int32_t* d_junk, cudaStream_t s) {
+  GF_CUDA(cudaMemsetAsync(d_pos, 0, sizeof(int32_t), s));
+  for (int i = 0; i < n; ++i) {
+    const int rc = decode_launch(m, kv, d_prompt + i, d_pos, kv->vlogits, i == n - 1 ? d_first : d_junk, nullptr, s);
+    if (rc) return rc;
+  }
+  return GF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gf_generate(gf_model* m, gf_kv* kv, const int32_t* h_prompt, int n_prompt, int n_new, int32_t* h_out,
+                gf_stream stream) {
+  if (!m || !kv || kv->m != m || !h_prompt || !h_out || n_prompt < 1 || n_new < 1 ||
+      (long long)n_prompt + n_new > kv->Tmax) {
+    set_error("gf_generate: bad arguments (n_prompt=%d, n_new=%d, Tmax=%d)", n_prompt, n_new, kv ? kv->Tmax : 0);
+    return GF_EINVAL;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  // [0] position, [1] junk argmax, [8..) the prompt then the generated tokens
+  DevInts d;
+  const size_t nints = 8 + (size_t)n_prompt + n_new;
+  GF_CUDA(cudaMalloc(&d.p, nints * sizeof(int32_t)));
+  int32_t* seq = d.p + 8;
+  GF_CUDA(cudaMemcpyAsync(seq, h_prompt, (size_t)n_prompt * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  int rc = feed_prompt(m, kv, seq, n_prompt, d.p, seq + n_prompt, d.p + 1, s);
+  if (rc) return rc;
+  // generated token j (j >= 1) is the argmax of the step fed token j - 1
+  for (int j = 1; j < n_new; ++j) {
+    int32_t* in = seq + n_prompt + j - 1;
+    if ((rc = decode_launch(m, kv, in, d.p, kv->vlogits, in + 1, nullptr, s))) return rc;
+  }
+  GF_CUDA(cudaMemcpyAsync(h_out, seq + n_prompt, (size_t)n_new * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  GF_CUDA(cudaStreamSynchronize(s));
+  return GF_OK;
+}
+
+int gf_generate_speculative(gf_model* target, gf_kv* tkv, gf_model* draft, gf_kv* dkv, const int32_t* h_prompt,
+                            int n_prompt, int n_new, int k, int32_t* h_out, gf_spec_stats* stats,
+                            gf_stream stream) {
+  if (!target || !tkv || tkv->m != target || !draft || !dkv || dkv->m != draft || tkv == dkv || !h_prompt ||
+      !h_out || n_prompt < 1 || n_new < 1 || k < 1 || k + 1 > MAX_M ||
+      target->cfg.vocab != draft->cfg.vocab ||
+      (long long)n_prompt + n_new + k + 1 > (tkv->Tmax < dkv->Tmax ? tkv->Tmax : dkv->Tmax)) {
+    set_error("gf_generate_speculative: bad arguments (k must be 1..%d, the vocabularies equal, "
+              "n_prompt + n_new + k + 1 <= both Tmax)", MAX_M - 1);
+    return GF_EINVAL;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  // [0] target position, [1] draft position, [2] accepted, [3] next token,
+  // [4] junk argmax, [8..8+k] the verify rows (current token, k drafts),
+  // [16..) the prompt
+  DevInts d;
+  GF_CUDA(cudaMalloc(&d.p, (16 + (size_t)n_prompt) * sizeof(int32_t)));
+  int32_t *pos_t = d.p, *pos_d = d.p + 1, *n_acc = d.p + 2, *nxt = d.p + 3, *junk = d.p + 4, *rows = d.p + 8;
+  int32_t* prompt = d.p + 16;
+  GF_CUDA(cudaMemcpyAsync(prompt, h_prompt, (size_t)n_prompt * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  int rc = feed_prompt(target, tkv, prompt, n_prompt, pos_t, rows, junk, s);
+  if (!rc) rc = feed_prompt(draft, dkv, prompt, n_prompt, pos_d, junk, junk, s);
+  if (rc) return rc;
+  gf_spec_stats st = {0, 0, 0};
+  int emitted = 0, p = n_prompt;  // rows[0] is the token at position p
+  int32_t h[16];
+  while (emitted < n_new) {
+    // the draft proposes rows[1..k] from rows[0], positions p .. p + k - 1
+    for (int j = 0; j < k; ++j)
+      if ((rc = decode_launch(draft, dkv, rows + j, pos_d, dkv->vlogits, rows + j + 1, nullptr, s))) return rc;
+    // the target checks rows[0..k] at positions p .. p + k in one pass
+    if ((rc = gf_verify_k(target, tkv, rows, k, pos_t, n_acc, nxt, nullptr, s))) return rc;
+    GF_CUDA(cudaMemcpyAsync(h, d.p, 16 * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    GF_CUDA(cudaStreamSynchronize(s));
+    const int n = h[2];
+    if (n < 0 || n > k || h[0] != p + n + 1) {
+      set_error("gf_generate_speculative: the verify pass returned n=%d at position %d (device error %d)", n,
+                h[0], gf_device_error());
+      return GF_EDEVICE;
+    }
+    if (st.rounds == 0) h_out[emitted++] = h[8];  // the target's token after the prompt
+    for (int j = 1; j <= n && emitted < n_new; ++j) h_out[emitted++] = h[8 + j];
+    if (emitted < n_new) h_out[emitted++] = h[3];
+    ++st.rounds;
+    st.drafted += k;
+    st.accepted += n;
+    // the draft's cache must hold rows[0..n] at p .. p + n: with all k
+    // accepted it has not yet seen rows[k]; otherwise step back
+    if (n == k) {
+      if ((rc = decode_launch(draft, dkv, rows + k, pos_d, dkv->vlogits, junk, nullptr, s))) return rc;
+    } else {
+      const int32_t back = p + n + 1;
+      GF_CUDA(cudaMemcpyAsync(pos_d, &back, sizeof back, cudaMemcpyHostToDevice, s));
+    }
+    GF_CUDA(cudaMemcpyAsync(rows, nxt, sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+    p += n + 1;
+  }
+  GF_CUDA(cudaStreamSynchronize(s));
+  if (stats) *stats = st;
+  return GF_OK;
+}
+
+}  // extern "C"
