@@ -1,26 +1,28 @@
 // engine.cu — the persistent phase engine of libgf (sm_103a).
 //
-// One CTA per SM runs a program of phases (a single GEMV or attention for the
-// standalone calls; every layer of a decode step for gf_decode_step).  In
-// each CTA one producer thread streams the CTA's weight slots and KV-cache
-// rows from HBM into a ring of 16 shared-memory slots, running ahead across
-// phase boundaries because the weight stream does not depend on activations.
-// A weight slot is 32 rows x 256 bytes of each row (plus, for int4, the
-// rows' scale/zero words), stored contiguously in the swizzled layout of
-// gf_internal.cuh and moved by one bulk asynchronous copy (the tensor-memory
-// accelerator's linear mode); a KV slot is 16 positions of K and of V, one
-// bulk copy each.  Completion is counted on an mbarrier per slot, and the
-// loads carry an L2 evict-first hint.  Slot X belongs to consumer warp
-// X mod 8 (two ring entries per warp), whose lane r owns row r of the slot:
-// it dequantises the int8 / int4 codes of its row in registers against the
-// fp32 input vector staged in shared memory (a broadcast read, the same for
-// all lanes) and keeps its row's partial sum, so that no cross-lane reduction
-// is needed.  A tile's partial sums from the warps that held its K-slots meet
-// in shared memory, where the last warp to arrive adds them in K order and
-// runs the epilogue.  Dependent phases are separated by grid barriers
-// (cooperative launch) or by per-head completion counters; every wait in the
-// kernel is bounded by a clock (2 s by default), after which the kernel
-// records an error code, drains its own copies in flight and returns.
+// One CTA per SM (8 consumer warps, 4 producer warps) runs a program of
+// phases: a single GEMV or attention for the standalone calls; every layer of
+// a decode step, or of a k-draft verification, for gf_decode_step /
+// gf_verify_k.  Lane 0 of each producer warp streams every fourth of the
+// CTA's weight slots and KV-cache slots from HBM into a ring of 16
+// shared-memory entries, running ahead across phase boundaries because the
+// weight stream does not depend on activations.  A weight slot is 32 rows x
+// 256 code bytes of each row (plus, for int4, the rows' scale/zero words),
+// stored contiguously in the swizzled layout of gf_internal.cuh and moved by
+// one bulk asynchronous copy (cp.async.bulk, the copy engine's linear mode)
+// with an L2 evict-first hint; a KV slot is up to 16 positions of K and of V.
+// Completion is counted on an mbarrier per entry.  Slot X of the stream
+// belongs to consumer warp X mod 8 (two ring entries per warp).  The warp's
+// lanes are 8 row lanes x 4 K quarters: each lane dequantises the int8 /
+// int4 codes of four rows over a quarter of the slot's K range in registers
+// against the fp32 input staged in shared memory, and the quarters meet in
+// two shuffles.  A tile's partial sums from the warps that held its K-slots
+// meet in shared memory, where the last warp to arrive adds them in K order
+// and runs the epilogue.  Dependent phases are separated by grid barriers
+// (cooperative launch) or by per-head completion counters (q/k/v rows ->
+// attention -> o projection); every wait in the kernel is bounded by a clock
+// (2 s by default), after which the kernel records an error code, drains its
+// own copies in flight and returns.
 //
 // The decode step computed here is the batch-size-1 autoregressive step of
 // the gpt-fast README ("Benchmarks", "Quantization"): RMSNorm, q/k/v, RoPE,
@@ -212,9 +214,11 @@ __device__ __forceinline__ Smem smem_layout(uint8_t* raw) {
   s.empty = s.full + NSLOT;
   s.cbar = s.empty + NSLOT;
   s.red = reinterpret_cast<float*>(base + OFF_MISC);
-  s.bcast = reinterpret_cast<int*>(base + OFF_MISC + 256);
-  s.moew = reinterpret_cast<float*>(base + OFF_MISC + 512);
-  s.ffnc = reinterpret_cast<int*>(base + OFF_MISC + 768);
+  s.bcast = reinterpret_cast<int*>(base + OFF_MISC + 512);
+  s.moew = reinterpret_cast<float*>(base + OFF_MISC + 1280);
+  s.ffnc = reinterpret_cast<int*>(base + OFF_MISC + 1536);
+  static_assert(NCW * MAX_M <= 128 && 64 + NCW * MAX_M <= 192 && 1536 + 2 * FFN_HN * 4 <= MISC_BYTES,
+                "misc shared-memory areas");
   s.phb = reinterpret_cast<Phase*>(base + OFF_PHB);
   return s;
 }
@@ -306,7 +310,8 @@ __device__ __forceinline__ int group_end(const TileGroups& tg, int i0) {
 // stream; producer p issues the slots X with X % NPROD == p, which use the
 // ring entries of that residue only.  One thread can issue a bulk copy only
 // every few hundred nanoseconds, which alone would cap the stream below the
-// HBM rate; two issue in parallel.
+// HBM rate; four issue in parallel (measured: the bf16 step, which waits on
+// its copies, runs about 5 % faster with four than with two).
 struct Prod {
   uint32_t it;
   uint64_t pol;
@@ -1964,15 +1969,15 @@ __device__ bool verify_finish(const Params& P, const Smem& S, Cons& cs, int cta,
       amax_merge(a, v, i);
     }
     if (cs.lane == 0) {
-      S.red[cs.warp * 8 + m] = a.v;  // red has 64 floats: warps x rows <= 8 x 8
-      S.bcast[cs.warp * 8 + m] = a.i;
+      S.red[cs.warp * MAX_M + m] = a.v;
+      S.bcast[64 + cs.warp * MAX_M + m] = a.i;
     }
   }
   if (!cta_sync(S, cs, P.err)) return false;
   if (cs.ctid == 0) {
     for (int m = 0; m < P.M; ++m) {
-      ArgMax b = {S.red[m], S.bcast[m]};
-      for (int w = 1; w < NCW; ++w) amax_merge(b, S.red[w * 8 + m], S.bcast[w * 8 + m]);
+      ArgMax b = {S.red[m], S.bcast[64 + m]};
+      for (int w = 1; w < NCW; ++w) amax_merge(b, S.red[w * MAX_M + m], S.bcast[64 + w * MAX_M + m]);
       P.amax_val[cta * MAX_M + m] = b.v;
       P.amax_idx[cta * MAX_M + m] = b.i;
     }

@@ -53,7 +53,7 @@ __host__ __device__ inline long long sz_addr(int K, int G, int n, int g) {
 
 // ------------------------------------------------------- engine sizes ----
 constexpr int NCW = 8;                       // consumer warps per CTA
-constexpr int NPROD = 2;                     // producer warps (lane 0 of each issues copies)
+constexpr int NPROD = 4;                     // producer warps (lane 0 of each issues copies)
 constexpr int NTHREADS = (NCW + NPROD) * 32;
 constexpr int SLOT_BYTES = 10240;            // ring entry: a slot of any type
 // Slot X of the CTA's stream (counted over the whole program) belongs to
@@ -71,7 +71,10 @@ constexpr int OFF_TB = OFF_XSUM + (KMAX / 16) * 4;       // [NTB][NCW][TR] parti
 constexpr int OFF_TBC = OFF_TB + NTB * NCW * TR * 4;     // [NTB] arrival counters, then [NTB] guards
 constexpr int OFF_BAR = OFF_TBC + 2 * NTB * 4;           // mbarriers
 constexpr int OFF_MISC = OFF_BAR + (2 * NSLOT + 2) * 8;
-constexpr int OFF_PHB = OFF_MISC + 1024;  // red[64] f32, bcast[64] i32, moew[64] f32, spare
+// red[128] f32, bcast[192] i32 (fixed slots below 64, the verify argmax
+// merge from 64), moew[64] f32, FFN counters [16] i32
+constexpr int MISC_BYTES = 2048;
+constexpr int OFF_PHB = OFF_MISC + MISC_BYTES;
 constexpr int PHB_BYTES = 256;            // one phase descriptor (two buffers)
 constexpr int SMEM_USED = OFF_PHB + 2 * PHB_BYTES;
 constexpr int SMEM_BYTES = SMEM_USED + 128;  // + slack to align the base to 128
