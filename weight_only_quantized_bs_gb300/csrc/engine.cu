@@ -1644,20 +1644,27 @@ __device__ __noinline__ AttnRet attn_call(const Phase& ph, const Params& P, cons
 // and multiplies them with the M rows, and adds its rows' M sums into a
 // shared accumulator (each (row, m) has one writer per K-slot, K-slots in
 // order: deterministic); the group's epilogues then run per (row, m).
+// A multi-row GEMV stages its M input rows VKB K values at a time (one
+// staging round covers VKB / slot_k K-slots: 2 int4, 4 int8, 8 bf16), so
+// that every round keeps all consumer warps busy and the rounds' staging
+// latency and barriers are paid K / VKB times per tile group.
+constexpr int VKB = 1024;
 struct VS {
-  float* xk;    // [MAX_M][512] inputs of the current K-slot (256 used)
-  float* xgk;   // [MAX_M][32] sums of the inputs per int4 group / int8 chunk, as S.xsum
+  float* xk;    // [MAX_M][VKB] inputs of the current round
+  float* xgk;   // [MAX_M][64] sums of the inputs per int4 group / int8 chunk, as S.xsum
   float* acc;   // [VTG * TR][MAX_M] row sums of the tile group
   float* rfac;  // [MAX_M] RMSNorm factors
 };
 __device__ __forceinline__ VS vsmem(const Smem& S) {
   VS v;
   v.xk = S.xs;
-  v.xgk = v.xk + MAX_M * 512;
-  v.acc = v.xgk + MAX_M * 32;
+  v.xgk = v.xk + MAX_M * VKB;
+  v.acc = v.xgk + MAX_M * 64;
   v.rfac = v.acc + VTG * TR * MAX_M;
   return v;
 }
+static_assert(MAX_M * VKB + MAX_M * 64 + VTG * TR * MAX_M + MAX_M <= KMAX, "verify staging area");
+static_assert(VKB / 32 <= 64 && VKB / 16 <= 64, "verify group sums per row");
 
 // Row m of the phase's input, element k: the source a decode step would read.
 __device__ __forceinline__ float4 vin4(const Phase& ph, const Params& P, const VS& V, int m, int e, int k4) {
@@ -1823,26 +1830,30 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
   for (int i0 = 0; tg.first + i0 * tg.G < tg.ntiles;) {
     const int i1 = group_end(tg, i0);
     const int seg = (tg.first + i0 * tg.G) / tg.tps, e = eseg[seg];
-    for (int b = 0; b < nb; ++b) {
-      // stage the K-slot's inputs of the M rows, zero past K (whole warps of
-      // consecutive float4, so that group sums shuffle within a warp)
-      const int per_m = SK / 4;  // float4 per row
-      for (int q0 = 0; q0 < M * per_m; q0 += NCW * 32) {
-        const int q = q0 + cs.ctid, m = q / per_m, f4 = q % per_m;
-        const bool st = m < M, ok = st && b * per_m + f4 < K / 4;
+    constexpr int KR = VKB / SK, PM = VKB / 4;  // K-slots and float4 per row of a round
+    for (int b0 = 0; b0 < nb; b0 += KR) {
+      const int b1 = min(nb, b0 + KR);
+      // stage the round's inputs of the M rows, zero past K (one row per
+      // iteration, whole warps of consecutive float4, so that group sums
+      // shuffle within a warp)
+      for (int q0 = 0; q0 < M * PM; q0 += NCW * 32) {
+        const int q = q0 + cs.ctid, m = q / PM, f4 = q % PM;
+        const bool st = m < M, ok = st && b0 * (SK / 4) + f4 < K / 4;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ok) a = vin4(ph, P, V, m, e, b * per_m + f4);
+        if (ok) a = vin4(ph, P, V, m, e, b0 * (SK / 4) + f4);
         const float4 mu = dq_mult(DT, f4 & 7);
-        if (st) reinterpret_cast<float4*>(V.xk)[m * per_m + f4] = make_float4(a.x * mu.x, a.y * mu.y, a.z * mu.z, a.w * mu.w);
+        if (st) reinterpret_cast<float4*>(V.xk)[m * PM + f4] = make_float4(a.x * mu.x, a.y * mu.y, a.z * mu.z, a.w * mu.w);
         if (DT != DT_BF16) {  // group / chunk sums as in stage_store
           float sg = a.x + a.y + a.z + a.w;
           const int span = DT == DT_INT4 ? Gq / 4 : 4;
           for (int o = 1; o < span; o <<= 1) sg += __shfl_xor_sync(0xffffffffu, sg, o);
           if (st && (lane & (span - 1)) == 0)
-            V.xgk[m * 32 + (4 * f4) / (DT == DT_INT4 ? Gq : 16)] = sg * (DT == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
+            V.xgk[m * 64 + (4 * f4) / (DT == DT_INT4 ? Gq : 16)] = sg * (DT == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
         }
       }
       if (!cta_sync(S, cs, P.err)) return false;
+      for (int b = b0; b < b1; ++b) {
+      const int kb = (b - b0) * SK;  // the K-slot's first input within the round
       for (int i = i0; i < i1; ++i, ++j) {
         const uint32_t it = cs.it + j;
         if ((int)(it % NCW) != w) continue;
@@ -1870,7 +1881,7 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
 #pragma unroll
               for (int m = 0; m < MAX_M; ++m) {
                 if (m < M) {
-                  const float4* xm = xk4 + m * (SK / 4) + u * 8 + 2 * jw;
+                  const float4* xm = xk4 + m * PM + kb / 4 + u * 8 + 2 * jw;
                   const float4 xa = xm[0], xb = xm[1];
                   a[m] = ffma2(c0, lo2(xa), a[m]);
                   a[m] = ffma2(c1, hi2(xa), a[m]);
@@ -1884,7 +1895,7 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
 #pragma unroll
               for (int m = 0; m < MAX_M; ++m) {
                 if (m < M) {
-                  const float4 xa = xk4[m * (SK / 4) + u * 4 + jw];
+                  const float4 xa = xk4[m * PM + kb / 4 + u * 4 + jw];
                   a[m] = ffma2(c0, lo2(xa), a[m]);
                   a[m] = ffma2(c1, hi2(xa), a[m]);
                 }
@@ -1894,7 +1905,7 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
 #pragma unroll
               for (int m = 0; m < MAX_M; ++m) {
                 if (m < M) {
-                  const float4 xa = xk4[m * (SK / 4) + u * 2 + (jw >> 1)];
+                  const float4 xa = xk4[m * PM + kb / 4 + u * 2 + (jw >> 1)];
                   a[m] = ffma2(c0, (jw & 1) ? hi2(xa) : lo2(xa), a[m]);
                 }
               }
@@ -1907,21 +1918,23 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
 #pragma unroll
               for (int m = 0; m < MAX_M; ++m) {
                 v[m] = fmaf(__uint_as_float(sz << 16), a[m].x + a[m].y,
-                            fmaf(__uint_as_float(sz & 0xFFFF0000u), V.xgk[m * 32 + gi], v[m]));
+                            fmaf(__uint_as_float(sz & 0xFFFF0000u), V.xgk[m * 64 + kb / Gq + gi], v[m]));
                 a[m] = make_float2(0.f, 0.f);
               }
             }
           } else if (DT == DT_INT8) {
 #pragma unroll
-            for (int m = 0; m < MAX_M; ++m) v[m] -= V.xgk[m * 32 + u];
+            for (int m = 0; m < MAX_M; ++m) v[m] -= V.xgk[m * 64 + kb / 16 + u];
           }
         }
         slot_release(S, cs, it);
+        // several warps hold K-slots of the same tile in one round
         float* accr = V.acc + ((i - i0) * TR + lane) * MAX_M;
 #pragma unroll
         for (int m = 0; m < MAX_M; ++m) {
-          if (m < M) accr[m] += DT == DT_INT4 ? v[m] : (a[m].x + a[m].y) + v[m];
+          if (m < M) atomicAdd(accr + m, DT == DT_INT4 ? v[m] : (a[m].x + a[m].y) + v[m]);
         }
+      }
       }
       if (!cta_sync(S, cs, P.err)) return false;
     }
