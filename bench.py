@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--spec-target", default="bf16", choices=["int4", "int8", "bf16"])
     ap.add_argument("--spec-draft", default="int4", choices=["int4", "int8", "bf16"])
     ap.add_argument("--spec-tokens", type=int, default=100)
+    ap.add_argument("--prefill", action="store_true",
+                    help="also time the 5-token prompt as one gf_prefill pass against 5 decode steps")
     ap.add_argument("--only-headline", action="store_true", help="skip the other two weight dtypes")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
@@ -356,6 +358,49 @@ def measure_speculative(gf, cfg, glob, layers, prompt, args):
             "timing": "host wall clock around each whole call (prompt included), after one untimed call"}
 
 
+def measure_prefill(gf, cfg, glob, layers, prompt, args, dev):
+    """The 5-token prompt as one gf_prefill pass (one weight stream for all
+    rows) against 5 gf_decode_step calls, on the headline weights; CUDA
+    events on the launching stream, median of 10 after 3 untimed."""
+    import statistics as st
+    import torch
+    m = gf.Model(cfg, args.dtype, glob, layers)
+    kv = gf.KV(m, 64)
+    toks = torch.tensor([int(t) for t in prompt], dtype=torch.int32, device=dev)
+    pos = torch.zeros(1, dtype=torch.int32, device=dev)
+    nxt = torch.zeros(1, dtype=torch.int32, device=dev)
+    lg = torch.empty(cfg["vocab"], dtype=torch.float32, device=dev)
+
+    def run_prefill():
+        pos.zero_()
+        gf.prefill(m, kv, toks, pos, nxt)
+
+    def run_steps():
+        pos.zero_()
+        for i in range(len(prompt)):
+            gf.decode_step(m, kv, toks[i:i + 1], pos, lg, nxt)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return st.median(ts)
+
+    t_pre, t_steps = timed(run_prefill), timed(run_steps)
+    err = gf.device_error()
+    kv.close()
+    m.close()
+    return {"tokens": len(prompt), "weights": args.dtype, "prefill_ms": round(t_pre, 3),
+            "decode_steps_ms": round(t_steps, 3), "device_error": err}
+
+
 # ------------------------------------------------------------ our arm -----
 def run_ours(args):
     import numpy as np
@@ -502,6 +547,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     spec = measure_speculative(gf, cfg, glob, layers, prompt, args) if args.speculate else None
+    pre = measure_prefill(gf, cfg, glob, layers, prompt, args, dev) if args.prefill else None
     head = results[args.dtype]
     out = {
         "metric": METRIC,
@@ -539,6 +585,8 @@ def run_ours(args):
     }
     if spec is not None:
         out["speculative"] = spec
+    if pre is not None:
+        out["prefill"] = pre
     del layers, glob
     if rank == 0 and not args.no_cpu_baseline:
         # the token stream from the first timed position, stage by stage, for

@@ -259,6 +259,19 @@ int gf_decode_step_traced(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_
 int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t* d_pos,
                 int32_t* d_n_accepted, int32_t* d_next_token, float* d_logits, gf_stream stream);
 
+/* Batched prefill (gpt-fast README, "Generate text": the prompt before the
+ * first generated token): the n device tokens d_tokens are fed at positions
+ * *d_pos .. *d_pos + n - 1 in passes of up to 8 rows, each ONE stream of the
+ * weights (the verify pass with every row accepted): the K/V rows of all n
+ * positions are written and *d_pos advances by n on the device.  The argmax
+ * of the last row (the first generated token) goes to *d_next_token and, if
+ * d_logits is not NULL (16-byte aligned, [vocab] fp32), that row's logits.
+ * The result equals n gf_decode_step calls up to the accumulation order.
+ * n >= 1; *d_pos + n <= Tmax (a pass past the cache records
+ * GF_DEVERR_BAD_TOKEN and writes nothing, as gf_verify_k). */
+int gf_prefill(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int n, int32_t* d_pos,
+               int32_t* d_next_token, float* d_logits, gf_stream stream);
+
 /* Greedy generation (gpt-fast README, "Generate text", at batch size 1): the
  * n_prompt host tokens h_prompt are fed one per gf_decode_step from position
  * 0 of kv (earlier contents are overwritten), then n_new tokens are

@@ -61,6 +61,7 @@ def test_host_checks_reject_before_launch(L):
     assert L.gf_unpack_w4g(vp(16), 4, 64, 48, vp(16), vp(16), vp(16), None) == 5
     assert L.gf_kv_reset(None, None) == 1
     assert L.gf_generate(None, None, None, 1, 1, None, None) == 1
+    assert L.gf_prefill(None, None, None, 1, None, None, None, None) == 1
     assert L.gf_generate_speculative(None, None, None, None, None, 1, 1, 0, None, None, None) == 1
     ull = ctypes.c_ulonglong
     assert L.gf_gemv_bf16_gated(vp(16), vp(16), 64, 64, vp(16), 0, None, ull(10**6), None) == 1   # no gate

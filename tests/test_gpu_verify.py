@@ -129,3 +129,43 @@ def test_speculative_generation_equals_greedy(name, target, draft, k):
     tm.close()
     dm.close()
     assert gf.device_error() == 0
+
+
+@pytest.mark.parametrize("name,dtype,n", [("tiny", "int8", 5), ("tiny", "int4", 13), ("small", "bf16", 8),
+                                          ("tiny-moe", "int8", 11)])
+def test_prefill_matches_oracle_and_continues(name, dtype, n):
+    """gf_prefill feeds an n-token prompt in passes of up to 8 rows (one
+    weight stream each): the last row's logits match the oracle's forward of
+    the prompt, its argmax is the next token, the position advances by n,
+    and decoding from the rows it wrote matches the oracle's continuation."""
+    cfg = models.config(name)
+    wc = models.WeightCache(cfg, seed=25)
+    prompt = [int(t) for t in models.prompt(cfg, 25, n)]
+    om = oracle.OracleModel(cfg, dtype, wc, tmax=64)
+    ref = om.forward(prompt, 0)
+    m = build_model(cfg, dtype, wc)
+    kv = gf.KV(m, 64)
+    dev = torch.device("cuda")
+    toks = torch.tensor(prompt, dtype=torch.int32, device=dev)
+    pos = torch.zeros(1, dtype=torch.int32, device=dev)
+    nxt = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    lg = torch.empty(cfg["vocab"], dtype=torch.float32, device=dev)
+    gf.prefill(m, kv, toks, pos, nxt, lg)
+    assert int(pos.item()) == n
+    got = lg.cpu().numpy().astype(np.float64)
+    assert np.abs(got - ref[-1]).max() <= 2e-2 * ref[-1].std()
+    assert int(nxt.item()) == int(np.argmax(got))
+    # three decode steps on the prefilled cache against the oracle's
+    t = int(np.argmax(ref[-1]))
+    am = torch.empty(1, dtype=torch.int32, device=dev)
+    tok = torch.zeros(1, dtype=torch.int32, device=dev)
+    for step in range(3):
+        rref = om.forward([t], n + step)[0]
+        tok.fill_(t)
+        gf.decode_step(m, kv, tok, pos, lg, am)
+        g = lg.cpu().numpy().astype(np.float64)
+        assert np.abs(g - rref).max() <= 2e-2 * rref.std(), step
+        t = int(np.argmax(rref))
+    kv.close()
+    m.close()
+    assert gf.device_error() == 0

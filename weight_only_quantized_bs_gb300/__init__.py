@@ -62,6 +62,7 @@ def lib():
             "gf_kv_destroy": ([vp], i32),
             "gf_kv_reset": ([vp, vp], i32),
             "gf_generate": ([vp, vp, vp, i32, i32, vp, vp], i32),
+            "gf_prefill": ([vp, vp, vp, i32, vp, vp, vp, vp], i32),
             "gf_generate_speculative": ([vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp], i32),
             "gf_kv_cache_ptrs": ([vp, vp, vp], i32),
             "gf_decode_step": ([vp, vp, vp, vp, vp, vp, vp], i32),
@@ -335,6 +336,13 @@ class SpecStats(ctypes.Structure):
 def _host_ints(seq):
     arr = (ctypes.c_int32 * len(seq))(*[int(t) for t in seq])
     return arr
+
+
+def prefill(model, kv, tokens, pos, next_token, logits=None, stream=None):
+    """gf_prefill: tokens (device int32 [n]) at *pos.. in passes of up to 8
+    rows; pos advances by n; next_token <- argmax of the last row."""
+    _check(lib().gf_prefill(model.h, kv.h, _p(tokens), int(tokens.numel()), _p(pos), _p(next_token), _p(logits),
+                            _s(stream)), "gf_prefill")
 
 
 def generate(model, kv, prompt, n_new, stream=None):

@@ -1836,19 +1836,31 @@ __device__ bool gemv_phase_m(const Phase& ph, const Params& P, const Smem& S, Co
       // stage the round's inputs of the M rows, zero past K (one row per
       // iteration, whole warps of consecutive float4, so that group sums
       // shuffle within a warp)
-      for (int q0 = 0; q0 < M * PM; q0 += NCW * 32) {
-        const int q = q0 + cs.ctid, m = q / PM, f4 = q % PM;
-        const bool st = m < M, ok = st && b0 * (SK / 4) + f4 < K / 4;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ok) a = vin4(ph, P, V, m, e, b0 * (SK / 4) + f4);
+      constexpr int VB = 4;  // rows whose loads are in flight together
+      static_assert(PM == NCW * 32, "one staging pass per row");
+      for (int m0 = 0; m0 < M; m0 += VB) {
+        const int f4 = cs.ctid;
+        const bool inK = b0 * (SK / 4) + f4 < K / 4;
+        float4 a[VB];
+#pragma unroll
+        for (int r = 0; r < VB; ++r) {
+          a[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (m0 + r < M && inK) a[r] = vin4(ph, P, V, m0 + r, e, b0 * (SK / 4) + f4);
+        }
         const float4 mu = dq_mult(DT, f4 & 7);
-        if (st) reinterpret_cast<float4*>(V.xk)[m * PM + f4] = make_float4(a.x * mu.x, a.y * mu.y, a.z * mu.z, a.w * mu.w);
-        if (DT != DT_BF16) {  // group / chunk sums as in stage_store
-          float sg = a.x + a.y + a.z + a.w;
-          const int span = DT == DT_INT4 ? Gq / 4 : 4;
-          for (int o = 1; o < span; o <<= 1) sg += __shfl_xor_sync(0xffffffffu, sg, o);
-          if (st && (lane & (span - 1)) == 0)
-            V.xgk[m * 64 + (4 * f4) / (DT == DT_INT4 ? Gq : 16)] = sg * (DT == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
+#pragma unroll
+        for (int r = 0; r < VB; ++r) {
+          const int m = m0 + r;
+          if (m >= M) break;  // uniform
+          reinterpret_cast<float4*>(V.xk)[m * PM + f4] =
+              make_float4(a[r].x * mu.x, a[r].y * mu.y, a[r].z * mu.z, a[r].w * mu.w);
+          if (DT != DT_BF16) {  // group / chunk sums as in stage_store
+            float sg = a[r].x + a[r].y + a[r].z + a[r].w;
+            const int span = DT == DT_INT4 ? Gq / 4 : 4;
+            for (int o = 1; o < span; o <<= 1) sg += __shfl_xor_sync(0xffffffffu, sg, o);
+            if ((lane & (span - 1)) == 0)
+              V.xgk[m * 64 + (4 * f4) / (DT == DT_INT4 ? Gq : 16)] = sg * (DT == DT_INT4 ? DQ_DOWN : 128.0f * DQ_DOWN);
+          }
         }
       }
       if (!cta_sync(S, cs, P.err)) return false;
@@ -2006,7 +2018,9 @@ __device__ bool verify_finish(const Params& P, const Smem& S, Cons& cs, int cta,
         a[m] = g.i;
       }
       int n = 0;
-      while (n < P.M - 1 && a[n] == P.tokens[n + 1]) ++n;
+      if (P.prefill) n = P.M - 1;  // a prompt: every row is the caller's
+      else
+        while (n < P.M - 1 && a[n] == P.tokens[n + 1]) ++n;
       *P.n_accepted = n;
       *P.next_token = a[n];
       *P.amax_tick = 0u;

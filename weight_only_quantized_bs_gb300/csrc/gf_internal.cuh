@@ -115,7 +115,7 @@ __host__ __device__ inline void ffn_piece(const FfnSplit& s, int d, int w, int k
 }
 constexpr int MAX_GQ = 4;                    // q heads per kv head (GQA group)
 constexpr int MAX_M = 8;                     // rows of a verify pass
-constexpr int VTG = 4;                       // tiles per group of a multi-row GEMV phase
+constexpr int VTG = 8;                       // tiles per group of a multi-row GEMV phase
 
 // --------------------------------------------------------------- phases --
 // PH_FFN: a dense FFN in one phase -- the gate/up GEMV (rows interleaved) and,
@@ -246,6 +246,7 @@ struct Params {
   int M;               // rows of the pass (1 for a decode step)
   const int* tokens;   // [M] token ids (verify)
   int* n_accepted;     // verify outputs
+  int prefill;         // verify program as a prefill pass: every row accepted (n = M - 1)
   int* next_token;
   float* hbuf_moe;     // verify MoE: [MAX_M][8][ffn] SwiGLU outputs per row and expert
 };

@@ -41,6 +41,7 @@ struct gf_kv {
   float* part = nullptr;
   float* hmoe = nullptr;       // verify MoE: [MAX_M][8][ffn]
   float* vlogits = nullptr;    // verify: [MAX_M][vocab] when the caller passes no logits
+  int32_t* vscratch = nullptr; // [16] prefill: the pass's accepted count
   gf::Phase* vprog = nullptr;  // verify program
   int nvphases = 0;
   float* amax_val = nullptr;
@@ -264,6 +265,7 @@ int gf_kv_create(gf_model* m, int Tmax, gf_kv** out) {
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_val, (size_t)G * MAX_M * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->amax_idx, (size_t)G * MAX_M * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->vlogits, (size_t)MAX_M * c.vocab * 4))) break;
+    if ((rc = dev_alloc(kv->allocs, (void**)&kv->vscratch, 16 * sizeof(int32_t)))) break;
     if (c.n_experts && (rc = dev_alloc(kv->allocs, (void**)&kv->hmoe, (size_t)MAX_M * 8 * c.ffn * 4))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->counters, kv->counter_bytes))) break;
     if ((rc = dev_alloc(kv->allocs, (void**)&kv->prog, (size_t)nph * sizeof(Phase)))) break;
@@ -612,6 +614,10 @@ static int decode_launch(gf_model* m, gf_kv* kv, const int32_t* d_token, int32_t
   return launch_engine(p, kv->sms, true, s);
 }
 
+static int verify_launch(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t* d_pos,
+                         int32_t* d_n_accepted, int32_t* d_next_token, float* d_logits, int prefill,
+                         cudaStream_t stream);
+
 int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t* d_pos, int32_t* d_n_accepted,
                 int32_t* d_next_token, float* d_logits, gf_stream stream) {
   if (!m || !kv || kv->m != m || !d_tokens || !d_pos || !d_n_accepted || !d_next_token || k < 0 || k + 1 > MAX_M) {
@@ -622,7 +628,37 @@ int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t*
     set_error("gf_verify_k: logits must be 16-byte aligned");
     return GF_EALIGN;
   }
+  return verify_launch(m, kv, d_tokens, k, d_pos, d_n_accepted, d_next_token, d_logits, 0, (cudaStream_t)stream);
+}
+
+int gf_prefill(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int n, int32_t* d_pos, int32_t* d_next_token,
+               float* d_logits, gf_stream stream) {
+  if (!m || !kv || kv->m != m || !d_tokens || !d_pos || !d_next_token || n < 1) {
+    set_error("gf_prefill: bad arguments (n=%d)", n);
+    return GF_EINVAL;
+  }
+  if (d_logits && !aligned16(d_logits)) {
+    set_error("gf_prefill: logits must be 16-byte aligned");
+    return GF_EALIGN;
+  }
   cudaStream_t s = (cudaStream_t)stream;
+  // passes of up to MAX_M rows; the last pass's last row gives the next
+  // token and (if asked) the logits
+  for (int c0 = 0; c0 < n; c0 += MAX_M) {
+    const int M = n - c0 < MAX_M ? n - c0 : MAX_M;
+    const int rc = verify_launch(m, kv, d_tokens + c0, M - 1, d_pos, kv->vscratch, d_next_token, kv->vlogits, 1, s);
+    if (rc) return rc;
+    if (d_logits && c0 + M == n)
+      GF_CUDA(cudaMemcpyAsync(d_logits, kv->vlogits + (size_t)(M - 1) * m->cfg.vocab,
+                              (size_t)m->cfg.vocab * sizeof(float), cudaMemcpyDeviceToDevice, s));
+  }
+  return GF_OK;
+}
+
+static int verify_launch(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t* d_pos,
+                         int32_t* d_n_accepted, int32_t* d_next_token, float* d_logits, int prefill,
+                         cudaStream_t stream) {
+  cudaStream_t s = stream;
   GF_CUDA(cudaMemsetAsync(kv->counters, 0, kv->counter_bytes, s));
   Params p;
   memset(&p, 0, sizeof p);
@@ -647,6 +683,7 @@ int gf_verify_k(gf_model* m, gf_kv* kv, const int32_t* d_tokens, int k, int32_t*
   p.tokens = d_tokens;
   p.n_accepted = d_n_accepted;
   p.next_token = d_next_token;
+  p.prefill = prefill;
   p.hbuf_moe = kv->hmoe;
   if (!p.err) {
     set_error("gf_verify_k: cannot resolve the device error word");
