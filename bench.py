@@ -195,7 +195,8 @@ class OracleStream:
         self.x = None
 
     def stage(self):
-        """Runs the next stage; returns its seconds."""
+        """Runs the next stage; returns its seconds (the lm_head stage's
+        logits are kept in self.logits)."""
         import numpy as np
         import oracle
         cfg, om = self.cfg, self.om
@@ -207,7 +208,7 @@ class OracleStream:
         if s < cfg["n_layers"]:
             self.x = om.layer_forward(s, self.x, pos)
         else:
-            om.lm_head(np.stack([oracle.rmsnorm(self.x[0], self.wc.glob["g_final"], cfg["eps"])]))
+            self.logits = om.lm_head(np.stack([oracle.rmsnorm(self.x[0], self.wc.glob["g_final"], cfg["eps"])]))[0]
         dt = time.perf_counter() - t0
         self.i += 1
         return dt

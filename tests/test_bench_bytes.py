@@ -40,3 +40,28 @@ def test_llama2_7b_kv_bytes_per_position():
     # Llama-3.1-8B: 8 kv heads, 128 KiB per position
     cfg = models.config("llama3.1-8b")
     assert bench.decode_bytes(cfg, 0, 9, 1) == 11 * 128 * 1024
+
+
+def test_reference_arm_stages_are_the_oracle_decode():
+    """The reference arm's stage stream (one layer, or the final norm and
+    lm_head, per step) reproduces the oracle's own token-by-token decode: two
+    whole tokens from position 3 after a seeded 3-row context give the
+    logits of OracleModel.forward over the same cache."""
+    import numpy as np
+    import oracle
+    from synth import models
+    cfg = models.config("tiny")
+    st = bench.OracleStream(cfg, "int8", 7, 3, cfg["n_layers"])
+    got = []
+    for _ in range(2):
+        for _ in range(st.n_stages):
+            st.stage()
+        got.append(st.logits)
+    om = oracle.OracleModel(cfg, "int8", models.WeightCache(cfg, seed=7, keep=False), tmax=3 + 64)
+    for l in range(cfg["n_layers"]):
+        k, v = models.kv_prefill(cfg, 7, l, 3)
+        om.K[l][:, :3, :] = oracle.bf16_to_double(k)
+        om.V[l][:, :3, :] = oracle.bf16_to_double(v)
+    toks = [int(t) for t in models.prompt(cfg, 7, 64)[:2]]
+    ref = om.forward(toks, 3)
+    assert np.allclose(np.stack(got), ref, rtol=0, atol=1e-12)
