@@ -63,6 +63,7 @@ def parse():
                     help="also time the 5-token prompt as one gf_prefill pass against 5 decode steps")
     ap.add_argument("--only-headline", action="store_true", help="skip the other two weight dtypes")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--group", type=int, default=32, choices=[32, 64, 128], help="int4 group size along K")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="use only the first L layers (profiling runs)")
     return ap.parse_args()
@@ -218,7 +219,7 @@ def bench_config(args, cfg, tmax, p_first, ctxs):
     """The `config` object of both arms' JSON line (identical for one command)."""
     c = {"workload": "%s-shaped greedy decode, %s weights" % (args.workload, args.dtype),
          "shapes": args.workload, "n_layers": cfg["n_layers"],
-         "weights": args.dtype + ("-g32" if args.dtype == "int4" else ""),
+         "weights": args.dtype + ("-g%d" % args.group if args.dtype == "int4" else ""),
          "batch": 1, "prompt": 1 if ctxs else N_PROMPT, "tmax": tmax,
          "positions": [p_first, p_first + args.steps],
          "parallelism": "replicas" if args.gpus > 1 else "single",
@@ -423,7 +424,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     gf.lib()
-    cfg = models.config(args.workload)
+    cfg = models.config(args.workload, group=args.group)
     if args.layers:
         cfg["n_layers"] = args.layers
     tmax, p_first, ctxs = bench_positions(args)
@@ -695,7 +696,7 @@ def run_reference(args):
     if rank != 0:
         return
     from synth import models
-    cfg = models.config(args.workload)
+    cfg = models.config(args.workload, group=args.group)
     if args.layers:
         cfg["n_layers"] = args.layers
     tmax, p_first, ctxs = bench_positions(args)

@@ -112,6 +112,47 @@ def test_llama2_7b_teacher_forced(dtype):
     _check(got, ams, ref)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("group", [64, 128])
+def test_llama2_7b_int4_group_sizes(group):
+    """int4 with groups of 64 and 128 along K at the full Llama-2-7B shapes:
+    3 teacher-forced steps from position 0."""
+    cfg = models.config("llama2-7b", group=group)
+    wc = models.WeightCache(cfg, seed=35, keep=False)
+    tokens = list(models.prompt(cfg, 35, 3))
+    ref = oracle.OracleModel(cfg, "int4", wc, tmax=16, keep=False).forward(tokens, 0)
+    m = build_model(cfg, "int4", wc)
+    kv = gf.KV(m, 16)
+    got, ams = _decode(m, kv, cfg, tokens, 0)
+    kv.close()
+    m.close()
+    _check(got, ams, ref)
+
+
+@pytest.mark.slow
+def test_llama2_7b_prefill_bf16():
+    """gf_prefill of a 4-token prompt at the full Llama-2-7B shapes (one
+    multi-row pass): the last row's logits and argmax against the oracle's
+    forward of the prompt, and the position advanced by 4."""
+    cfg = models.config("llama2-7b")
+    wc = models.WeightCache(cfg, seed=36, keep=False)
+    tokens = [int(t) for t in models.prompt(cfg, 36, 4)]
+    ref = oracle.OracleModel(cfg, "bf16", wc, tmax=16, keep=False).forward(tokens, 0)[-1]
+    m = build_model(cfg, "bf16", wc)
+    kv = gf.KV(m, 16)
+    dev = torch.device("cuda")
+    toks = torch.tensor(tokens, dtype=torch.int32, device=dev)
+    pos = torch.zeros(1, dtype=torch.int32, device=dev)
+    nxt = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    lg = torch.empty(cfg["vocab"], dtype=torch.float32, device=dev)
+    gf.prefill(m, kv, toks, pos, nxt, lg)
+    got = lg.cpu().numpy().astype(np.float64)
+    kv.close()
+    m.close()
+    assert int(pos.item()) == 4
+    _check(got[None, :], [int(nxt.item())], ref[None, :])
+
+
 def _write_rows(kv, cfg, tmax, l, k, v, r0, r1):
     """Rows [r0, r1) of layer l's K and V caches (bf16 [Hkv][tmax][hd]) from
     the host arrays k, v ([Hkv][>= r1][hd]), one copy per head."""

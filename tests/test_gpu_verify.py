@@ -100,7 +100,7 @@ def test_verify_k0_is_a_decode_step():
 
 
 @pytest.mark.parametrize("name,target,draft,k", [("tiny", "bf16", "int4", 4), ("small", "int8", "int4", 3),
-                                                 ("tiny", "int8", "int8", 7)])
+                                                 ("tiny", "int8", "int8", 7), ("tiny-moe", "int8", "int4", 3)])
 def test_speculative_generation_equals_greedy(name, target, draft, k):
     """gf_generate_speculative (a draft copy of the same seeded model in
     another weight type proposes k tokens, the target verifies) emits exactly
