@@ -1128,12 +1128,13 @@ __device__ bool osplit_phase(const Phase& ph, const Params& P, const Smem& S, Co
     const uint32_t it = cs.it + (uint32_t)k;
     if ((int)(it % NCW) != w) continue;
     const int u = first + k * G, lt = u / nb, b = u % nb;
-    int ok = 1;
-    if (lane == 0) {
-      const int h0 = b * SK / ph.hd, h1 = min((b * SK + SK - 1) / ph.hd, ph.Hq - 1);
-      for (int g = h0 / gq; g <= h1 / gq && ok; ++g) ok = counter_wait(ph.attd + g, 1u, P.err, ERR_WAIT_HEAD, cs.lim);
-    }
-    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    // the kv groups of the slot's heads, one lane each, polled together
+    const int h0 = b * SK / ph.hd, h1 = min((b * SK + SK - 1) / ph.hd, ph.Hq - 1);
+    const int g = h0 / gq + lane;
+    const bool mine = g <= h1 / gq;
+    const bool ok = !mine || counter_wait(ph.attd + g, 1u, P.err, ERR_WAIT_HEAD, cs.lim);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    __syncwarp();  // the polling lanes' acquires order every lane's reads below
     // inputs b*SK .. b*SK + SK - 1: lane l holds PL consecutive ones
     float sg = 0.f;
 #pragma unroll
@@ -1393,13 +1394,13 @@ __device__ __forceinline__ void attn_rows(AttnRows<HD, NP>& r, const uint16_t* R
 // lane's dims of each head, pre-scaled by 1/sqrt(HD)); updates m and l and
 // returns in pr[jj] the probability of position lane/2 (0 past np) and in
 // cr[jj] the factor that rescales the head's running output.
-template <int HD, int NP>
+template <int HD, int NP, int NG>
 __device__ __forceinline__ void attn_scores(const AttnRows<HD, NP>& kr, int np, int gq, const float (*q)[HD / 32],
                                             float* m, float* l, float* pr, float* cr, int lane) {
   constexpr int DPL = HD / 32;
   const bool valid = (lane >> 1) < np;
 #pragma unroll
-  for (int jj = 0; jj < MAX_GQ; ++jj) {
+  for (int jj = 0; jj < NG; ++jj) {
     pr[jj] = 0.f;
     cr[jj] = 1.f;
     if (jj < gq) {
@@ -1433,12 +1434,12 @@ __device__ __forceinline__ void attn_scores(const AttnRows<HD, NP>& kr, int np, 
   }
 }
 // o = o * cr + sum_i pr_i v_i for each head (V rows vr).
-template <int HD, int NP>
+template <int HD, int NP, int NG>
 __device__ __forceinline__ void attn_values(const AttnRows<HD, NP>& vr, int gq, const float* pr, const float* cr,
                                             float (*o)[HD / 32]) {
   constexpr int DPL = HD / 32;
 #pragma unroll
-  for (int jj = 0; jj < MAX_GQ; ++jj) {
+  for (int jj = 0; jj < NG; ++jj) {
     if (jj < gq) {
 #pragma unroll
       for (int d = 0; d < DPL; ++d) o[jj][d] *= cr[jj];
@@ -1465,7 +1466,10 @@ __device__ __forceinline__ bool attn_done(const Phase& ph, const Smem& S, Cons& 
   return true;
 }
 
-template <int HD, bool VER>
+// NG: the largest number of q heads per kv head this copy handles (1, 2 or
+// 4); the per-head loops and registers are sized by it, so a model with one
+// q head per kv head runs a quarter of the code.
+template <int HD, int NG, bool VER>
 __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons& cs, const AttnUnit& au, int pos,
                           uint32_t& j) {
   constexpr int DPL = HD / 32;
@@ -1511,9 +1515,9 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
   }
   if (!cta_sync(S, cs, P.err)) return false;
 
-  float q[MAX_GQ][DPL], m[MAX_GQ], l[MAX_GQ], o[MAX_GQ][DPL];
+  float q[NG][DPL], m[NG], l[NG], o[NG][DPL];
 #pragma unroll
-  for (int jj = 0; jj < MAX_GQ; ++jj) {
+  for (int jj = 0; jj < NG; ++jj) {
     m[jj] = -INFINITY;
     l[jj] = 0.f;
 #pragma unroll
@@ -1522,10 +1526,10 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
       o[jj][d] = 0.f;
     }
   }
-  float pr[MAX_GQ], cr[MAX_GQ];
+  float pr[NG], cr[NG];
   if (has_g) {
-    attn_scores<HD, NPG>(gk, p1 - pg, gq, q, m, l, pr, cr, lane);
-    attn_values<HD, NPG>(gv, gq, pr, cr, o);
+    attn_scores<HD, NPG, NG>(gk, p1 - pg, gq, q, m, l, pr, cr, lane);
+    attn_values<HD, NPG, NG>(gv, gq, pr, cr, o);
   }
   for (int k = (w - (int)((cs.it + j) % NCW) + NCW) % NCW; k < nslots; k += NCW) {
     const uint32_t it = cs.it + j + (uint32_t)k;
@@ -1536,19 +1540,19 @@ __device__ bool attn_unit(const Phase& ph, const Params& P, const Smem& S, Cons&
     {
       AttnRows<HD, APS> kr;
       attn_rows<HD, APS, false>(kr, kb, np, lane);
-      attn_scores<HD, APS>(kr, np, gq, q, m, l, pr, cr, lane);
+      attn_scores<HD, APS, NG>(kr, np, gq, q, m, l, pr, cr, lane);
     }
     {
       AttnRows<HD, APS> vr;
       attn_rows<HD, APS, false>(vr, kb + APS * HD, np, lane);
       slot_release(S, cs, it);  // the slot's rows are in registers
-      attn_values<HD, APS>(vr, gq, pr, cr, o);
+      attn_values<HD, APS, NG>(vr, gq, pr, cr, o);
     }
   }
   j += (uint32_t)nslots;
   // the warps of this CTA merge in shared memory
 #pragma unroll
-  for (int jj = 0; jj < MAX_GQ; ++jj) {
+  for (int jj = 0; jj < NG; ++jj) {
     if (jj < gq) {
       float* dst = sc + (w * gq + jj) * (HD + 2);
 #pragma unroll
@@ -1623,11 +1627,11 @@ struct AttnRet {
   uint32_t j, cphase, starved;
   int ok;
 };
-template <int HD, bool VER>
+template <int HD, int NG, bool VER>
 __device__ __noinline__ AttnRet attn_call(const Phase& ph, const Params& P, const Smem S, Cons cs, const AttnUnit au,
                                           int pos, uint32_t j) {
   AttnRet r;
-  r.ok = attn_unit<HD, VER>(ph, P, S, cs, au, pos, j);
+  r.ok = attn_unit<HD, NG, VER>(ph, P, S, cs, au, pos, j);
   r.j = j;
   r.cphase = cs.cphase;
   r.starved = cs.starved;
@@ -2236,8 +2240,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
       for (int u = first_unit(cta, ph.rot, G); u < nunits; u += G) {
         AttnUnit au;
         attn_units(ph, P, pos, u, &au);
-        const AttnRet r = ph.hd == 128 ? attn_call<128, VER>(ph, P, S, cs, au, pos, j)
-                                       : attn_call<64, VER>(ph, P, S, cs, au, pos, j);
+        const int gq = ph.Hq / ph.Hkv;
+        const AttnRet r =
+            ph.hd == 128 ? (gq == 1   ? attn_call<128, 1, VER>(ph, P, S, cs, au, pos, j)
+                            : gq == 2 ? attn_call<128, 2, VER>(ph, P, S, cs, au, pos, j)
+                                      : attn_call<128, MAX_GQ, VER>(ph, P, S, cs, au, pos, j))
+                         : (gq == 1   ? attn_call<64, 1, VER>(ph, P, S, cs, au, pos, j)
+                            : gq == 2 ? attn_call<64, 2, VER>(ph, P, S, cs, au, pos, j)
+                                      : attn_call<64, MAX_GQ, VER>(ph, P, S, cs, au, pos, j));
         j = r.j;
         cs.cphase = r.cphase;
         cs.starved = r.starved;
