@@ -2003,24 +2003,35 @@ __device__ bool verify_finish(const Params& P, const Smem& S, Cons& cs, int cta,
     }
   }
   if (!cta_sync(S, cs, P.err)) return false;
-  if (cs.ctid == 0) {
-    for (int m = 0; m < P.M; ++m) {
-      ArgMax b = {S.red[m], S.bcast[64 + m]};
-      for (int w = 1; w < NCW; ++w) amax_merge(b, S.red[w * MAX_M + m], S.bcast[64 + w * MAX_M + m]);
-      P.amax_val[cta * MAX_M + m] = b.v;
-      P.amax_idx[cta * MAX_M + m] = b.i;
+  if (cs.warp == 0) {
+    int last = 0;
+    if (cs.lane == 0) {
+      for (int m = 0; m < P.M; ++m) {
+        ArgMax b = {S.red[m], S.bcast[64 + m]};
+        for (int w = 1; w < NCW; ++w) amax_merge(b, S.red[w * MAX_M + m], S.bcast[64 + w * MAX_M + m]);
+        P.amax_val[cta * MAX_M + m] = b.v;
+        P.amax_idx[cta * MAX_M + m] = b.i;
+      }
+      __threadfence();
+      last = atomicAdd(P.amax_tick, 1u) == (unsigned)(P.nctas - 1);
     }
-    __threadfence();
-    const unsigned old = atomicAdd(P.amax_tick, 1u);
-    if (old == (unsigned)(P.nctas - 1)) {
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      // the last CTA merges every CTA's candidates: 32 lanes load in parallel
       __threadfence();
       int a[MAX_M];
       for (int m = 0; m < P.M; ++m) {
         ArgMax g = {-INFINITY, 0x7fffffff};
-        for (int k = 0; k < P.nctas; ++k)
+        for (int k = cs.lane; k < P.nctas; k += 32)
           amax_merge(g, __ldcg(P.amax_val + k * MAX_M + m), __ldcg(P.amax_idx + k * MAX_M + m));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float v = __shfl_xor_sync(0xffffffffu, g.v, o);
+          const int i = __shfl_xor_sync(0xffffffffu, g.i, o);
+          amax_merge(g, v, i);
+        }
         a[m] = g.i;
       }
+      if (cs.lane == 0) {
       int n = 0;
       if (P.prefill) n = P.M - 1;  // a prompt: every row is the caller's
       else
@@ -2030,6 +2041,7 @@ __device__ bool verify_finish(const Params& P, const Smem& S, Cons& cs, int cta,
       *P.amax_tick = 0u;
       int* pos = const_cast<int*>(P.d_pos);
       *pos = *pos + n + 1;
+      }
     }
   }
   return true;
@@ -2090,20 +2102,32 @@ __device__ bool argmax_finish(const Params& P, const Smem& S, Cons& cs, int cta,
     S.bcast[cs.warp] = am.i;
   }
   if (!cta_sync(S, cs, P.err)) return false;
-  if (cs.ctid == 0) {
-    ArgMax b = {S.red[0], S.bcast[0]};
-    for (int w = 1; w < NCW; ++w) amax_merge(b, S.red[w], S.bcast[w]);
-    P.amax_val[cta] = b.v;
-    P.amax_idx[cta] = b.i;
-    __threadfence();
-    const unsigned old = atomicAdd(P.amax_tick, 1u);
-    if (old == (unsigned)(P.nctas - 1)) {
+  if (cs.warp == 0) {
+    int last = 0;
+    if (cs.lane == 0) {
+      ArgMax b = {S.red[0], S.bcast[0]};
+      for (int w = 1; w < NCW; ++w) amax_merge(b, S.red[w], S.bcast[w]);
+      P.amax_val[cta] = b.v;
+      P.amax_idx[cta] = b.i;
+      __threadfence();
+      last = atomicAdd(P.amax_tick, 1u) == (unsigned)(P.nctas - 1);
+    }
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      // the last CTA merges every CTA's candidate: 32 lanes load in parallel
       __threadfence();
       ArgMax g = {-INFINITY, 0x7fffffff};
-      for (int k = 0; k < P.nctas; ++k) amax_merge(g, __ldcg(P.amax_val + k), __ldcg(P.amax_idx + k));
-      *P.argmax = g.i;
-      *P.amax_tick = 0u;
-      if (P.pos_inc) *P.pos_inc = *P.pos_inc + 1;
+      for (int k = cs.lane; k < P.nctas; k += 32) amax_merge(g, __ldcg(P.amax_val + k), __ldcg(P.amax_idx + k));
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float v = __shfl_xor_sync(0xffffffffu, g.v, o);
+        const int i = __shfl_xor_sync(0xffffffffu, g.i, o);
+        amax_merge(g, v, i);
+      }
+      if (cs.lane == 0) {
+        *P.argmax = g.i;
+        *P.amax_tick = 0u;
+        if (P.pos_inc) *P.pos_inc = *P.pos_inc + 1;
+      }
     }
   }
   return true;
