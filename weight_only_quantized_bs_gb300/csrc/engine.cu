@@ -1102,6 +1102,14 @@ __device__ bool gemv_phase(const Phase& ph, const Params& P, const Smem& S, Cons
     const int n = lt * TR + lane;
     const float yp = __shfl_xor_sync(0xffffffffu, tot, 1);
     if (n < Ns) gemv_epilogue(ph, P, S, seg, n, tot, yp, pos, rp, am);
+    if (ph.headc) {
+      // this tile's q/k/v rows are written: release them to the tile's kv
+      // group (the warp barrier orders every lane's stores before lane 0's
+      // release, so the waiting attention unit's acquire sees them all)
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ph.headc + qkv_group(ph, lt)) : "memory");
+    }
   }
   cs.it += j;
   return true;
@@ -2290,20 +2298,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_engine(const __grid_constant__ 
     if (tid < PH16) cp_async_wait_all();  // the next phase's descriptor has landed
     // Past the barrier below, lanes of warp 0 may start the next phase and
     // overwrite this descriptor's buffer with the one after it: what is read
-    // of it later is read before, or by all of warp 0 before a __syncwarp.
+    // of it later is read before the barrier.
     const int sbar = ph.signal_bar;
-    const bool qkv_signal = ph.headc != nullptr && ph.kind == PH_GEMV;
     // every warp of this CTA has finished the phase (its global writes made)
     if (!cta_sync(S, cs, P.err)) return;
-    if (qkv_signal && warp == 0) {
-      // the q/k/v rows of this CTA's tiles are in memory: count them for their
-      // kv groups, one lane per local tile, each after a fence
-      __threadfence();
-      const int tps = (ph.N + TR - 1) / TR;
-      for (int t = first_unit(cta, ph.rot, G) + lane * G; t < tps; t += 32 * G)
-        atomicAdd(ph.headc + qkv_group(ph, t), 1u);
-      __syncwarp();
-    }
     if (sbar >= 0 && tid == 0) grid_arrive(P.bars + sbar);
     if (tr) tr[4] = gtimer();
   }
