@@ -1466,11 +1466,11 @@ __device__ __forceinline__ void attn_values(const AttnRows<HD, NP>& vr, int gq, 
 
 // The outputs of kv group kvh's heads are written (by this CTA's threads):
 // publish that for the o projection units waiting on the group (PH_OSPLIT).
+// The CTA barrier orders every thread's stores before thread 0's release.
 __device__ __forceinline__ bool attn_done(const Phase& ph, const Smem& S, Cons& cs, const Params& P, int kvh) {
   if (!ph.attd) return true;
-  __threadfence();
   if (!cta_sync(S, cs, P.err)) return false;
-  if (cs.ctid == 0) atomicAdd(ph.attd + kvh, 1u);
+  if (cs.ctid == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ph.attd + kvh) : "memory");
   return true;
 }
 
